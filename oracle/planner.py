@@ -1,0 +1,91 @@
+"""Reference for the split planner (test infrastructure only).
+
+Two things live here, both written plainly so they can be read against their
+sources:
+
+1. The pages' own split heuristic and grid arithmetic ("Kimi K3 decode on 2x8
+   B200: DP16 vs DP2 x DCP8", section "MLA: bytes conserved, DP16 kernel slowed
+   by wave quantisation"): split = min(148 // B // (q_len * 2), 32), with the
+   floor of 1 that the same paragraph implies ("split = 1 for B >= 8"), and the
+   grid (2, B * q_len, split) on 148 SMs.
+
+2. A brute-force statement of this library's wave-rounding objective, the
+   one the C planner must reproduce exactly:
+     units       one CTA pair per (virtual request v, split s, row group g),
+                 launched in that order (g fastest), G = ceil(H*q_len / 128)
+     unit cost   pages(v, s) + c0 page-tiles, where request v's P_v =
+                 ceil(L_v / 64) pages are dealt to splits as
+                 floor((s+1) P_v / S) - floor(s P_v / S)
+     makespan    list scheduling of the units, in launch order, onto `slots`
+                 pair slots (each unit starts on the slot that frees first)
+     objective   J(S) = makespan(S) + lam * S * rows / 1024, rows = V*q_len*H
+                 (the partial outputs each extra split writes and re-reads)
+     choice      the S in [1, S_max] with the smallest J; ties go to fewer
+                 splits.  Wave efficiency = sum(unit costs) / (slots *
+                 makespan).
+"""
+from __future__ import annotations
+
+import heapq
+from typing import List, Sequence, Tuple
+
+PAGES_SMS = 148          # B200 SM count used by the pages' heuristic
+ROWS_PER_GROUP = 128     # query rows per CTA pair (one tensor-core M tile)
+
+
+def pages_heuristic_split(B: int, q_len: int, sms: int = PAGES_SMS) -> int:
+    """The pages' split rule, with the implied floor of one split."""
+    return max(1, min(sms // B // (q_len * 2), 32))
+
+
+def pages_grid(B: int, q_len: int, split: int) -> Tuple[int, int, int]:
+    """The pages' grid (2, B * q_len, split) for the M128 2-CTA path."""
+    return (2, B * q_len, split)
+
+
+def pages_waves(B: int, q_len: int, split: int, sms: int = PAGES_SMS):
+    """CTAs of the pages' grid and how many waves they take on `sms` SMs."""
+    x, y, z = pages_grid(B, q_len, split)
+    ctas = x * y * z
+    return ctas, ctas / sms
+
+
+def split_pages(P: int, S: int, s: int) -> int:
+    return (s + 1) * P // S - s * P // S
+
+
+def makespan(costs: Sequence[float], slots: int) -> float:
+    heap = [0.0] * min(slots, max(1, len(costs)))
+    heapq.heapify(heap)
+    end = 0.0
+    for c in costs:
+        t = heapq.heappop(heap) + c
+        end = max(end, t)
+        heapq.heappush(heap, t)
+    return end
+
+
+def unit_costs(seq_lens: Sequence[int], H: int, q_len: int, S: int,
+               c0: float, page: int = 64) -> List[float]:
+    G = -(-H * q_len // ROWS_PER_GROUP)
+    out = []
+    for L in seq_lens:
+        P = -(-L // page)
+        for s in range(S):
+            c = split_pages(P, S, s) + c0
+            out.extend([c] * G)
+    return out
+
+
+def plan(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
+         s_max: int = 64, c0: float = 4.0, lam: float = 1.0):
+    """Brute-force planner: returns (S, wave_efficiency, makespan)."""
+    rows = len(seq_lens) * q_len * H
+    best = None
+    for S in range(1, s_max + 1):
+        costs = unit_costs(seq_lens, H, q_len, S, c0)
+        ms = makespan(costs, slots)
+        J = ms + lam * S * rows / 1024.0
+        if best is None or J < best[0] - 1e-9:
+            best = (J, S, sum(costs) / (slots * ms), ms)
+    return best[1], best[2], best[3]
