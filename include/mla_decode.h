@@ -1,0 +1,244 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA latent-decode library.
+ *
+ * The library computes weight-absorbed multi-head latent attention (MLA)
+ * decode with MTP verification over a paged latent KV cache, as split-KV
+ * flash-decoding: one launch writes a partial (O, LSE) per KV split (and per
+ * context shard), a second launch merges the partials by LSE.
+ *
+ * Pages that define the operations (cited by title and section):
+ *   [VRAM-KV]  "Resident VRAM: weights and KV cache" (zdszero.github.io),
+ *              section "KV 账：每 token 字节由注意力架构决定" (KV ledger): the MLA
+ *              cache stores one latent row per token of kv_lora_rank (512,
+ *              c_kv) + qk_rope_head_dim (64, RoPE key) elements, no head dim.
+ *   [VRAM-POOL] same page, sections "cell_size：每 token 字节的代码形态" and
+ *              "req_to_token 的大小从哪来": the per-layer pool is
+ *              (size + page_size, 1, 576); req_to_token is an int32 2-D table
+ *              [requests, context] from token index to pool slot.
+ *   [K3-MLA]   "Kimi K3 decode on 2x8 B200: DP16 vs DP2 x DCP8"
+ *              (zdszero.github.io), section "MLA：字节守恒，但 DP16 的 kernel 被
+ *              wave 量化拖慢" (MLA: bytes conserved, the DP16 kernel is slowed
+ *              by wave quantisation): the decode kernel's split count and grid,
+ *              the partial (O, LSE) exchange and the LSE combine
+ *              (dcp_lse_combine), 96 heads with replicated Q on every shard.
+ *   [K3-SPLIT] same page, section "问题：同样 16 张卡、同样的并发，按什么切": the
+ *              latent KV split token-interleaved, slot p on shard p % 8.
+ *   [K3-INTRO] same page, opening paragraphs: 5 tokens verified per request
+ *              per step (q_len = 5, causal among the draft tokens).
+ *   [K3-MEM]   same page, section "显存：固定开销决定状态池有多大": 96 heads, qk
+ *              head dim 192 (128 nope + 64 rope), absorbed query 512-d.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device memory owned by the caller; host
+ *     pointers are marked "host".  The library allocates nothing, keeps no
+ *     per-call state and never frees caller memory.
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
+ *     checked on the host before anything is launched; on error nothing is
+ *     launched and mla_last_error_string() (thread-local) says why.
+ *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Problems found on the device (a bounded wait
+ *     that gave up, a sequence length beyond the page table) are OR-ed as
+ *     MLA_STATUS_* bits into the optional device word `status`, which the
+ *     caller zeroes and reads back.
+ *   - Query row order is the flat [B, q_len, H] order: row r = (b*q_len+i)*H+h.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* same type as cudaStream_t */
+
+enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1, /* null pointer, bad size or count */
+  MLA_ERR_UNSUPPORTED = -2, /* valid but not built (e.g. page_size != 64) */
+  MLA_ERR_MISALIGNED = -3,  /* a pointer breaks the stated alignment */
+  MLA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+  MLA_ERR_PAGE_TABLE = -5   /* mla_check_page_table found a bad entry */
+};
+
+/* Bits OR-ed into the device status word by the kernels. */
+enum {
+  MLA_STATUS_WAIT_TIMEOUT = 1, /* a bounded pipeline wait gave up; outputs of
+                                  that CTA are incomplete */
+  MLA_STATUS_BAD_LENGTH = 2,   /* a sequence length exceeded the page table
+                                  stride and was clamped */
+  MLA_STATUS_BAD_SLOT = 4      /* a page's slot run lay outside the pool; its
+                                  rows were read as zeros */
+};
+
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+
+/* Latent row geometry ([VRAM-KV], [K3-MEM]). */
+#define MLA_ROW_DIM 576   /* kv_lora_rank + qk_rope_head_dim */
+#define MLA_NOPE_DIM 512  /* kv_lora_rank: c_kv, also the value */
+#define MLA_ROPE_DIM 64   /* qk_rope_head_dim */
+#define MLA_VALUE_DIM 512
+#define MLA_PAGE_SIZE 64  /* the only page size the kernels are built for */
+#define MLA_ROWS_PER_PAIR 128 /* query rows one CTA pair owns */
+
+/* Last error message of this thread ("" if none).  Owned by the library. */
+const char* mla_last_error_string(void);
+
+/* SM count of `device` (cudaDevAttrMultiProcessorCount), or a negative
+ * MLA_ERR_* code. */
+int mla_num_sms(int device);
+
+/* Number of CTA pairs of the decode kernel that can be resident at once on
+ * the current device (cudaOccupancyMaxActiveClusters with the kernel's
+ * cluster size, block size and shared memory), or a negative MLA_ERR_*. */
+int mla_pair_slots(void);
+
+/*
+ * The pages' split rule, reproduced for comparison ([K3-MLA]):
+ *   split = max(1, min(148 // B // (q_len * 2), 32)).
+ * The floor of 1 is implied by the same paragraph ("split = 1 for B >= 8").
+ * Returns the split count, or MLA_ERR_INVALID_ARG for B < 1 or q_len < 1.
+ */
+int mla_plan_heuristic(int B, int q_len);
+
+/*
+ * Wave-rounding split planner (replaces the rule above; [K3-MLA] shows that
+ * rule leaving a partial second wave).  Work units are CTA pairs, one per
+ * (virtual request v, split s, row group g) with G = ceil(H*q_len / 128) row
+ * groups, launched in that order.  For every S in [1, s_max] the unit costs
+ * pages(v, s) + c0 page tiles, where request v's P_v = ceil(L_v / 64) pages
+ * are dealt as floor((s+1) P_v / S) - floor(s P_v / S); the units are list-
+ * scheduled onto `slots` pair slots in launch order; the objective is
+ *   J(S) = makespan(S) + lam * S * rows / 1024,   rows = V * q_len * H,
+ * (the second term prices the partial outputs each extra split writes and
+ * the combine re-reads).  The smallest J wins, ties go to fewer splits.
+ *   seq_lens_host  host int32 [V] (V = num_shards * B virtual requests)
+ *   slots          concurrent pair slots (> 0)
+ *   s_max          largest split count considered (1..1024)
+ *   num_splits_out chosen S;  wave_eff_out: sum(unit cost)/(slots*makespan);
+ *   makespan_out   makespan in page tiles (may be NULL)
+ */
+int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
+                int slots, int s_max, double c0, double lam,
+                int* num_splits_out, float* wave_eff_out,
+                double* makespan_out);
+
+/*
+ * mla_plan_ex with the library's defaults: slots = mla_pair_slots() when
+ * num_sms == 0, else num_sms / 2; s_max = 64; c0 = 4; lam = 1.
+ *   B, num_shards  requests and context shards (V = B * num_shards);
+ *   seq_lens_host  host int32 [num_shards * B] (shard-local lengths).
+ */
+int mla_plan(int B, int q_len, int H, int num_shards,
+             const int32_t* seq_lens_host, int num_sms, int* num_splits_out,
+             float* wave_eff_out);
+
+/*
+ * Host-side check of a page table (optional validation mode).  All
+ * pointers are HOST copies.  Checks, for every virtual request v < V:
+ * 1 <= q_len; 0 <= seq_lens[v] <= stride; without kv_limit seq_lens[v] >=
+ * q_len; with kv_limit 0 <= kv_limit[v, i] <= seq_lens[v]; every entry
+ * t < seq_lens[v] is a slot in [0, num_slots); every page is one contiguous,
+ * page-aligned run: req_to_token[v, t] == req_to_token[v, 64*(t/64)] + t%64
+ * and req_to_token[v, 64*(t/64)] % 64 == 0.  The decode kernels read only the
+ * first entry of each page and rely on these properties.
+ * Returns MLA_OK or MLA_ERR_PAGE_TABLE / MLA_ERR_INVALID_ARG with a message.
+ */
+int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
+                         const int32_t* seq_lens_host,
+                         const int32_t* kv_limit_host, int V, int q_len,
+                         int page_size, int64_t num_slots);
+
+/*
+ * Partial decode ([VRAM-KV], [K3-MLA], [K3-SPLIT], [K3-INTRO]): for every
+ * split s, shard c, request b, query i, head h (row r = (b*q_len+i)*H+h,
+ * virtual request v = c*B + b), over the tokens of split s of v's page list
+ * that query i may see (t < kv_limit[v, i], or t <= seq_lens[v] - q_len + i
+ * when kv_limit is NULL):
+ *   x    = [q_nope_absorbed[b,i,h,:512] ; q_rope[b,i,h,:64]]
+ *   k_t  = kv_pages[req_to_token[v, t], :576]  (FP8: bytes * kv_scale[slot])
+ *   s_t  = sm_scale * <x, k_t>
+ *   LSE_part[s,c,b,i,h] = ln sum_t exp(s_t)            (-inf if no token)
+ *   O_part[s,c,b,i,h,:] = sum_t exp(s_t - LSE) k_t[:512] (0 if no token)
+ * Split s of a request with P pages covers pages [s*P/S, (s+1)*P/S).
+ *
+ *   q_nope_absorbed  bf16 [B, q_len, H, 512], contiguous, 16-B aligned
+ *   q_rope           bf16 [B, q_len, H, 64], contiguous, 16-B aligned
+ *   kv_pages         [num_slots, 576]: bf16 (1152-B rows) or E4M3 bytes
+ *                    (576-B rows); 16-B aligned; num_slots >= page_size
+ *   kv_scale         fp32 [num_slots] (FP8), NULL for BF16
+ *   req_to_token     int32 [num_shards*B, r2t_stride]; only the entry of the
+ *                    first token of each page is read (see
+ *                    mla_check_page_table for the contract)
+ *   seq_lens         int32 [num_shards*B], device; counts the q_len draft
+ *                    tokens already in the cache
+ *   kv_limit         int32 [num_shards*B, q_len] or NULL
+ *   num_shards       token-interleaved context shards sharing one Q (1 = none)
+ *   page_size        must be 64 (else MLA_ERR_UNSUPPORTED)
+ *   num_splits       KV splits per request, >= 1 (see mla_plan)
+ *   O_part           fp32 [num_splits, num_shards, B, q_len, H, 512], 16-B al.
+ *   LSE_part         fp32 [num_splits, num_shards, B, q_len, H]
+ *   status           device int or NULL (MLA_STATUS_* bits are OR-ed in)
+ * Rows of slots beyond a request's length (the tail of its last page) are
+ * never used, whatever they hold.
+ */
+int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
+                       const void* kv_pages, const float* kv_scale,
+                       mla_kv_dtype kv_dtype, int64_t num_slots,
+                       const int32_t* req_to_token, int64_t r2t_stride,
+                       const int32_t* seq_lens, const int32_t* kv_limit,
+                       int B, int q_len, int H, int num_shards, int page_size,
+                       float sm_scale, int num_splits, float* O_part,
+                       float* LSE_part, int* status, mla_stream_t stream);
+
+/*
+ * The same computation on plain CUDA cores (no tensor cores, no TMA): a
+ * slow, simple GPU kernel kept to cross-check the tensor-core path and to
+ * cover shapes it does not take.  Same arguments and outputs.
+ */
+int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
+                            const void* kv_pages, const float* kv_scale,
+                            mla_kv_dtype kv_dtype, int64_t num_slots,
+                            const int32_t* req_to_token, int64_t r2t_stride,
+                            const int32_t* seq_lens, const int32_t* kv_limit,
+                            int B, int q_len, int H, int num_shards,
+                            int page_size, float sm_scale, int num_splits,
+                            float* O_part, float* LSE_part, int* status,
+                            mla_stream_t stream);
+
+/*
+ * LSE combine ([K3-MLA], dcp_lse_combine): for each of `rows` rows, over the
+ * num_parts partials (part j at O_part + j*rows*512, LSE_part + j*rows):
+ *   M = max_j LSE_j; w_j = exp(LSE_j - M) (parts with LSE = -inf skipped);
+ *   out = sum_j w_j O_j / sum_j w_j;  lse_out = M + ln sum_j w_j.
+ * All parts empty: out = 0, lse_out = -inf.
+ *   O_part   fp32 [num_parts, rows, 512], 16-B aligned
+ *   LSE_part fp32 [num_parts, rows]
+ *   out      bf16 [rows, 512] (round to nearest even), 16-B aligned
+ *   lse_out  fp32 [rows] or NULL
+ * With mla_decode_partial's layout, num_parts = num_splits * num_shards and
+ * rows = B * q_len * H.
+ */
+int mla_lse_combine(const float* O_part, const float* LSE_part, int num_parts,
+                    int64_t rows, void* out, float* lse_out,
+                    mla_stream_t stream);
+
+/*
+ * Page-table gather through the decode kernel's own TMA path (for the
+ * bit-exact test of the gather): copies the raw bytes of token t's row,
+ * kv_pages[req_to_token[v, t]], for t < seq_lens[v], into
+ * dense_out[row_offset[v] + t, :].
+ *   row_offset  int64 [V] device, the first dense row of each request
+ *   dense_out   [sum_v seq_lens[v], 576] of the KV element type, 16-B al.
+ */
+int mla_debug_gather(const void* kv_pages, mla_kv_dtype kv_dtype,
+                     int64_t num_slots, const int32_t* req_to_token,
+                     int64_t r2t_stride, const int32_t* seq_lens,
+                     const int64_t* row_offset, int V, int page_size,
+                     void* dense_out, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,232 @@
+"""GB300 (sm_103a) MLA latent decode: thin Python binding of libmla_decode.so.
+
+Every function here only marshals arguments (torch tensors -> device
+pointers, the current CUDA stream) into the C ABI declared in
+include/mla_decode.h; all arithmetic runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing, loading it raises.
+
+    import mla_latent_decode_gb300 as mla
+    O_part, LSE_part = mla.decode_partial(q_nope, q_rope, kv, ..., num_splits)
+    out, lse = mla.lse_combine(O_part, LSE_part)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
+ROW_DIM, NOPE_DIM, ROPE_DIM, VALUE_DIM, PAGE_SIZE = 576, 512, 64, 512, 64
+KV_BF16, KV_FP8_E4M3 = 0, 1
+STATUS_WAIT_TIMEOUT, STATUS_BAD_LENGTH, STATUS_BAD_SLOT = 1, 2, 4
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MlaError(RuntimeError):
+    """A non-zero return code of the C library, with its message."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+def library() -> ctypes.CDLL:
+    """Load libmla_decode.so (built by ``build.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i32, i64, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                 ctypes.c_float, ctypes.c_double)
+        sig = {
+            "mla_last_error_string": (ctypes.c_char_p, []),
+            "mla_num_sms": (i32, [i32]),
+            "mla_pair_slots": (i32, []),
+            "mla_plan_heuristic": (i32, [i32, i32]),
+            "mla_plan_ex": (i32, [i32, i32, i32, p, i32, i32, f64, f64, p, p, p]),
+            "mla_plan": (i32, [i32, i32, i32, i32, p, i32, p, p]),
+            "mla_check_page_table": (i32, [p, i64, p, p, i32, i32, i32, i64]),
+            "mla_decode_partial": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
+                                         i32, i32, i32, i32, f32, i32, p, p, p, p]),
+            "mla_decode_partial_simt": (i32, [p, p, p, p, i32, i64, p, i64, p, p,
+                                              i32, i32, i32, i32, i32, f32, i32, p,
+                                              p, p, p]),
+            "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
+            "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise MlaError(rc, library().mla_last_error_string().decode())
+    return rc
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _host_i32(x) -> "ctypes.Array":
+    vals = [int(v) for v in (x.tolist() if torch.is_tensor(x) else x)]
+    return (ctypes.c_int32 * len(vals))(*vals)
+
+
+# ------------------------------------------------------------------ planning
+def num_sms(device: int = 0) -> int:
+    return _check(library().mla_num_sms(device))
+
+
+def pair_slots() -> int:
+    """Concurrently resident CTA pairs of the decode kernel on this device."""
+    return _check(library().mla_pair_slots())
+
+
+def plan_heuristic(B: int, q_len: int) -> int:
+    """The pages' split rule max(1, min(148 // B // (2 q_len), 32))."""
+    return _check(library().mla_plan_heuristic(B, q_len))
+
+
+def plan_ex(seq_lens: Sequence[int], q_len: int, H: int, slots: int,
+            s_max: int = 64, c0: float = 4.0, lam: float = 1.0):
+    """Wave-rounding planner: returns (num_splits, wave_eff, makespan)."""
+    arr = _host_i32(seq_lens)
+    S, eff, ms = ctypes.c_int(), ctypes.c_float(), ctypes.c_double()
+    _check(library().mla_plan_ex(len(arr), q_len, H, arr, slots, s_max,
+                                 float(c0), float(lam), ctypes.byref(S),
+                                 ctypes.byref(eff), ctypes.byref(ms)))
+    return S.value, eff.value, ms.value
+
+
+def plan(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
+         num_sms: int = 0):
+    """Planner with the library defaults; num_sms=0 asks the device."""
+    arr = _host_i32(seq_lens)
+    assert len(arr) == B * num_shards
+    S, eff = ctypes.c_int(), ctypes.c_float()
+    _check(library().mla_plan(B, q_len, H, num_shards, arr, num_sms,
+                              ctypes.byref(S), ctypes.byref(eff)))
+    return S.value, eff.value
+
+
+def check_page_table(req_to_token, seq_lens, kv_limit, q_len: int,
+                     num_slots: int, page_size: int = PAGE_SIZE) -> None:
+    """Host validation of a page table (raises MlaError on a bad entry)."""
+    r2t = req_to_token.detach().to("cpu", torch.int32).contiguous()
+    sl = seq_lens.detach().to("cpu", torch.int32).contiguous()
+    kl = None if kv_limit is None else kv_limit.detach().to("cpu", torch.int32).contiguous()
+    _check(library().mla_check_page_table(
+        _ptr(r2t), r2t.shape[1], _ptr(sl), _ptr(kl), r2t.shape[0], q_len,
+        page_size, num_slots))
+
+
+# ------------------------------------------------------------------ kernels
+def _kv_dtype(kv: torch.Tensor) -> int:
+    if kv.dtype == torch.bfloat16:
+        return KV_BF16
+    if kv.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return KV_FP8_E4M3
+    raise TypeError(f"kv dtype {kv.dtype}: expected bfloat16 or uint8 (E4M3)")
+
+
+def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
+                   kv_limit, num_splits: int, sm_scale: float,
+                   num_shards: int = 1, O_part=None, LSE_part=None,
+                   status=None, simt: bool = False, stream=None):
+    """Partial (O, LSE) per split and shard; see mla_decode_partial.
+
+    Returns (O_part fp32 [S, shards, B, q, H, 512], LSE_part fp32 [S, shards,
+    B, q, H]); outputs are allocated with torch unless given.
+    """
+    B, q_len, H, _ = q_nope.shape
+    dev = q_nope.device
+    if O_part is None:
+        O_part = torch.empty((num_splits, num_shards, B, q_len, H, VALUE_DIM),
+                             dtype=torch.float32, device=dev)
+    if LSE_part is None:
+        LSE_part = torch.empty((num_splits, num_shards, B, q_len, H),
+                               dtype=torch.float32, device=dev)
+    fn = library().mla_decode_partial_simt if simt else library().mla_decode_partial
+    _check(fn(_ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale),
+              _kv_dtype(kv), kv.shape[0], _ptr(req_to_token),
+              req_to_token.stride(0), _ptr(seq_lens), _ptr(kv_limit), B, q_len,
+              H, num_shards, PAGE_SIZE, float(sm_scale), num_splits,
+              _ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream)))
+    return O_part, LSE_part
+
+
+def lse_combine(O_part, LSE_part, out=None, lse_out=None, stream=None):
+    """LSE merge over the leading part dims -> (bf16 [rows, 512], fp32 [rows])."""
+    value_shape = LSE_part.shape
+    nd = LSE_part.dim()
+    parts = 1
+    # leading dims (splits, shards) are parts; the rest are rows
+    lead = 2 if nd == 5 else 1
+    for d in value_shape[:lead]:
+        parts *= d
+    rows = LSE_part.numel() // parts
+    row_shape = tuple(value_shape[lead:])
+    if out is None:
+        out = torch.empty(row_shape + (VALUE_DIM,), dtype=torch.bfloat16,
+                          device=O_part.device)
+    if lse_out is None:
+        lse_out = torch.empty(row_shape, dtype=torch.float32, device=O_part.device)
+    _check(library().mla_lse_combine(_ptr(O_part), _ptr(LSE_part), parts, rows,
+                                     _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
+
+
+def debug_gather(kv, req_to_token, seq_lens, row_offset, total_rows: int,
+                 stream=None):
+    """Raw-byte gather of every live token row through the TMA path."""
+    out = torch.empty((max(total_rows, 1), ROW_DIM), dtype=kv.dtype, device=kv.device)
+    _check(library().mla_debug_gather(
+        _ptr(kv), _kv_dtype(kv), kv.shape[0], _ptr(req_to_token),
+        req_to_token.stride(0), _ptr(seq_lens), _ptr(row_offset),
+        req_to_token.shape[0], PAGE_SIZE, _ptr(out), _stream(stream)))
+    return out[:total_rows]
+
+
+def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
+           status=None, stream=None):
+    """One decode step of a synth.Batch-like object: partial + combine.
+
+    Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H], num_splits).
+    """
+    wl = batch.wl
+    if num_splits is None:
+        num_splits = wl.num_splits or plan(
+            wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards)[0]
+    O_part, LSE_part = decode_partial(
+        batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+        batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,
+        wl.sm_scale, num_shards=wl.num_shards, status=status, simt=simt,
+        stream=stream)
+    out, lse = lse_combine(O_part, LSE_part, stream=stream)
+    return out, lse, num_splits
+
+
+def batch_lengths(batch):
+    """Host list of the (virtual) request lengths of a batch."""
+    return [int(x) for x in batch.seq_lens.tolist()]

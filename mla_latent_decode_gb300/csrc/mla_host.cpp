@@ -1,0 +1,245 @@
+// mla_host.cpp -- host side of the MLA decode C ABI: error state, the split
+// planners, the page-table check and the argument checks shared by the
+// launches.  Page citations use the tags defined in include/mla_decode.h.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <vector>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+std::string& last_error() {
+  static thread_local std::string msg;
+  return msg;
+}
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  last_error() = buf;
+  return code;
+}
+
+int check_decode_args(const DecodeArgs& a) {
+  if (!a.q_nope || !a.q_rope || !a.kv || !a.req_to_token || !a.seq_lens ||
+      !a.O_part || !a.LSE_part)
+    return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (a.B < 1 || a.q_len < 1 || a.H < 1 || a.num_shards < 1 ||
+      a.num_splits < 1)
+    return fail(MLA_ERR_INVALID_ARG,
+                "B=%d q_len=%d H=%d num_shards=%d num_splits=%d must be >= 1",
+                a.B, a.q_len, a.H, a.num_shards, a.num_splits);
+  if (a.num_splits > 4096 || a.num_shards > 64)
+    return fail(MLA_ERR_INVALID_ARG, "num_splits %d > 4096 or num_shards %d > 64",
+                a.num_splits, a.num_shards);
+  const int64_t rows = (int64_t)a.B * a.q_len * a.H;
+  if (rows * a.num_shards * a.num_splits > (int64_t)1 << 31)
+    return fail(MLA_ERR_INVALID_ARG, "too many output rows");
+  if (a.page_size != MLA_PAGE_SIZE)
+    return fail(MLA_ERR_UNSUPPORTED, "page_size %d: only %d is built",
+                a.page_size, MLA_PAGE_SIZE);
+  if (a.kv_dtype != MLA_KV_BF16 && a.kv_dtype != MLA_KV_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)a.kv_dtype);
+  if (a.kv_dtype == MLA_KV_FP8_E4M3 && !a.kv_scale)
+    return fail(MLA_ERR_INVALID_ARG, "FP8 KV needs kv_scale");
+  if (a.num_slots < a.page_size || a.num_slots > ((int64_t)1 << 31) - 1)
+    return fail(MLA_ERR_INVALID_ARG, "num_slots %lld out of range",
+                (long long)a.num_slots);
+  if (a.r2t_stride < 1)
+    return fail(MLA_ERR_INVALID_ARG, "r2t_stride %lld < 1",
+                (long long)a.r2t_stride);
+  if (!std::isfinite(a.sm_scale))
+    return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (!aligned(a.q_nope, 16) || !aligned(a.q_rope, 16) || !aligned(a.kv, 16) ||
+      !aligned(a.O_part, 16) || !aligned(a.LSE_part, 4) ||
+      !aligned(a.req_to_token, 4) || !aligned(a.seq_lens, 4) ||
+      (a.kv_limit && !aligned(a.kv_limit, 4)) ||
+      (a.kv_scale && !aligned(a.kv_scale, 4)) ||
+      (a.status && !aligned(a.status, 4)))
+    return fail(MLA_ERR_MISALIGNED,
+                "q/kv/O_part need 16-B alignment, the int/float arrays 4-B");
+  return MLA_OK;
+}
+
+// List-scheduling makespan of units in launch order on `slots` slots.
+static double makespan(const std::vector<double>& costs, int slots) {
+  if (costs.empty()) return 0.0;
+  std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+  const size_t n = std::min<size_t>((size_t)slots, costs.size());
+  for (size_t k = 0; k < n; ++k) heap.push(0.0);
+  double end = 0.0;
+  for (double c : costs) {
+    double t = heap.top() + c;
+    heap.pop();
+    end = std::max(end, t);
+    heap.push(t);
+  }
+  return end;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_last_error_string(void) { return last_error().c_str(); }
+
+int mla_num_sms(int device) {
+  int n = 0;
+  cudaError_t e =
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  return n;
+}
+
+// [K3-MLA]: split = min(148 // B // (q_len * 2), 32), floored at 1.
+int mla_plan_heuristic(int B, int q_len) {
+  if (B < 1 || q_len < 1)
+    return fail(MLA_ERR_INVALID_ARG, "B and q_len must be >= 1");
+  return std::max(1, std::min(148 / B / (q_len * 2), 32));
+}
+
+int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
+                int slots, int s_max, double c0, double lam,
+                int* num_splits_out, float* wave_eff_out,
+                double* makespan_out) {
+  if (V < 1 || q_len < 1 || H < 1 || !seq_lens_host || !num_splits_out)
+    return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
+  if (slots < 1 || s_max < 1 || s_max > 1024 || !(c0 >= 0) || !(lam >= 0))
+    return fail(MLA_ERR_INVALID_ARG, "slots/s_max/c0/lam out of range");
+  const int G = (H * q_len + MLA_ROWS_PER_PAIR - 1) / MLA_ROWS_PER_PAIR;
+  const double rows = (double)V * q_len * H;
+  double bestJ = 0, bestEff = 0, bestMs = 0;
+  int bestS = 0;
+  std::vector<double> costs;
+  for (int S = 1; S <= s_max; ++S) {
+    costs.clear();
+    double total = 0;
+    for (int v = 0; v < V; ++v) {
+      const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
+      const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+      for (int s = 0; s < S; ++s) {
+        const double c = (double)((s + 1) * P / S - s * P / S) + c0;
+        for (int g = 0; g < G; ++g) {
+          costs.push_back(c);
+          total += c;
+        }
+      }
+    }
+    const double ms = makespan(costs, slots);
+    const double J = ms + lam * S * rows / 1024.0;
+    if (bestS == 0 || J < bestJ - 1e-9) {
+      bestJ = J;
+      bestS = S;
+      bestMs = ms;
+      bestEff = ms > 0 ? total / ((double)slots * ms) : 1.0;
+    }
+  }
+  *num_splits_out = bestS;
+  if (wave_eff_out) *wave_eff_out = (float)bestEff;
+  if (makespan_out) *makespan_out = bestMs;
+  return MLA_OK;
+}
+
+int mla_plan(int B, int q_len, int H, int num_shards,
+             const int32_t* seq_lens_host, int num_sms, int* num_splits_out,
+             float* wave_eff_out) {
+  if (B < 1 || num_shards < 1)
+    return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
+  int slots;
+  if (num_sms > 0) {
+    slots = std::max(1, num_sms / 2);
+  } else {
+    slots = mla_pair_slots();
+    if (slots < 0) return slots;
+    if (slots == 0) return fail(MLA_ERR_CUDA, "no CTA pair fits on this device");
+  }
+  return mla_plan_ex(B * num_shards, q_len, H, seq_lens_host, slots, 64, 4.0,
+                     1.0, num_splits_out, wave_eff_out, nullptr);
+}
+
+int mla_check_page_table(const int32_t* r2t, int64_t stride,
+                         const int32_t* seq_lens, const int32_t* kv_limit,
+                         int V, int q_len, int page_size, int64_t num_slots) {
+  if (!r2t || !seq_lens || V < 1 || q_len < 1 || stride < 1 ||
+      page_size < 1 || num_slots < 1)
+    return fail(MLA_ERR_INVALID_ARG, "bad page-table check arguments");
+  for (int v = 0; v < V; ++v) {
+    const int64_t L = seq_lens[v];
+    if (L < 0 || L > stride)
+      return fail(MLA_ERR_PAGE_TABLE, "seq_lens[%d] = %lld outside [0, %lld]",
+                  v, (long long)L, (long long)stride);
+    if (!kv_limit && L < q_len)
+      return fail(MLA_ERR_PAGE_TABLE, "seq_lens[%d] = %lld < q_len %d", v,
+                  (long long)L, q_len);
+    if (kv_limit)
+      for (int i = 0; i < q_len; ++i) {
+        const int32_t k = kv_limit[(int64_t)v * q_len + i];
+        if (k < 0 || k > L)
+          return fail(MLA_ERR_PAGE_TABLE, "kv_limit[%d,%d] = %d outside [0, %lld]",
+                      v, i, k, (long long)L);
+      }
+    const int32_t* row = r2t + (int64_t)v * stride;
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t first = row[t - t % page_size];
+      if (first % page_size != 0)
+        return fail(MLA_ERR_PAGE_TABLE, "page of token %lld of request %d starts "
+                    "at slot %lld, not a multiple of %d", (long long)t, v,
+                    (long long)first, page_size);
+      if (row[t] != first + t % page_size)
+        return fail(MLA_ERR_PAGE_TABLE, "token %lld of request %d: slot %d is not "
+                    "page-contiguous", (long long)t, v, row[t]);
+      if (row[t] < 0 || row[t] >= num_slots)
+        return fail(MLA_ERR_PAGE_TABLE, "token %lld of request %d: slot %d outside "
+                    "[0, %lld)", (long long)t, v, row[t], (long long)num_slots);
+    }
+  }
+  return MLA_OK;
+}
+
+int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
+                       const void* kv_pages, const float* kv_scale,
+                       mla_kv_dtype kv_dtype, int64_t num_slots,
+                       const int32_t* req_to_token, int64_t r2t_stride,
+                       const int32_t* seq_lens, const int32_t* kv_limit, int B,
+                       int q_len, int H, int num_shards, int page_size,
+                       float sm_scale, int num_splits, float* O_part,
+                       float* LSE_part, int* status, mla_stream_t stream) {
+  DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
+               num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
+               B,               q_len,     H,        num_shards, page_size,
+               sm_scale,        num_splits, O_part,  LSE_part,  status,
+               (cudaStream_t)stream};
+  int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  return launch_tc(a);
+}
+
+int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
+                            const void* kv_pages, const float* kv_scale,
+                            mla_kv_dtype kv_dtype, int64_t num_slots,
+                            const int32_t* req_to_token, int64_t r2t_stride,
+                            const int32_t* seq_lens, const int32_t* kv_limit,
+                            int B, int q_len, int H, int num_shards,
+                            int page_size, float sm_scale, int num_splits,
+                            float* O_part, float* LSE_part, int* status,
+                            mla_stream_t stream) {
+  DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
+               num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
+               B,               q_len,     H,        num_shards, page_size,
+               sm_scale,        num_splits, O_part,  LSE_part,  status,
+               (cudaStream_t)stream};
+  int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  return launch_simt(a);
+}
+
+}  // extern "C"

