@@ -1,0 +1,430 @@
+"""Benchmark: weight-absorbed MLA decode (partial + LSE combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config dp16]
+                    [--impl reference]
+
+One step is one pass of the whole hot path over one batch: the split plan
+(computed once per batch shape, before timing, from the host lengths), the
+tensor-core partial decode launch and the LSE-combine launch.  The default
+workload is 16 requests x q_len 5 x 96 heads x 100k-token context, BF16
+latent KV in 64-token pages with a random page permutation, synthetic N(0,1)
+data (seed = rank).
+
+value      attention TFLOP/s over all ranks, inputs resident in HBM
+           (algorithmic FLOPs 2*H*(576+512)*sum_b sum_i (L_b - q_len + 1 + i)
+           per step / device time), max over ranks of the timed region
+e2e        the same metric through the public API from pinned host buffers:
+           every step copies the queries, page table and lengths to the device
+           and reads the output and LSE back (the KV cache is resident state)
+roofline   the partial-decode kernel alone: algorithmic FLOPs / its mean
+           CUDA-event duration inside the timed region vs measured bf16 peak
+cpu_baseline  the fp64 oracle on a bounded sample of rows, host cores
+
+With N > 1 (torchrun) every rank decodes its own batch of the same shape
+(independent requests, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MLA decode µs/layer & attention TFLOP/s at 100k ctx; "
+          "% of GB300 tensor peak")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_partial_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dp16")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--splits", type=int, default=0, help="0: planner")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(wl):
+    lens = wl.seq_lens
+    ctx = lens[0] if len(set(lens)) == 1 else f"{min(lens)}..{max(lens)}"
+    return (f"{wl.name}: {wl.B} requests x q_len {wl.q_len} x {wl.H} heads x "
+            f"{ctx} context, {wl.kv_dtype} latent KV (576-d rows), page "
+            f"{wl.page_size}" + (f", {wl.num_shards} interleaved shards"
+                                 if wl.num_shards > 1 else ""))
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("mla_tc") or f in ("ptx_sm103.cuh", "mla_tma.cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name, units):
+    """DRAM bytes per launch from a committed ncu summary, only if it was
+    taken on the current kernel source; scaled by units if captured smaller."""
+    try:
+        d = json.load(open(PROFILE_TRAFFIC))
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    e = d.get("workloads", {}).get(config_name)
+    if not e:
+        return None
+    return e["dram_bytes_per_launch"] * units / e.get("units", units)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        for line in open(self.out.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def oracle_sample(batch, hb, seconds, rank_seed=0):
+    """Time the fp64 oracle on a bounded sample of rows; returns the
+    cpu_baseline object in the metric's unit (TFLOP/s)."""
+    import numpy as np
+    import oracle
+
+    wl = batch.wl
+    r2t, sl, kl = hb["req_to_token"], hb["seq_lens"], hb["kv_limit"]
+    rng = np.random.default_rng(rank_seed)
+    threads = oracle.num_threads()
+
+    def rows_flops(rows):
+        tot = 0
+        per = wl.q_len * wl.H
+        for r in rows:
+            b, i = divmod(int(r) // wl.H, wl.q_len)
+            L = int(sl[b])
+            n = int(kl[b, i]) if kl is not None else L - wl.q_len + 1 + i
+            tot += 2 * (576 + 512) * max(0, min(n, L))
+        return tot
+
+    B_q = wl.B
+    shard_r2t = r2t[:B_q]
+    shard_sl = sl[:B_q]
+    shard_kl = None if kl is None else kl[:B_q]
+    # calibrate on one row per thread, then size the sample to `seconds`
+    n_rows = max(threads, 1)
+    rows = rng.choice(wl.rows, size=min(n_rows, wl.rows), replace=False)
+    t0 = time.perf_counter()
+    oracle.mla_decode_rows(hb["q_nope"], hb["q_rope"], hb["kv"], batch.kv_is_fp8,
+                           hb["kv_scale"], shard_r2t, shard_sl, shard_kl, B_q,
+                           wl.q_len, wl.H, wl.sm_scale, rows)
+    dt = time.perf_counter() - t0
+    want = int(len(rows) * max(1.0, seconds / max(dt, 1e-3)))
+    rows = rng.choice(wl.rows, size=min(want, wl.rows), replace=False)
+    t0 = time.perf_counter()
+    oracle.mla_decode_rows(hb["q_nope"], hb["q_rope"], hb["kv"], batch.kv_is_fp8,
+                           hb["kv_scale"], shard_r2t, shard_sl, shard_kl, B_q,
+                           wl.q_len, wl.H, wl.sm_scale, rows)
+    dt = time.perf_counter() - t0
+    fl = rows_flops(rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{len(rows)} of {wl.rows} query rows of the same "
+                       f"workload (shard 0 where sharded), full visible "
+                       f"context each, {dt:.1f} s wall, fp64"),
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from mla_latent_decode_gb300 import synth
+
+    wl = synth.config(args.config)
+    batch = synth.make_batch(wl, seed=0, device="cpu")
+    hb = synth.host_bits(batch)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    vals = []
+    for k in range(args.warmup + args.steps):
+        cb = oracle_sample(batch, hb, per_step, rank_seed=k)
+        if k >= args.warmup:
+            vals.append(cb)
+    v = statistics.median(c["value"] for c in vals)
+    fl = wl.flops()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": fl / (v * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(wl)},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": vals[0]["cores"],
+                         "kind": "oracle", "sample": vals[0]["sample"]},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = dist_env()
+    import torch
+
+    import mla_latent_decode_gb300 as mla
+    from mla_latent_decode_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    mla.library()  # fail loudly if the CUDA library is missing
+
+    wl = synth.config(args.config)
+    batch = synth.make_batch(wl, seed=rank, device="cuda")
+    lens = mla.batch_lengths(batch)
+    slots = mla.pair_slots()
+    if args.splits > 0:
+        S, eff = args.splits, None
+    elif wl.num_splits:
+        S, eff = wl.num_splits, None
+    else:
+        S, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards)
+    S_pages = mla.plan_heuristic(wl.B, wl.q_len)
+
+    dev = torch.device("cuda", local)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
+                         dtype=torch.float32, device=dev)
+    LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
+                           dtype=torch.float32, device=dev)
+    out = torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.B, wl.q_len, wl.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+                           batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
+                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status)
+        if ev is not None:
+            ev[1].record(stream)
+        mla.lse_combine(O_part, LSE_part, out, lse)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.1)  # let the sampler take its first reading
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    part_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in timed region")
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    fl = wl.flops()
+    ms_per_step = total_ms / args.steps
+    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    peaks, peak_kind = measured_peaks()
+    part_mean = statistics.mean(part_ms)
+    achieved = fl / (part_mean * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = profiled_traffic(args.config, 1)
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = batch.q_nope.cpu().pin_memory()
+        hr = batch.q_rope.cpu().pin_memory()
+        ht = batch.req_to_token.cpu().pin_memory()
+        hs = batch.seq_lens.cpu().pin_memory()
+        ho = torch.empty_like(out, device="cpu").pin_memory()
+        hl = torch.empty_like(lse, device="cpu").pin_memory()
+        dq, dr = torch.empty_like(batch.q_nope), torch.empty_like(batch.q_rope)
+        dt_, ds = torch.empty_like(batch.req_to_token), torch.empty_like(batch.seq_lens)
+        bi = sum(x.numel() * x.element_size() for x in (hq, hr, ht, hs))
+        bo = sum(x.numel() * x.element_size() for x in (ho, hl))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dr.copy_(hr, non_blocking=True)
+            dt_.copy_(ht, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
+                               batch.kv_limit, S, wl.sm_scale, wl.num_shards,
+                               O_part, LSE_part, status)
+            mla.lse_combine(O_part, LSE_part, out, lse)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(10, args.steps // 2)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * fl * n_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hb = synth.host_bits(batch)
+        cpu = oracle_sample(batch, hb, args.cpu_seconds)
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": workload_desc(wl), "B": wl.B, "q_len": wl.q_len,
+                "H": wl.H, "context": wl.seq_lens[0] if len(set(wl.seq_lens)) == 1 else "ragged",
+                "num_shards": wl.num_shards, "num_splits": S,
+                "planner_wave_eff": eff, "pages_rule_splits": S_pages,
+                "pair_slots": slots,
+                "l2": f"inputs larger than L2 ({batch.kv.numel() * batch.kv.element_size() / 1e9:.2f} GB KV), no flush",
+                "parallelism": f"dp{world} (independent requests per rank)",
+            },
+            "us_per_layer": ms_per_step * 1e3,
+            "partial_us": part_mean * 1e3,
+            "combine_us": statistics.mean(comb_ms) * 1e3,
+            "kv_gbs": sum(wl.seq_lens) * wl.kv_row_bytes() * world * args.steps
+                      / (total_ms * 1e-3) / 1e9,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": traffic,
+                         "kernel": "mla_partial_tc_kernel",
+                         "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)"},
+            "hbm_frac": (sum(wl.seq_lens) * wl.kv_row_bytes() / (part_mean * 1e-3)
+                         / 1e9) / float(peaks["hbm_gbs"]),
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": 2 * args.steps,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -109,6 +109,13 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// 32-bit store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr,
+                                               uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)
+               : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
@@ -230,6 +237,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in every CTA of `cta_mask`
+// when every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar,
+                                                     uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 

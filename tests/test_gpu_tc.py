@@ -1,0 +1,166 @@
+"""GPU parity of the tensor-core decode path (mla_decode_partial) vs the oracle.
+
+Small cases span several tiles, ragged tails, empty splits, shards and the
+rescale path (peaked softmax); the full-size 16 x 5 x 96 x 100k workload is
+checked on sampled rows in the launch configuration bench.py times.  Bitwise
+properties (page-permutation invariance, causality, determinism) need no
+oracle.  Expected values come only from oracle/.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_decode_gb300 as mla
+from mla_latent_decode_gb300 import build, synth
+from parity import check_close, f64, oracle_rows, split_range
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    mla.library()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+CASES = [
+    ("tiny", synth.config("tiny"), 1),
+    ("one_token", synth.Workload("one", 1, 1, 16, [1]), 1),
+    ("small_bf16", synth.Workload("s", 3, 5, 96, [1000, 257, 5]), 3),
+    ("heads16_q3", synth.Workload("h", 2, 3, 16, [130, 3]), 7),
+    ("rows_200", synth.Workload("r", 2, 2, 100, [700, 640]), 2),
+    ("peaked", synth.Workload("p", 2, 5, 96, [3000, 333], q_scale=8.0), 4),
+    ("long_one_split", synth.Workload("l", 1, 5, 96, [20_000]), 1),
+    ("empty_splits", synth.Workload("e", 2, 5, 32, [64, 200]), 9),
+]
+
+
+@pytest.mark.parametrize("name,wl,S", CASES, ids=[c[0] for c in CASES])
+def test_tc_decode_matches_oracle(name, wl, S):
+    batch = synth.make_batch(wl, seed=3, device="cuda")
+    hb = synth.host_bits(batch)
+    st = _status()
+    out, lse, _ = mla.decode(batch, num_splits=S, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O_ref, l_ref = oracle_rows(batch, hb, None)
+    m = check_close(f64(out).reshape(-1, 512), f64(lse).reshape(-1), O_ref, l_ref,
+                    wl.kv_dtype, name)
+    print(name, m)
+
+
+def test_tc_partials_match_oracle_per_split():
+    wl = synth.Workload("parts", 2, 5, 40, [1000, 100], q_scale=2.0)
+    batch = synth.make_batch(wl, seed=4, device="cuda")
+    hb = synth.host_bits(batch)
+    S = 5
+    O_part, LSE_part = mla.decode_partial(
+        batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale, batch.req_to_token,
+        batch.seq_lens, batch.kv_limit, S, wl.sm_scale)
+    torch.cuda.synchronize()
+    rows = np.arange(wl.rows)
+    b_of = rows // (wl.q_len * wl.H)
+    for s in range(S):
+        lo = np.array([split_range(wl.seq_lens[b], S, s)[0] for b in b_of])
+        hi = np.array([split_range(wl.seq_lens[b], S, s)[1] for b in b_of])
+        O_ref, l_ref = oracle_rows(batch, hb, rows, lo=lo, hi=hi)
+        check_close(f64(O_part[s, 0]).reshape(-1, 512), f64(LSE_part[s, 0]).reshape(-1),
+                    O_ref, l_ref, "bf16", f"split {s}")
+
+
+def test_tc_shards_match_unsharded_oracle():
+    sh = synth.Workload("dcp", 3, 5, 96, [517, 64, 9], num_shards=8)
+    base = synth.Workload("dcp", 3, 5, 96, [517, 64, 9])
+    b_sh = synth.make_batch(sh, seed=5, device="cuda")
+    b_un = synth.make_batch(base, seed=5, device="cuda")
+    st = _status()
+    out_s, lse_s, _ = mla.decode(b_sh, num_splits=2, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O_ref, l_ref = oracle_rows(b_un, synth.host_bits(b_un), None)
+    check_close(f64(out_s).reshape(-1, 512), f64(lse_s).reshape(-1), O_ref, l_ref,
+                "bf16", "sharded")
+
+
+def test_tc_agrees_with_cuda_core_path():
+    wl = synth.Workload("x", 4, 5, 96, [2000, 1500, 64, 777], q_scale=3.0)
+    batch = synth.make_batch(wl, seed=6, device="cuda")
+    a, la, _ = mla.decode(batch, num_splits=3)
+    b, lb, _ = mla.decode(batch, num_splits=3, simt=True)
+    torch.cuda.synchronize()
+    check_close(f64(a).reshape(-1, 512), f64(la).reshape(-1), f64(b).reshape(-1, 512),
+                f64(lb).reshape(-1), "bf16", "tc vs simt")
+
+
+def test_tc_page_permutation_and_determinism_are_bitwise():
+    wl = synth.Workload("perm", 3, 5, 96, [900, 4000, 130])
+    a = synth.make_batch(wl, seed=7, device="cuda")
+    b = synth.make_batch(wl, seed=7, device="cuda", page_seed=999)
+    assert not torch.equal(a.req_to_token, b.req_to_token)
+    oa, la, _ = mla.decode(a, num_splits=4)
+    oa2, la2, _ = mla.decode(a, num_splits=4)
+    ob, lb, _ = mla.decode(b, num_splits=4)
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+    assert torch.equal(oa, oa2) and torch.equal(la, la2)
+
+
+def test_tc_draft_tokens_are_causal():
+    """Zero queries make the softmax flat (O = mean of the visible c_kv rows),
+    so adding 1 to draft token j's c_kv must move every row of query i >= j by
+    exactly 1/n_i and leave the rows of queries i < j bitwise unchanged
+    (checked on the fp32 partial output of a single split)."""
+    q_len, H = 5, 96
+    wl = synth.Workload("causal", 2, q_len, H, [300, 77], q_scale=0.0)
+
+    def run(batch):
+        O, L = mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, None,
+                                  batch.req_to_token, batch.seq_lens, None, 1,
+                                  wl.sm_scale)
+        torch.cuda.synchronize()
+        return O[0, 0], L[0, 0]
+
+    base = synth.make_batch(wl, seed=8, device="cuda")
+    o0, l0 = run(base)
+    for j in range(q_len):
+        pb = synth.make_batch(wl, seed=8, device="cuda")
+        delta = {}
+        for b in range(2):
+            slot = int(pb.req_to_token[b, wl.seq_lens[b] - q_len + j])
+            pb.kv[slot, :512] += 1
+            # the stored shift is 1 up to the bf16 rounding of the new row
+            delta[b] = (pb.kv[slot, :512].double() - base.kv[slot, :512].double()).cpu().numpy()
+        o1, l1 = run(pb)
+        assert torch.equal(o0[:, :j], o1[:, :j]) and torch.equal(l0[:, :j], l1[:, :j])
+        for b in range(2):
+            assert np.abs(delta[b] - 1).max() <= 2 ** -4
+            for i in range(j, q_len):
+                n = wl.seq_lens[b] - q_len + 1 + i
+                d = (o1[b, i].double() - o0[b, i].double()).cpu().numpy()
+                assert np.abs(d - delta[b][None, :] / n).max() < 2e-6, (b, i, j)
+
+
+def test_tc_full_size_dp16_sampled_rows():
+    """16 requests x q_len 5 x 96 heads x 100k tokens, planner splits (the
+    configuration bench.py times), checked on rows sampled across requests,
+    queries, heads and row groups."""
+    wl = synth.config("dp16")
+    batch = synth.make_batch(wl, seed=0, device="cuda")
+    st = _status()
+    out, lse, S = mla.decode(batch, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    hb = synth.host_bits(batch)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([
+        rng.choice(wl.rows, 40, replace=False),
+        [0, wl.rows - 1, 127, 128, 383, 384, 479]]))  # row-group edges
+    O_ref, l_ref = oracle_rows(batch, hb, rows)
+    got = f64(out).reshape(-1, 512)[rows]
+    m = check_close(got, f64(lse).reshape(-1)[rows], O_ref, l_ref, "bf16",
+                    f"dp16 S={S}")
+    print("dp16", S, m)
