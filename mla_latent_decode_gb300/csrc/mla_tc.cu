@@ -8,24 +8,27 @@
 // Design (GB300, one CTA per SM):
 //   All H*q_len query rows of a request share one latent KV row per token, so
 //   S = Q K^T (576-d) and O = P V (512-d, V = the c_kv columns of the same
-//   row) are dense contractions with M = query rows.  A 128-row M tile needs
-//   its fp32 O accumulator (128 x 512) to fill all 512 TMEM columns of an SM,
-//   so the work of one 128-row group is split over a CTA pair (a cluster of
-//   two):
-//     rank 0, the "S-CTA": Q (bf16 pairs) in TMEM columns [0, 288), three S
-//       buffers of 64 columns; streams K tiles (one 64-token page = 9 TMA
-//       boxes of 64 tokens x 64 dims, 128-B swizzle) through a ring, issues
-//       S = Q K^T with A from TMEM, runs the online softmax in registers (one
-//       thread per row, base-2, lazy rescaling), and ships P (bf16, K-major
-//       128-B swizzled) plus the per-row rescale factors to the peer with a
-//       bulk shared-memory copy.
-//     rank 1, the "O-CTA": O (128 x 512 fp32) in all of TMEM; streams the
-//       8 c_kv boxes of each page, issues O += P V (A = P from shared memory,
-//       B = V MN-major from the TMA boxes, N = 256 per instruction), rescales
-//       O rows when the S-CTA raised its running max, and writes the
-//       normalised O_part rows.
-//   The tensor work splits 576 : 512 between the two SMs; no QK^T is
-//   repeated.  Every wait is bounded (ptx_sm103.cuh); a timeout sets
+//   row) are dense contractions with M = query rows.  A 128-row fp32 O
+//   accumulator over 512 values fills all 512 TMEM columns of an SM, so one
+//   128-row group is served by a cluster of two CTAs:
+//     rank 0, the "S-CTA": Q_nope (bf16 pairs) in TMEM columns [0, 256),
+//       Q_rope in shared memory, one S buffer of up to 256 columns (an S tile
+//       is up to 4 pages = 256 tokens).  K arrives in 32-KB stages (one
+//       64-dim chunk of the tile's pages, 128-byte swizzled TMA boxes); each
+//       stage feeds 4 MMAs of M=128, N=64*pages, K=16.  Two softmax
+//       warpgroups own two pages each, exchange row maxima once per tile,
+//       keep base-2 running statistics with lazy rescaling, and ship each
+//       page's P (bf16, K-major, 128-byte swizzled) plus rescale factors to
+//       the peer with a bulk shared-memory copy.
+//     rank 1, the "O-CTA": O (128 x 512 fp32) in all of TMEM; V (the c_kv
+//       columns) arrives in 32-KB stages (256 dims of one page); each P
+//       message feeds 8 MMAs of M=128, N=256, K=16 (A = P from shared memory,
+//       B = V MN-major).  Correction warps rescale O rows when the S-CTA
+//       raised a running max, then write the normalised O_part rows.
+//   A barrier wait or a tcgen05.commit costs the single issuing thread
+//   ~70-100 cycles that the tensor pipe does not hide, so every stage is
+//   sized to carry four MMAs of up to 256 columns (512 tensor cycles) per
+//   wait/commit pair.  Every wait is bounded (ptx_sm103.cuh); a timeout sets
 //   MLA_STATUS_WAIT_TIMEOUT and the CTA pair finishes early.
 #include <cuda_bf16.h>
 
@@ -37,42 +40,49 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;        // 6 warps
-constexpr int kRingS = 22;           // 8-KB box slots, S-CTA
-constexpr int kRingO = 20;           // O-CTA: a multiple of 4 (4-box groups)
-constexpr int kRing = kRingS > kRingO ? kRingS : kRingO;
-constexpr int kNS = 3;               // S buffers in TMEM
+constexpr int kThreads = 384;        // 12 warps = 3 warpgroups
+constexpr int kStages = 5;           // 32-KB ring stages (4 boxes each)
+constexpr int kBoxesPerStage = 4;
+constexpr int kTilePages = 4;        // pages per S tile (N <= 256)
 constexpr int kNP = 2;               // P message slots
 constexpr int kRows = MLA_ROWS_PER_PAIR;  // 128
-constexpr int kTile = MLA_PAGE_SIZE;      // 64 tokens per tile
-constexpr int kPBytes = kRows * kTile * 2;          // 16384
+constexpr int kPage = MLA_PAGE_SIZE;      // 64 tokens
+constexpr int kPBytes = kRows * kPage * 2;          // 16384
 constexpr int kAlphaOff = kPBytes;                  // float alpha[128]
 constexpr int kFlagOff = kPBytes + kRows * 4;       // uint32 flags[4]
 constexpr int kPMsgBytes = kFlagOff + 16;           // 16912 = 1057 x 16
 constexpr int kPSlotStride = 17408;                 // 17 KB, 1024-aligned
-constexpr uint32_t kQCols = MLA_ROW_DIM / 2;        // 288
-constexpr uint32_t kSCol0 = kQCols;                 // S buffers: 288 + 64 i
+constexpr uint32_t kSCol0 = 256;                    // S buffer columns
 constexpr float kTau = 8.f;          // lazy-rescale threshold (log2 units)
 constexpr uint32_t kFull = 0xffffffffu;
+// Register split of the S-CTA (setmaxnreg): 384 threads launch with 168
+// registers each (64,512); the producer/MMA warpgroup gives registers away so
+// the two softmax warpgroups can hold a 128 x 256 fp32 score tile.  The split
+// is one-way: nobody asks for registers back before the CTA exits.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
+__host__ __device__ constexpr uint32_t idesc_s(int pages) {
+  return idesc_bf16_f32(128, 64 * pages, false, false);
+}
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
 
 struct __align__(1024) Smem {
-  uint8_t ring[kRing][kBoxBytes];
+  uint8_t ring[kStages * kBoxesPerStage][kBoxBytes];  // 160 KB
+  uint8_t qrope[kRows * 128];                         // S-CTA: Q_rope rows
   uint8_t pslot[kNP][kPSlotStride];
   float fin[kRows];
-  uint64_t full[kRing];
-  uint64_t empty[kRing];
-  uint64_t sfull[kNS];
-  uint64_t sempty[kNS];
+  float xch[2][kRows];      // S-CTA: per-warpgroup row maxima / partial sums
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t sfull, sempty;
   uint64_t pfull[kNP];
   uint64_t pempty[kNP];
-  uint64_t drain;
-  uint64_t corr_done;
-  uint64_t tail_ready;
-  uint64_t fin_full;
-  uint64_t qready;
+  uint64_t sent[kNP];       // S-CTA: one arrival per message sent in slot k
+  uint64_t drain, corr_done, tail_ready, fin_full, qready;
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -109,8 +119,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Record a failed wait: device status, this CTA's and the peer's abort flag.
-__device__ __noinline__ void signal_abort(Smem& s, const TcParams& p,
-                                          uint32_t rank) {
+__device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
+                                             uint32_t rank) {
   if (p.status) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
   s.abort_flag = 1;
   st_cluster_u32(mapa(smem_u32(&s.abort_flag), rank ^ 1u), 1u);
@@ -118,7 +128,7 @@ __device__ __noinline__ void signal_abort(Smem& s, const TcParams& p,
 
 // Per-pair work description, identical on both CTAs of the pair.
 struct Work {
-  int v, b, shard, split, r_base, nrows, ntiles;
+  int v, b, shard, split, r_base, nrows, npages;
   int64_t L, p0;
 };
 
@@ -138,135 +148,201 @@ __device__ __forceinline__ Work pair_work(const TcParams& p) {
   if (L > p.r2t_stride) L = p.r2t_stride;
   if (L < 0) L = 0;
   w.L = L;
-  const int64_t P = (L + kTile - 1) / kTile;
+  const int64_t P = (L + kPage - 1) / kPage;
   w.p0 = (int64_t)w.split * P / p.num_splits;
   const int64_t p1 = (int64_t)(w.split + 1) * P / p.num_splits;
-  w.ntiles = (int)(p1 - w.p0);
+  w.npages = (int)(p1 - w.p0);
   return w;
 }
 
-// ------------------------------------------------------------- producer ----
-// One warp streams `kBoxes` boxes per page tile into the ring.  The page
-// table is read 32 tiles ahead (one entry per lane) so the TMA issue never
-// waits on a dependent global load.
-template <int kBoxes, int kRingN>
-__device__ void producer(Smem& s, const CUtensorMap* map, const TcParams& p,
-                         const Work& w, uint32_t rank, int lane,
-                         bool zero_tail) {
-  uint32_t slot = 0, phase = 0;
-  auto page_base = [&](int j) -> int32_t {
-    if (j >= w.ntiles) return 0;
-    const int32_t base =
-        p.r2t[(int64_t)w.v * p.r2t_stride + (w.p0 + j) * kTile];
-    if (base < 0 || (base & (kTile - 1)) || (int64_t)base + kTile > p.num_slots)
-      return -1;
-    return base;
-  };
-  int32_t cur = 0, nxt = page_base(lane);
+__device__ __forceinline__ int tile_pages(const Work& w, int j) {
+  return min(kTilePages, w.npages - j * kTilePages);
+}
+
+// Base slot of page m of the pair's range, or -1 if it lies outside the pool.
+__device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
+                                             int m) {
+  if (m >= w.npages) return 0;
+  const int32_t base = p.r2t[(int64_t)w.v * p.r2t_stride + (w.p0 + m) * kPage];
+  if (base < 0 || (base & (kPage - 1)) || (int64_t)base + kPage > p.num_slots)
+    return -1;
+  return base;
+}
+
+// -------------------------------------------------------- S-CTA producer ---
+// Stage = one 64-dim chunk of the (up to 4) pages of an S tile.  Page bases
+// are read 32 pages ahead (one per lane) so a TMA issue never waits on a
+// dependent global load.
+__device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
+                                           const TcParams& p, const Work& w,
+                                           uint32_t rank, int lane) {
+  uint32_t stage = 0, phase = 0;
+  int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
-  for (int j = 0; j < w.ntiles; ++j) {
-    if ((j & 31) == 0) {
+  const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
+  for (int j = 0; j < ntiles && ok; ++j) {
+    const int m0 = j * kTilePages;
+    if (m0 % 32 == 0 && m0 > 0) {
       cur = nxt;
-      nxt = page_base(j + 32 + lane);
+      nxt = page_base(p, w, m0 + 32 + lane);
     }
-    const int32_t base = __shfl_sync(kFull, cur, j & 31);
-    // A page outside the pool reads as zeros (TMA fills out-of-range rows).
-    const int32_t y = base < 0 ? (int32_t)p.num_slots : base;
-    if (base < 0 && lane == 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
-    const uint32_t slot0 = slot, phase0 = phase;
-    if (lane == 0 && ok) {
-      for (int c = 0; c < kBoxes; ++c) {
-        if (!mbar_wait(smem_u32(&s.empty[slot]), phase ^ 1u, &s.abort_flag)) {
+    const int np = tile_pages(w, j);
+    // Page bases of this tile, one per lane q < 4 (a page outside the pool
+    // reads a row past the end, which TMA fills with zeros).
+    const int32_t bq = __shfl_sync(kFull, cur, (m0 + (lane & 3)) & 31);
+    const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
+    if (lane < np && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
+    const int32_t y0 = __shfl_sync(kFull, yq, 0), y1 = __shfl_sync(kFull, yq, 1);
+    const int32_t y2 = __shfl_sync(kFull, yq, 2), y3 = __shfl_sync(kFull, yq, 3);
+    if (lane == 0) {
+      for (int c = 0; c < kBf16BoxesPerPage; ++c) {
+        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(smem_u32(&s.full[slot]), kBoxBytes);
-        tma_load_2d(smem_u32(s.ring[slot]), map, smem_u32(&s.full[slot]),
-                    c * 64, y);
-        if (++slot == (uint32_t)kRingN) {
-          slot = 0;
+        const uint32_t fb = smem_u32(&s.full[stage]);
+        mbar_arrive_expect_tx(fb, np * kBoxBytes);
+        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage]);
+        tma_load_2d(dst, map, fb, c * 64, y0);
+        if (np > 1) tma_load_2d(dst + kBoxBytes, map, fb, c * 64, y1);
+        if (np > 2) tma_load_2d(dst + 2 * kBoxBytes, map, fb, c * 64, y2);
+        if (np > 3) tma_load_2d(dst + 3 * kBoxBytes, map, fb, c * 64, y3);
+        if (++stage == kStages) {
+          stage = 0;
           phase ^= 1u;
         }
       }
     }
     ok = __shfl_sync(kFull, ok, 0);
-    slot = __shfl_sync(kFull, slot, 0);
-    phase = __shfl_sync(kFull, phase, 0);
-    if (!ok) {
-      if (lane == 0) signal_abort(s, p, rank);
-      break;
+  }
+  if (!ok && lane == 0) signal_abort(s, p, rank);
+}
+
+// -------------------------------------------------------- O-CTA producer ---
+// Stage = 256 c_kv dims of one page (4 boxes): two stages per page.  The
+// request's last page may be partly filled: rows past its length can hold
+// anything (even NaN) and 0 * NaN would poison O = P V, so they are zeroed
+// before the MMA may read them.
+__device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
+                                           const TcParams& p, const Work& w,
+                                           uint32_t rank, int lane) {
+  uint32_t stage = 0, phase = 0;
+  int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
+  bool ok = true;
+  for (int m = 0; m < w.npages && ok; ++m) {
+    if (m % 32 == 0 && m > 0) {
+      cur = nxt;
+      nxt = page_base(p, w, m + 32 + lane);
     }
-    // The request's last page may be partly filled: rows past its length
-    // can hold anything (even NaN), and 0 * NaN would poison O = P V, so
-    // they are zeroed in every c_kv box before the MMA may read them.
-    const int64_t t0 = (w.p0 + j) * kTile;
-    if (zero_tail && t0 + kTile > w.L) {
+    const int32_t b = __shfl_sync(kFull, cur, m & 31);
+    const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
+    const uint32_t stage0 = stage, phase0 = phase;
+    if (lane == 0) {
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&s.full[stage]);
+        mbar_arrive_expect_tx(fb, kBoxesPerStage * kBoxBytes);
+        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage]);
+#pragma unroll
+        for (int q = 0; q < kBoxesPerStage; ++q)
+          tma_load_2d(dst + q * kBoxBytes, map, fb, (4 * h + q) * 64, y);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    stage = __shfl_sync(kFull, stage, 0);
+    phase = __shfl_sync(kFull, phase, 0);
+    if (!ok) break;
+    const int64_t t0 = (w.p0 + m) * kPage;
+    if (t0 + kPage > w.L) {
       const int keep = (int)(w.L - t0);
-      uint32_t sl = slot0, ph = phase0;
-      for (int c = 0; c < kBoxes; ++c) {
-        if (!mbar_wait(smem_u32(&s.full[sl]), ph, &s.abort_flag)) ok = false;
-        uint4* box = reinterpret_cast<uint4*>(s.ring[sl]);
-        for (int k = keep * 8 + lane; k < kTile * 8; k += 32)
-          box[k] = make_uint4(0, 0, 0, 0);
-        if (++sl == (uint32_t)kRingN) {
-          sl = 0;
+      uint32_t st = stage0, ph = phase0;
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait(smem_u32(&s.full[st]), ph, &s.abort_flag)) ok = false;
+        for (int q = 0; q < kBoxesPerStage; ++q) {
+          uint4* box = reinterpret_cast<uint4*>(s.ring[st * kBoxesPerStage + q]);
+          for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
+            box[k] = make_uint4(0, 0, 0, 0);
+        }
+        if (++st == kStages) {
+          st = 0;
           ph ^= 1u;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (!__all_sync(kFull, ok)) {
-        if (lane == 0) signal_abort(s, p, rank);
-        break;
-      }
-      if (lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
+      ok = __all_sync(kFull, ok);
+      if (ok && lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
     }
   }
+  if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
 // ---------------------------------------------------------- S-CTA: MMA ----
-__device__ void mma_s(Smem& s, const TcParams& p, const Work& w, uint32_t tmem,
-                      uint32_t rank) {
+__device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
+                                      const Work& w, uint32_t tmem,
+                                      uint32_t rank) {
   if (!mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) {
     signal_abort(s, p, rank);
     return;
   }
   tc_fence_after();
-  uint32_t slot = 0, phase = 0;
-  for (int j = 0; j < w.ntiles; ++j) {
-    const int sb = j % kNS;
-    if (!mbar_wait(smem_u32(&s.sempty[sb]), ((j / kNS) & 1) ^ 1u, &s.abort_flag)) {
+  const uint32_t d = tmem + kSCol0;
+  const uint64_t qr = sdesc_sw128(smem_u32(s.qrope), 16, 1024);
+  uint32_t stage = 0, phase = 0;
+  const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
+  for (int j = 0; j < ntiles; ++j) {
+    const uint32_t idesc = idesc_s(tile_pages(w, j));
+    // the softmax has read the previous tile's S out of TMEM
+    if (!mbar_wait(smem_u32(&s.sempty), (j & 1) ^ 1u, &s.abort_flag)) {
       signal_abort(s, p, rank);
       return;
     }
     tc_fence_after();
-    const uint32_t d = tmem + kSCol0 + 64u * sb;
     for (int c = 0; c < kBf16BoxesPerPage; ++c) {
-      if (!mbar_wait(smem_u32(&s.full[slot]), phase, &s.abort_flag)) {
+      if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
         signal_abort(s, p, rank);
         return;
       }
-      tc_fence_after();
-      const uint32_t b0 = smem_u32(s.ring[slot]);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int ks = c * 4 + kk;  // 16-element K step
-        mma_ts(d, tmem + 8u * ks, sdesc_sw128(b0 + 32u * kk, 16, 1024), kIdescS,
-               ks > 0);
+      const uint64_t b =
+          sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]), 16, 1024);
+      if (c < 8) {
+        // A = Q_nope from TMEM: K step ks = 4c + kk at column 8 ks; each K
+        // step advances B by 32 B (2 descriptor units).
+        mma_ts(d, tmem + 32u * c + 0, b + 0, idesc, c > 0 ? 1u : 0u);
+        mma_ts(d, tmem + 32u * c + 8, b + 2, idesc, 1u);
+        mma_ts(d, tmem + 32u * c + 16, b + 4, idesc, 1u);
+        mma_ts(d, tmem + 32u * c + 24, b + 6, idesc, 1u);
+      } else {
+        // A = Q_rope from shared memory (K-major, 128-B swizzle).
+        mma_ss(d, qr + 0, b + 0, idesc, 1u);
+        mma_ss(d, qr + 2, b + 2, idesc, 1u);
+        mma_ss(d, qr + 4, b + 4, idesc, 1u);
+        mma_ss(d, qr + 6, b + 6, idesc, 1u);
       }
-      mma_commit(smem_u32(&s.empty[slot]));
-      if (++slot == (uint32_t)kRingS) {
-        slot = 0;
+      mma_commit(smem_u32(&s.empty[stage]));
+      if (++stage == kStages) {
+        stage = 0;
         phase ^= 1u;
       }
     }
-    mma_commit(smem_u32(&s.sfull[sb]));
+    mma_commit(smem_u32(&s.sfull));
   }
 }
 
 // ------------------------------------------------------ S-CTA: softmax ----
-__device__ void softmax(Smem& s, const TcParams& p, const Work& w,
-                        uint32_t tmem, uint32_t rank, int warp, int lane) {
+// Warps 4..11: warpgroup g = 0 (warps 4-7) owns pages 0,1 of each S tile,
+// g = 1 (warps 8-11) pages 2,3.  Thread = query row r (TMEM lane).
+__device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
+                                        const Work& w, uint32_t tmem,
+                                        uint32_t rank, int warp, int lane) {
+  const int g = (warp - 4) >> 2;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -281,22 +357,33 @@ __device__ void softmax(Smem& s, const TcParams& p, const Work& w,
   }
   const int64_t qrow = (int64_t)w.b * p.q_len * p.H + rr;
 
-  // Q row -> TMEM columns [0, 288): 32-bit column c holds elements 2c, 2c+1.
+  // Q row: nope part -> TMEM columns [0, 256) (column c holds elements 2c,
+  // 2c+1), rope part -> shared memory in the K-major 128-B swizzled layout.
+  if (g == 0) {
 #pragma unroll 1
-  for (int c = 0; c < 9; ++c) {
-    uint32_t v[32];
-    const uint4* src = c < 8 ? p.q_nope + qrow * 64 + c * 8 : p.q_rope + qrow * 8;
+    for (int c = 0; c < 8; ++c) {
+      uint32_t v[32];
+      const uint4* src = p.q_nope + qrow * 64 + c * 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 x = row_ok ? src[k] : make_uint4(0, 0, 0, 0);
+        v[4 * k] = x.x;
+        v[4 * k + 1] = x.y;
+        v[4 * k + 2] = x.z;
+        v[4 * k + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_base + 32u * c, v);
+    }
+    tmem_wait_st();
+  } else {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint4 x = row_ok ? src[k] : make_uint4(0, 0, 0, 0);
-      v[4 * k] = x.x;
-      v[4 * k + 1] = x.y;
-      v[4 * k + 2] = x.z;
-      v[4 * k + 3] = x.w;
+      const uint4 x = row_ok ? p.q_rope[qrow * 8 + k] : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(s.qrope + (r >> 3) * 1024 +
+                                box_chunk_offset(r & 7, k)) = x;
     }
-    tmem_st32(tmem + lane_base + 32u * c, v);
+    fence_proxy_async_smem();
   }
-  tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&s.qready));
@@ -304,39 +391,66 @@ __device__ void softmax(Smem& s, const TcParams& p, const Work& w,
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
   const uint32_t peer_pfull0 = mapa(smem_u32(&s.pfull[0]), 1);
-  for (int j = 0; j < w.ntiles; ++j) {
-    const int sb = j % kNS;
-    const int k = j % kNP;
-    uint32_t sa[32], sb2[32];
-    if (ok && !mbar_wait(smem_u32(&s.sfull[sb]), (j / kNS) & 1, &s.abort_flag))
-      ok = false;
+  const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
+  const uint32_t bar_wg = 2 + g;  // named barrier of this warpgroup
+  const float sc = p.scale_log2;
+  for (int j = 0; j < ntiles; ++j) {
+    const int np = tile_pages(w, j);
+    const int myp = min(2, max(0, np - 2 * g));  // pages this warpgroup owns
+    uint32_t s0[32], s1[32], s2[32], s3[32];
+    if (ok && !mbar_wait(smem_u32(&s.sfull), j & 1, &s.abort_flag)) ok = false;
     tc_fence_after();
-    if (__all_sync(kFull, ok)) {
-      tmem_ld32(tmem + lane_base + kSCol0 + 64u * sb, sa);
-      tmem_ld32(tmem + lane_base + kSCol0 + 64u * sb + 32, sb2);
+    if (__all_sync(kFull, ok) && myp > 0) {
+      const uint32_t col = tmem + lane_base + kSCol0 + 128u * g;
+      tmem_ld32(col, s0);
+      tmem_ld32(col + 32, s1);
+      if (myp > 1) {
+        tmem_ld32(col + 64, s2);
+        tmem_ld32(col + 96, s3);
+      }
       tmem_wait_ld();
-    } else {
-      ok = false;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) sa[c] = sb2[c] = 0u;
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.sempty[sb]));
+    if (lane == 0) mbar_arrive(smem_u32(&s.sempty));
 
-    const int64_t t0 = (w.p0 + j) * kTile;
+    // Visible columns of this row among this warpgroup's 128 columns.
+    const int64_t t0 = (w.p0 + (int64_t)j * kTilePages + 2 * g) * kPage;
     const int64_t nv = n - t0;
-    const int nvis = nv <= 0 ? 0 : (nv >= kTile ? kTile : (int)nv);
-    float x[64];
-    float mt = -INFINITY;
+    const int nvis = nv <= 0 ? 0 : (nv >= 64 * myp ? 64 * myp : (int)nv);
+    // Scale to base 2 in place; columns this row may not see become -inf (a
+    // select: garbage or NaN in a masked column never propagates).
+    auto scale_mask = [&](uint32_t (&a)[32], int c0) {
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      x[c] = __uint_as_float(c < 32 ? sa[c] : sb2[c - 32]) * p.scale_log2;
-      if (c < nvis) mt = fmaxf(mt, x[c]);
-    }
+      for (int c = 0; c < 32; ++c)
+        a[c] = __float_as_uint(c0 + c < nvis ? __uint_as_float(a[c]) * sc
+                                             : -INFINITY);
+    };
+    scale_mask(s0, 0);
+    scale_mask(s1, 32);
+    scale_mask(s2, 64);
+    scale_mask(s3, 96);
+    auto xs = [&](int c) -> float {
+      return __uint_as_float(c < 32 ? s0[c] : c < 64 ? s1[c - 32]
+                                    : c < 96 ? s2[c - 64] : s3[c - 96]);
+    };
+    float mx[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      mx[c] = fmaxf(fmaxf(fmaxf(xs(c), xs(c + 16)), fmaxf(xs(c + 32), xs(c + 48))),
+                    fmaxf(fmaxf(xs(c + 64), xs(c + 80)), fmaxf(xs(c + 96), xs(c + 112))));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], mx[c + 8]);
+    const float mt_own = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    // Row maximum over the whole tile: exchange with the other warpgroup.
+    s.xch[g][r] = mt_own;
+    named_bar_sync(1, 256);
+    const float mt = fmaxf(mt_own, s.xch[g ^ 1][r]);
+    named_bar_sync(1, 256);  // both read before the next tile overwrites
     float alpha = 1.f;
-    if (nvis > 0) {
-      if (l == 0.f) {
+    if (mt > -INFINITY) {
+      if (m_ref == -INFINITY) {
         m_ref = mt;  // first visible token of this row: O is still zero
       } else if (mt > m_ref + kTau) {
         alpha = ex2(m_ref - mt);
@@ -344,82 +458,120 @@ __device__ void softmax(Smem& s, const TcParams& p, const Work& w,
         m_ref = mt;
       }
     }
+    // A row with nothing visible yet keeps m_ref = -inf: shift by 0 instead
+    // so every p is ex2(-inf) = 0, not NaN.
+    const float shift = m_ref == -INFINITY ? 0.f : m_ref;
 
-    // Wait until the peer has consumed the previous message in slot k.
-    if (ok && !mbar_wait(smem_u32(&s.pempty[k]), ((j / kNP) & 1) ^ 1u,
-                         &s.abort_flag))
-      ok = false;
-    uint8_t* stg = s.pslot[k];
-    float psum = 0.f;
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      uint32_t wv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c0 = cc * 8 + 2 * e;
-        const float pa = c0 < nvis ? ex2(x[c0] - m_ref) : 0.f;
-        const float pb = c0 + 1 < nvis ? ex2(x[c0 + 1] - m_ref) : 0.f;
-        psum += pa + pb;
-        wv[e] = pack_bf16(pa, pb);
+    // One page of P: 64 columns held in two 32-register arrays (constant
+    // indices only, so the scores stay in registers).
+    auto emit_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
+                         int q) {
+      const int msg = j * kTilePages + 2 * g + q;  // page index in the split
+      const int k = msg % kNP;
+      const int u = msg / kNP;  // use index of slot k
+      // Uses of a slot alternate between the two warpgroups, which run
+      // concurrently.  Before waiting for use u-1 to be consumed, make sure
+      // it has been sent: the consumed-barrier is then at phase u-1 or u,
+      // and its parity test cannot alias a phase two behind.
+      if (u > 0) {
+        if (ok && !mbar_wait(smem_u32(&s.sent[k]), (u - 1) & 1, &s.abort_flag))
+          ok = false;
+        if (ok && !mbar_wait(smem_u32(&s.pempty[k]), (u - 1) & 1, &s.abort_flag))
+          ok = false;
       }
-      // K-major, 128-B swizzle: 8-row groups 1024 B apart, 16-B chunk cc of
-      // row r at position cc ^ (r % 8) within its 128-B row.
-      *reinterpret_cast<uint4*>(stg + (r >> 3) * 1024 + box_chunk_offset(r & 7, cc)) =
-          make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      uint8_t* stg = s.pslot[k];
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = cc * 8 + 2 * e;
+          const float xa = __uint_as_float(c0 < 32 ? lo[c0] : hi[c0 - 32]);
+          const float xb = __uint_as_float(c0 + 1 < 32 ? lo[c0 + 1] : hi[c0 - 31]);
+          const float pa = ex2(xa - shift);
+          const float pb = ex2(xb - shift);
+          ps4[e] += pa + pb;
+          wv[e] = pack_bf16(pa, pb);
+        }
+        // K-major, 128-B swizzle: 8-row groups 1024 B apart, 16-B chunk cc
+        // of row r at position cc ^ (r % 8) within its 128-B row.
+        *reinterpret_cast<uint4*>(stg + (r >> 3) * 1024 +
+                                  box_chunk_offset(r & 7, cc)) =
+            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      // The tile's rescale travels with its first page only.
+      const bool first = (g == 0 && q == 0);
+      reinterpret_cast<float*>(stg + kAlphaOff)[r] = first ? alpha : 1.f;
+      const bool any = __any_sync(kFull, first && alpha != 1.f);
+      if (lane == 0)
+        reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
+      fence_proxy_async_smem();
+      named_bar_sync(bar_wg, 128);
+      if ((warp & 3) == 0 && lane == 0) {
+        if (s.abort_flag) {
+          ok = false;
+        } else {
+          // The peer armed pfull[k] with the byte count itself.
+          bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
+                            peer_pfull0 + 8u * k);
+        }
+        mbar_arrive(smem_u32(&s.sent[k]));  // also when skipped on abort
+      }
+    };
+    if (myp > 0) emit_page(s0, s1, 0);
+    if (myp > 1) emit_page(s2, s3, 1);
+  }
+
+  // Final statistics: l = sum of both warpgroups' partial sums.
+  s.xch[g][r] = l;
+  named_bar_sync(1, 256);
+  if (g == 0) {
+    const float lt = l + s.xch[1][r];
+    if (row_ok) {
+      const int64_t rows = (int64_t)p.B * p.q_len * p.H;
+      const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
+      p.LSE_part[part * rows + qrow] =
+          lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
     }
-    l += psum;
-    reinterpret_cast<float*>(stg + kAlphaOff)[r] = alpha;
-    const bool any = __any_sync(kFull, alpha != 1.f);
-    if (lane == 0) reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
+    s.fin[r] = lt > 0.f ? 1.f / lt : 0.f;
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0) {
-      if (s.abort_flag) {
+    named_bar_sync(2, 128);
+    if (warp == 4 && lane == 0 && !s.abort_flag)
+      bulk_copy_to_peer(mapa(smem_u32(s.fin), 1), smem_u32(s.fin), kRows * 4,
+                        mapa(smem_u32(&s.fin_full), 1));
+    // Before teardown: every P slot released by the peer, so no remote
+    // arrive can land after this CTA exits.
+    for (int m = max(0, w.npages - kNP); m < w.npages && ok; ++m)
+      if (!mbar_wait(smem_u32(&s.pempty[m % kNP]), (m / kNP) & 1,
+                     &s.abort_flag))
         ok = false;
-      } else {
-        const uint32_t rfull = peer_pfull0 + 8u * k;
-        mbar_arrive_expect_tx_cluster(rfull, kPMsgBytes);
-        bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes, rfull);
-      }
-    }
   }
-
-  // Final statistics: LSE to global, 1/l to the peer's epilogue.
-  if (row_ok) {
-    const int64_t rows = (int64_t)p.B * p.q_len * p.H;
-    const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-    p.LSE_part[part * rows + qrow] =
-        l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-  }
-  s.fin[r] = l > 0.f ? 1.f / l : 0.f;
-  fence_proxy_async_smem();
-  named_bar_sync(1, 128);
-  if (warp == 2 && lane == 0 && !s.abort_flag) {
-    const uint32_t rfin = mapa(smem_u32(&s.fin_full), 1);
-    mbar_arrive_expect_tx_cluster(rfin, kRows * 4);
-    bulk_copy_to_peer(mapa(smem_u32(s.fin), 1), smem_u32(s.fin), kRows * 4, rfin);
-  }
-  // Before teardown: every P slot released by the peer, so no remote arrive
-  // can land after this CTA exits.
-  for (int j = max(0, w.ntiles - kNP); j < w.ntiles && ok; ++j)
-    if (!mbar_wait(smem_u32(&s.pempty[j % kNP]), (j / kNP) & 1, &s.abort_flag))
-      ok = false;
   if (!__all_sync(kFull, ok) && lane == 0) signal_abort(s, p, rank);
 }
 
 // ---------------------------------------------------------- O-CTA: MMA ----
-__device__ void mma_o(Smem& s, const TcParams& p, const Work& w, uint32_t tmem,
-                      uint32_t rank) {
-  uint32_t slot = 0, phase = 0, ev = 0;
-  const bool has_tail = (w.p0 + w.ntiles) * kTile > w.L;
+__device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
+                                      const Work& w, uint32_t tmem,
+                                      uint32_t rank) {
+  uint32_t stage = 0, phase = 0, ev = 0;
+  const bool has_tail = (w.p0 + w.npages) * kPage > w.L;
   bool ok = true;
-  for (int j = 0; j < w.ntiles && ok; ++j) {
-    const int k = j % kNP;
-    if (!mbar_wait(smem_u32(&s.pfull[k]), (j / kNP) & 1, &s.abort_flag)) {
+  // Each P message lands by a bulk copy whose bytes complete on pfull[k];
+  // this CTA arms the barrier (one arrival + the byte count) itself, so the
+  // sender needs no cluster-scope arrive: the first use of each slot is armed
+  // at set-up, the next one as soon as a message has been received.
+  for (int m = 0; m < w.npages && ok; ++m) {
+    const int k = m % kNP;
+    if (!mbar_wait(smem_u32(&s.pfull[k]), (m / kNP) & 1, &s.abort_flag)) {
       ok = false;
       break;
     }
-    const uint32_t* fl = reinterpret_cast<const uint32_t*>(s.pslot[k] + kFlagOff);
+    if (m + kNP < w.npages)
+      mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes);
+    const uint32_t* fl =
+        reinterpret_cast<const uint32_t*>(s.pslot[k] + kFlagOff);
     if (fl[0] | fl[1] | fl[2] | fl[3]) {
       // Rows raised their running max: let the correction warps rescale O
       // once every earlier product has landed.
@@ -433,39 +585,34 @@ __device__ void mma_o(Smem& s, const TcParams& p, const Work& w, uint32_t tmem,
       }
       ++ev;
     }
-    if (has_tail && j == w.ntiles - 1 &&
+    if (has_tail && m == w.npages - 1 &&
         !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
       ok = false;
       break;
     }
-    const uint32_t pa = smem_u32(s.pslot[k]);
-    uint32_t used[8];
-    for (int h = 0; h < 2 && ok; ++h) {
-      for (int c = 0; c < 4; ++c) {
-        if (!mbar_wait(smem_u32(&s.full[slot]), phase, &s.abort_flag)) {
-          ok = false;
-          break;
-        }
-        used[4 * h + c] = slot;
-        if (++slot == (uint32_t)kRingO) {
-          slot = 0;
-          phase ^= 1u;
-        }
+    const uint64_t a = sdesc_sw128(smem_u32(s.pslot[k]), 16, 1024);
+    for (int h = 0; h < 2; ++h) {
+      if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+        ok = false;
+        break;
       }
-      if (!ok) break;
       tc_fence_after();
-      const uint32_t vb = smem_u32(s.ring[used[4 * h]]);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {  // 16 tokens per step
-        // A = P: K-major, 8-row groups 1024 B apart.  B = V: MN-major, next
-        // 64 dims one box (8 KB) on, next 8 tokens 1024 B on.
-        mma_ss(tmem + 256u * h, sdesc_sw128(pa + 32u * kk, 16, 1024),
-               sdesc_sw128(vb + 2048u * kk, kBoxBytes, 1024), kIdescO,
-               (j > 0 || kk > 0) ? 1u : 0u);
+      // B = V: MN-major, next 64 dims one box (8 KB) on, next 8 tokens 1 KB
+      // on; each 16-token K step advances 2048 B (128 descriptor units).
+      const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]),
+                                     kBoxBytes, 1024);
+      const uint32_t d = tmem + 256u * h;
+      mma_ss(d, a + 0, b + 0, kIdescO, m > 0 ? 1u : 0u);
+      mma_ss(d, a + 2, b + 128, kIdescO, 1u);
+      mma_ss(d, a + 4, b + 256, kIdescO, 1u);
+      mma_ss(d, a + 6, b + 384, kIdescO, 1u);
+      mma_commit(smem_u32(&s.empty[stage]));
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     if (!ok) break;
-    for (int c = 0; c < 8; ++c) mma_commit(smem_u32(&s.empty[used[c]]));
     mma_commit_multicast(smem_u32(&s.pempty[k]), (uint16_t)1u);  // S-CTA
   }
   if (!ok) signal_abort(s, p, rank);
@@ -475,9 +622,10 @@ __device__ void mma_o(Smem& s, const TcParams& p, const Work& w, uint32_t tmem,
 }
 
 // ---------------------------------------- O-CTA: correction + epilogue ----
-__device__ void correct_and_store(Smem& s, const TcParams& p, const Work& w,
-                                  uint32_t tmem, uint32_t rank, int warp,
-                                  int lane) {
+__device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
+                                                  const Work& w, uint32_t tmem,
+                                                  uint32_t rank, int warp,
+                                                  int lane) {
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -498,7 +646,8 @@ __device__ void correct_and_store(Smem& s, const TcParams& p, const Work& w,
         tmem_ld32(tmem + lane_base + c0, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+        for (int e = 0; e < 32; ++e)
+          v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
         tmem_st32(tmem + lane_base + c0, v);
       }
       tmem_wait_st();
@@ -552,27 +701,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     s.ctl_slot = 0;
     s.ctl_final = 0;
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
-    for (int i = 0; i < kNS; ++i) {
-      mbar_init(smem_u32(&s.sfull[i]), 1);
-      mbar_init(smem_u32(&s.sempty[i]), 4);
-    }
+    mbar_init(smem_u32(&s.sfull), 1);
+    mbar_init(smem_u32(&s.sempty), 8);   // the 8 softmax warps
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
       mbar_init(smem_u32(&s.pempty[i]), 1);
+      mbar_init(smem_u32(&s.sent[i]), 1);
     }
     mbar_init(smem_u32(&s.drain), 2);
     mbar_init(smem_u32(&s.corr_done), 4);
     mbar_init(smem_u32(&s.tail_ready), 1);
     mbar_init(smem_u32(&s.fin_full), 1);
-    mbar_init(smem_u32(&s.qready), 4);
+    mbar_init(smem_u32(&s.qready), 8);
+    if (rank == 1 && w.npages > 0) {
+      mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
+      for (int k = 0; k < kNP && k < w.npages; ++k)
+        mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes);
+    }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
   }
-  if (rank == 0 && threadIdx.x == 32 && w.L > p.r2t_stride && p.status)
+  if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
+      p.status)
     atomicOr(p.status, MLA_STATUS_BAD_LENGTH);
   if (warp == 1) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
@@ -584,45 +738,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
   cluster_sync();  // the peer's barriers exist before any remote operation
 
-  if (w.ntiles > 0) {
-    if (rank == 0) {
+  // Teardown, repeated at the end of every role: roles never rejoin, so no
+  // warp ever asks setmaxnreg for registers back (a warpgroup that did could
+  // take them before the softmax warpgroups got theirs and stall both).
+  auto teardown = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    cluster_sync();
+  };
+
+  if (w.npages > 0 && rank == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
       if (warp == 0)
-        producer<kBf16BoxesPerPage, kRingS>(s, &kv_map, p, w, rank, lane, false);
+        producer_s(s, &kv_map, p, w, rank, lane);
       else if (warp == 1) {
         if (lane == 0) mma_s(s, p, w, tmem, rank);
         __syncwarp();
-      } else
-        softmax(s, p, w, tmem, rank, warp, lane);
-    } else {
-      if (warp == 0)
-        producer<8, kRingO>(s, &kv_map, p, w, rank, lane, true);
-      else if (warp == 1) {
-        if (lane == 0) mma_o(s, p, w, tmem, rank);
-        __syncwarp();
-      } else
-        correct_and_store(s, p, w, tmem, rank, warp, lane);
+      }
+      teardown();
+      return;
     }
-  } else if (warp >= 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    softmax(s, p, w, tmem, rank, warp, lane);
+    teardown();
+    return;
+  }
+  if (w.npages > 0) {
+    if (warp == 0)
+      producer_o(s, &kv_map, p, w, rank, lane);
+    else if (warp == 1) {
+      if (lane == 0) mma_o(s, p, w, tmem, rank);
+      __syncwarp();
+    } else if (warp >= 4 && warp < 8)
+      correct_and_store(s, p, w, tmem, rank, warp, lane);
+  } else if (warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0, LSE = -inf.
     const int r = (warp & 3) * 32 + lane;
     if (r < w.nrows) {
       const int64_t rows = (int64_t)p.B * p.q_len * p.H;
       const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-      const int64_t orow = part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r;
+      const int64_t orow =
+          part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r;
       if (rank == 0) {
         p.LSE_part[orow] = -INFINITY;
       } else {
         float4* d4 = reinterpret_cast<float4*>(p.O_part + orow * MLA_VALUE_DIM);
-        for (int e = 0; e < MLA_VALUE_DIM / 4; ++e) d4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < MLA_VALUE_DIM / 4; ++e)
+          d4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
   }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
-  cluster_sync();
+  teardown();
 }
 
 }  // namespace
@@ -683,7 +852,9 @@ extern "C" int mla_pair_slots(void) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, mla::mla_partial_tc_kernel, &cfg);
-  if (e != cudaSuccess) return mla::cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+  e = cudaOccupancyMaxActiveClusters(&clusters, mla::mla_partial_tc_kernel,
+                                     &cfg);
+  if (e != cudaSuccess)
+    return mla::cuda_fail(e, "cudaOccupancyMaxActiveClusters");
   return clusters;
 }

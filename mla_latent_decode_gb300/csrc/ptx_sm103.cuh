@@ -77,11 +77,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`.  Returns false on timeout or when
-// *abort becomes non-zero (another warp of the CTA gave up first).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: spin with a time limit.  (Inlined: kernels that
+// rebalance registers with setmaxnreg cannot make real calls there.)
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar,
+                                                      uint32_t parity,
+                                                      volatile int* abort) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it != 0; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -91,6 +91,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
   }
   return false;
+}
+
+// Wait for phase `parity` of `bar`.  Returns false on timeout or when
+// *abort becomes non-zero (another warp of the CTA gave up first).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort) {
+  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------- cluster
