@@ -187,33 +187,28 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
       nxt = page_base(p, w, m0 + 32 + lane);
     }
     const int np = tile_pages(w, j);
-    // Page bases of this tile, one per lane q < 4 (a page outside the pool
-    // reads a row past the end, which TMA fills with zeros).
+    // Lane q < np owns page q of this tile (a page outside the pool reads a
+    // row past the end, which TMA fills with zeros); the np boxes of a stage
+    // then go out as one TMA instruction across those lanes.
     const int32_t bq = __shfl_sync(kFull, cur, (m0 + (lane & 3)) & 31);
     const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
     if (lane < np && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
-    const int32_t y0 = __shfl_sync(kFull, yq, 0), y1 = __shfl_sync(kFull, yq, 1);
-    const int32_t y2 = __shfl_sync(kFull, yq, 2), y3 = __shfl_sync(kFull, yq, 3);
-    if (lane == 0) {
-      for (int c = 0; c < kBf16BoxesPerPage; ++c) {
-        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+    for (int c = 0; c < kBf16BoxesPerPage && ok; ++c) {
+      if (lane == 0) {
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
+          mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * kBoxBytes);
+        else
           ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&s.full[stage]);
-        mbar_arrive_expect_tx(fb, np * kBoxBytes);
-        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage]);
-        tma_load_2d(dst, map, fb, c * 64, y0);
-        if (np > 1) tma_load_2d(dst + kBoxBytes, map, fb, c * 64, y1);
-        if (np > 2) tma_load_2d(dst + 2 * kBoxBytes, map, fb, c * 64, y2);
-        if (np > 3) tma_load_2d(dst + 3 * kBoxBytes, map, fb, c * 64, y3);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      if (ok && lane < np)
+        tma_load_2d(smem_u32(s.ring[stage * kBoxesPerStage + lane]), map,
+                    smem_u32(&s.full[stage]), c * 64, yq);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
-    ok = __shfl_sync(kFull, ok, 0);
   }
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
@@ -237,27 +232,24 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     const int32_t b = __shfl_sync(kFull, cur, m & 31);
     const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
     const uint32_t stage0 = stage, phase0 = phase;
-    if (lane == 0) {
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+    for (int h = 0; h < 2 && ok; ++h) {
+      if (lane == 0) {
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
+          mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
+                                kBoxesPerStage * kBoxBytes);
+        else
           ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&s.full[stage]);
-        mbar_arrive_expect_tx(fb, kBoxesPerStage * kBoxBytes);
-        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage]);
-#pragma unroll
-        for (int q = 0; q < kBoxesPerStage; ++q)
-          tma_load_2d(dst + q * kBoxBytes, map, fb, (4 * h + q) * 64, y);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      // Lane q < 4 loads the 64 dims [256h + 64q, +64) of the page.
+      if (ok && lane < kBoxesPerStage)
+        tma_load_2d(smem_u32(s.ring[stage * kBoxesPerStage + lane]), map,
+                    smem_u32(&s.full[stage]), (4 * h + lane) * 64, y);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
-    ok = __shfl_sync(kFull, ok, 0);
-    stage = __shfl_sync(kFull, stage, 0);
-    phase = __shfl_sync(kFull, phase, 0);
     if (!ok) break;
     const int64_t t0 = (w.p0 + m) * kPage;
     if (t0 + kPage > w.L) {
@@ -462,10 +454,29 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     // so every p is ex2(-inf) = 0, not NaN.
     const float shift = m_ref == -INFINITY ? 0.f : m_ref;
 
-    // One page of P: 64 columns held in two 32-register arrays (constant
-    // indices only, so the scores stay in registers).
-    auto emit_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
-                         int q) {
+    // P of both pages, packed bf16 pairs, computed before any wait for a
+    // message slot so the exponentials stay off the cross-SM round trip.
+    uint32_t pk0[32], pk1[32];
+    auto make_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
+                         uint32_t (&pk)[32]) {
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int c0 = 2 * c;
+        const float xa = __uint_as_float(c0 < 32 ? lo[c0] : hi[c0 - 32]);
+        const float xb = __uint_as_float(c0 + 1 < 32 ? lo[c0 + 1] : hi[c0 - 31]);
+        const float pa = ex2(xa - shift);
+        const float pb = ex2(xb - shift);
+        ps4[c & 3] += pa + pb;
+        pk[c] = pack_bf16(pa, pb);
+      }
+      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+    };
+    if (myp > 0) make_page(s0, s1, pk0);
+    if (myp > 1) make_page(s2, s3, pk1);
+
+    // Ship one page: wait for its slot, store, hand it to the peer.
+    auto emit_page = [&](const uint32_t (&pk)[32], int q) {
       const int msg = j * kTilePages + 2 * g + q;  // page index in the split
       const int k = msg % kNP;
       const int u = msg / kNP;  // use index of slot k
@@ -480,27 +491,13 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
           ok = false;
       }
       uint8_t* stg = s.pslot[k];
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t wv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c0 = cc * 8 + 2 * e;
-          const float xa = __uint_as_float(c0 < 32 ? lo[c0] : hi[c0 - 32]);
-          const float xb = __uint_as_float(c0 + 1 < 32 ? lo[c0 + 1] : hi[c0 - 31]);
-          const float pa = ex2(xa - shift);
-          const float pb = ex2(xb - shift);
-          ps4[e] += pa + pb;
-          wv[e] = pack_bf16(pa, pb);
-        }
+      for (int cc = 0; cc < 8; ++cc)
         // K-major, 128-B swizzle: 8-row groups 1024 B apart, 16-B chunk cc
         // of row r at position cc ^ (r % 8) within its 128-B row.
         *reinterpret_cast<uint4*>(stg + (r >> 3) * 1024 +
                                   box_chunk_offset(r & 7, cc)) =
-            make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      }
-      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       // The tile's rescale travels with its first page only.
       const bool first = (g == 0 && q == 0);
       reinterpret_cast<float*>(stg + kAlphaOff)[r] = first ? alpha : 1.f;
@@ -520,8 +517,8 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
         mbar_arrive(smem_u32(&s.sent[k]));  // also when skipped on abort
       }
     };
-    if (myp > 0) emit_page(s0, s1, 0);
-    if (myp > 1) emit_page(s2, s3, 1);
+    if (myp > 0) emit_page(pk0, 0);
+    if (myp > 1) emit_page(pk1, 1);
   }
 
   // Final statistics: l = sum of both warpgroups' partial sums.
