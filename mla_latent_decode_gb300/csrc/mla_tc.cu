@@ -41,10 +41,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 384;        // 12 warps = 3 warpgroups
-constexpr int kStages = 5;           // 32-KB ring stages (4 boxes each)
+constexpr int kStages = 4;           // 32-KB ring stages (4 boxes each)
 constexpr int kBoxesPerStage = 4;
 constexpr int kTilePages = 4;        // pages per S tile (N <= 256)
-constexpr int kNP = 2;               // P message slots
+constexpr int kNP = 4;               // P message slots (page index mod 4)
 constexpr int kRows = MLA_ROWS_PER_PAIR;  // 128
 constexpr int kPage = MLA_PAGE_SIZE;      // 64 tokens
 constexpr int kPBytes = kRows * kPage * 2;          // 16384
@@ -71,7 +71,7 @@ __host__ __device__ constexpr uint32_t idesc_s(int pages) {
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
 
 struct __align__(1024) Smem {
-  uint8_t ring[kStages * kBoxesPerStage][kBoxBytes];  // 160 KB
+  uint8_t ring[kStages * kBoxesPerStage][kBoxBytes];  // 128 KB
   uint8_t qrope[kRows * 128];                         // S-CTA: Q_rope rows
   uint8_t pslot[kNP][kPSlotStride];
   float fin[kRows];
@@ -277,20 +277,25 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
 }
 
 // ---------------------------------------------------------- S-CTA: MMA ----
+// Two issuing threads (warps 1 and 2) split every S tile by pages: half h
+// computes the columns of pages 2h, 2h+1 (N = 64 or 128) into TMEM columns
+// [256 + 128h, +128).  The accumulators are disjoint, and each thread's
+// barrier waits and commits overlap the other thread's MMAs.
 __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
-                                      uint32_t rank) {
+                                      uint32_t rank, int half) {
   if (!mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) {
     signal_abort(s, p, rank);
     return;
   }
   tc_fence_after();
-  const uint32_t d = tmem + kSCol0;
+  const uint32_t d = tmem + kSCol0 + 128u * half;
   const uint64_t qr = sdesc_sw128(smem_u32(s.qrope), 16, 1024);
   uint32_t stage = 0, phase = 0;
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles; ++j) {
-    const uint32_t idesc = idesc_s(tile_pages(w, j));
+    const int mine = min(2, max(0, tile_pages(w, j) - 2 * half));
+    const uint32_t idesc = idesc_s(mine > 0 ? mine : 1);
     // the softmax has read the previous tile's S out of TMEM
     if (!mbar_wait(smem_u32(&s.sempty), (j & 1) ^ 1u, &s.abort_flag)) {
       signal_abort(s, p, rank);
@@ -302,23 +307,25 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
         signal_abort(s, p, rank);
         return;
       }
-      const uint64_t b =
-          sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]), 16, 1024);
-      if (c < 8) {
-        // A = Q_nope from TMEM: K step ks = 4c + kk at column 8 ks; each K
-        // step advances B by 32 B (2 descriptor units).
-        mma_ts(d, tmem + 32u * c + 0, b + 0, idesc, c > 0 ? 1u : 0u);
-        mma_ts(d, tmem + 32u * c + 8, b + 2, idesc, 1u);
-        mma_ts(d, tmem + 32u * c + 16, b + 4, idesc, 1u);
-        mma_ts(d, tmem + 32u * c + 24, b + 6, idesc, 1u);
-      } else {
-        // A = Q_rope from shared memory (K-major, 128-B swizzle).
-        mma_ss(d, qr + 0, b + 0, idesc, 1u);
-        mma_ss(d, qr + 2, b + 2, idesc, 1u);
-        mma_ss(d, qr + 4, b + 4, idesc, 1u);
-        mma_ss(d, qr + 6, b + 6, idesc, 1u);
+      if (mine > 0) {
+        const uint64_t b = sdesc_sw128(
+            smem_u32(s.ring[stage * kBoxesPerStage + 2 * half]), 16, 1024);
+        if (c < 8) {
+          // A = Q_nope from TMEM: K step ks = 4c + kk at column 8 ks; each K
+          // step advances B by 32 B (2 descriptor units).
+          mma_ts(d, tmem + 32u * c + 0, b + 0, idesc, c > 0 ? 1u : 0u);
+          mma_ts(d, tmem + 32u * c + 8, b + 2, idesc, 1u);
+          mma_ts(d, tmem + 32u * c + 16, b + 4, idesc, 1u);
+          mma_ts(d, tmem + 32u * c + 24, b + 6, idesc, 1u);
+        } else {
+          // A = Q_rope from shared memory (K-major, 128-B swizzle).
+          mma_ss(d, qr + 0, b + 0, idesc, 1u);
+          mma_ss(d, qr + 2, b + 2, idesc, 1u);
+          mma_ss(d, qr + 4, b + 4, idesc, 1u);
+          mma_ss(d, qr + 6, b + 6, idesc, 1u);
+        }
       }
-      mma_commit(smem_u32(&s.empty[stage]));
+      mma_commit(smem_u32(&s.empty[stage]));  // both halves release a stage
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
@@ -700,9 +707,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.ctl_final = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
-      mbar_init(smem_u32(&s.empty[i]), 1);
+      mbar_init(smem_u32(&s.empty[i]), rank == 0 ? 2 : 1);  // S: two MMA threads
     }
-    mbar_init(smem_u32(&s.sfull), 1);
+    mbar_init(smem_u32(&s.sfull), 2);
     mbar_init(smem_u32(&s.sempty), 8);   // the 8 softmax warps
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
@@ -751,8 +758,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
       if (warp == 0)
         producer_s(s, &kv_map, p, w, rank, lane);
-      else if (warp == 1) {
-        if (lane == 0) mma_s(s, p, w, tmem, rank);
+      else if (warp == 1 || warp == 2) {
+        if (lane == 0) mma_s(s, p, w, tmem, rank, warp - 1);
         __syncwarp();
       }
       teardown();
