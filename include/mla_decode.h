@@ -176,6 +176,8 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   kv_limit         int32 [num_shards*B, q_len] or NULL
  *   num_shards       token-interleaved context shards sharing one Q (1 = none)
  *   page_size        must be 64 (else MLA_ERR_UNSUPPORTED)
+ *   sm_scale         softmax scale, finite and > 0 (1/sqrt(192) for the
+ *                    192-d pre-absorption query/key head)
  *   num_splits       KV splits per request, >= 1 (see mla_plan)
  *   O_part           fp32 [num_splits, num_shards, B, q_len, H, 512], 16-B al.
  *   LSE_part         fp32 [num_splits, num_shards, B, q_len, H]

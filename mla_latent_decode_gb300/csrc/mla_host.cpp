@@ -55,8 +55,9 @@ int check_decode_args(const DecodeArgs& a) {
   if (a.r2t_stride < 1)
     return fail(MLA_ERR_INVALID_ARG, "r2t_stride %lld < 1",
                 (long long)a.r2t_stride);
-  if (!std::isfinite(a.sm_scale))
-    return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (!std::isfinite(a.sm_scale) || !(a.sm_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "sm_scale %g is not a positive number",
+                (double)a.sm_scale);
   if (!aligned(a.q_nope, 16) || !aligned(a.q_rope, 16) || !aligned(a.kv, 16) ||
       !aligned(a.O_part, 16) || !aligned(a.LSE_part, 4) ||
       !aligned(a.req_to_token, 4) || !aligned(a.seq_lens, 4) ||

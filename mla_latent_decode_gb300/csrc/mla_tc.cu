@@ -81,7 +81,6 @@ struct __align__(1024) Smem {
   uint64_t sfull, sempty;
   uint64_t pfull[kNP];
   uint64_t pempty[kNP];
-  uint64_t sent[kNP];       // S-CTA: one arrival per message sent in slot k
   uint64_t drain, corr_done, tail_ready, fin_full, qready;
   uint32_t tmem_base;
   int abort_flag;
@@ -116,6 +115,33 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Three-operand maximum (one ALU instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Packed pair arithmetic: two fp32 lanes per instruction.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  return x;
+}
+__device__ __forceinline__ void f2unpack(uint64_t x, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Record a failed wait: device status, this CTA's and the peer's abort flag.
@@ -417,31 +443,38 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     const int64_t t0 = (w.p0 + (int64_t)j * kTilePages + 2 * g) * kPage;
     const int64_t nv = n - t0;
     const int nvis = nv <= 0 ? 0 : (nv >= 64 * myp ? 64 * myp : (int)nv);
-    // Scale to base 2 in place; columns this row may not see become -inf (a
-    // select: garbage or NaN in a masked column never propagates).
-    auto scale_mask = [&](uint32_t (&a)[32], int c0) {
+    // Columns this row may not see become -inf (a select: garbage or NaN in
+    // a masked column never propagates).  Only the tiles at the end of the
+    // split need it; on every other tile all 128 columns of every row of the
+    // warp are visible and the scores are used as loaded.
+    if (!__all_sync(kFull, nvis == 128)) {
+      auto mask = [&](uint32_t (&a)[32], int c0) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        a[c] = __float_as_uint(c0 + c < nvis ? __uint_as_float(a[c]) * sc
-                                             : -INFINITY);
-    };
-    scale_mask(s0, 0);
-    scale_mask(s1, 32);
-    scale_mask(s2, 64);
-    scale_mask(s3, 96);
+        for (int c = 0; c < 32; ++c)
+          a[c] = c0 + c < nvis ? a[c] : __float_as_uint(-INFINITY);
+      };
+      mask(s0, 0);
+      mask(s1, 32);
+      mask(s2, 64);
+      mask(s3, 96);
+    }
     auto xs = [&](int c) -> float {
       return __uint_as_float(c < 32 ? s0[c] : c < 64 ? s1[c - 32]
                                     : c < 96 ? s2[c - 64] : s3[c - 96]);
     };
+    // Row maximum of the raw scores; the scale is positive, so the maximum
+    // of the scaled scores is the scaled maximum (rounding is monotone).
     float mx[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      mx[c] = fmaxf(fmaxf(fmaxf(xs(c), xs(c + 16)), fmaxf(xs(c + 32), xs(c + 48))),
-                    fmaxf(fmaxf(xs(c + 64), xs(c + 80)), fmaxf(xs(c + 96), xs(c + 112))));
-#pragma unroll
-    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], mx[c + 8]);
-    const float mt_own = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      mx[c] = fmaxf(max3(xs(c), xs(c + 16), xs(c + 32)),
+                    max3(max3(xs(c + 48), xs(c + 64), xs(c + 80)), xs(c + 96),
+                         xs(c + 112)));
+    const float m5a = max3(mx[0], mx[1], mx[2]), m5b = max3(mx[3], mx[4], mx[5]);
+    const float m5c = max3(mx[6], mx[7], mx[8]), m5d = max3(mx[9], mx[10], mx[11]);
+    const float m5e = max3(mx[12], mx[13], mx[14]);
+    const float mt_own =
+        max3(max3(m5a, m5b, m5c), max3(m5d, m5e, mx[15]), -INFINITY) * sc;
     // Row maximum over the whole tile: exchange with the other warpgroup.
     s.xch[g][r] = mt_own;
     named_bar_sync(1, 256);
@@ -464,39 +497,42 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     // P of both pages, packed bf16 pairs, computed before any wait for a
     // message slot so the exponentials stay off the cross-SM round trip.
     uint32_t pk0[32], pk1[32];
+    // p = 2^(x * scale - m_ref): one packed FMA per pair of columns, the row
+    // sum in two packed accumulators.
+    const uint64_t sc2 = f2pack(sc, sc), nshift2 = f2pack(-shift, -shift);
     auto make_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
                          uint32_t (&pk)[32]) {
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const int c0 = 2 * c;
         const float xa = __uint_as_float(c0 < 32 ? lo[c0] : hi[c0 - 32]);
         const float xb = __uint_as_float(c0 + 1 < 32 ? lo[c0 + 1] : hi[c0 - 31]);
-        const float pa = ex2(xa - shift);
-        const float pb = ex2(xb - shift);
-        ps4[c & 3] += pa + pb;
+        float ya, yb;
+        f2unpack(ffma2(f2pack(xa, xb), sc2, nshift2), ya, yb);
+        const float pa = ex2(ya), pb = ex2(yb);
+        if (c & 1) acc1 = fadd2(acc1, f2pack(pa, pb));
+        else acc0 = fadd2(acc0, f2pack(pa, pb));
         pk[c] = pack_bf16(pa, pb);
       }
-      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      float a0, a1, b0, b1;
+      f2unpack(acc0, a0, a1);
+      f2unpack(acc1, b0, b1);
+      l += (a0 + a1) + (b0 + b1);
     };
     if (myp > 0) make_page(s0, s1, pk0);
     if (myp > 1) make_page(s2, s3, pk1);
 
-    // Ship one page: wait for its slot, store, hand it to the peer.
+    // Ship one page: wait for its slot, store, hand it to the peer.  Slot
+    // k = (2g + q) belongs to this warpgroup and page position alone (four
+    // slots, four pages per tile), so its uses are sequential here.
     auto emit_page = [&](const uint32_t (&pk)[32], int q) {
       const int msg = j * kTilePages + 2 * g + q;  // page index in the split
       const int k = msg % kNP;
       const int u = msg / kNP;  // use index of slot k
-      // Uses of a slot alternate between the two warpgroups, which run
-      // concurrently.  Before waiting for use u-1 to be consumed, make sure
-      // it has been sent: the consumed-barrier is then at phase u-1 or u,
-      // and its parity test cannot alias a phase two behind.
-      if (u > 0) {
-        if (ok && !mbar_wait(smem_u32(&s.sent[k]), (u - 1) & 1, &s.abort_flag))
-          ok = false;
-        if (ok && !mbar_wait(smem_u32(&s.pempty[k]), (u - 1) & 1, &s.abort_flag))
-          ok = false;
-      }
+      if (u > 0 && ok &&
+          !mbar_wait(smem_u32(&s.pempty[k]), (u - 1) & 1, &s.abort_flag))
+        ok = false;
       uint8_t* stg = s.pslot[k];
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
@@ -513,16 +549,10 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
         reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
       fence_proxy_async_smem();
       named_bar_sync(bar_wg, 128);
-      if ((warp & 3) == 0 && lane == 0) {
-        if (s.abort_flag) {
-          ok = false;
-        } else {
-          // The peer armed pfull[k] with the byte count itself.
-          bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
-                            peer_pfull0 + 8u * k);
-        }
-        mbar_arrive(smem_u32(&s.sent[k]));  // also when skipped on abort
-      }
+      if ((warp & 3) == 0 && lane == 0 && ok && !s.abort_flag)
+        // The peer armed pfull[k] with the byte count itself.
+        bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
+                          peer_pfull0 + 8u * k);
     };
     if (myp > 0) emit_page(pk0, 0);
     if (myp > 1) emit_page(pk1, 1);
@@ -714,7 +744,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
       mbar_init(smem_u32(&s.pempty[i]), 1);
-      mbar_init(smem_u32(&s.sent[i]), 1);
     }
     mbar_init(smem_u32(&s.drain), 2);
     mbar_init(smem_u32(&s.corr_done), 4);
