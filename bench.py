@@ -264,7 +264,7 @@ def main():
     wl = synth.config(args.config)
     batch = synth.make_batch(wl, seed=rank, device="cuda")
     lens = mla.batch_lengths(batch)
-    slots = mla.pair_slots()
+    slots = mla.cluster_slots()
     if args.splits > 0:
         S, eff = args.splits, None
     elif wl.num_splits:
@@ -399,7 +399,7 @@ def main():
                 "H": wl.H, "context": wl.seq_lens[0] if len(set(wl.seq_lens)) == 1 else "ragged",
                 "num_shards": wl.num_shards, "num_splits": S,
                 "planner_wave_eff": eff, "pages_rule_splits": S_pages,
-                "pair_slots": slots,
+                "cluster_slots": slots,
                 "l2": f"inputs larger than L2 ({batch.kv.numel() * batch.kv.element_size() / 1e9:.2f} GB KV), no flush",
                 "parallelism": f"dp{world} (independent requests per rank)",
             },

@@ -80,7 +80,7 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 #define MLA_ROPE_DIM 64   /* qk_rope_head_dim */
 #define MLA_VALUE_DIM 512
 #define MLA_PAGE_SIZE 64  /* the only page size the kernels are built for */
-#define MLA_ROWS_PER_PAIR 128 /* query rows one CTA pair owns */
+#define MLA_ROWS_PER_UNIT 256 /* query rows one work unit (a 4-CTA cluster) owns */
 
 /* Last error message of this thread ("" if none).  Owned by the library. */
 const char* mla_last_error_string(void);
@@ -89,10 +89,11 @@ const char* mla_last_error_string(void);
  * MLA_ERR_* code. */
 int mla_num_sms(int device);
 
-/* Number of CTA pairs of the decode kernel that can be resident at once on
- * the current device (cudaOccupancyMaxActiveClusters with the kernel's
- * cluster size, block size and shared memory), or a negative MLA_ERR_*. */
-int mla_pair_slots(void);
+/* Number of work units of the tensor-core decode kernel (clusters of four
+ * CTAs, one CTA per SM) that can be resident at once on the current device
+ * (cudaOccupancyMaxActiveClusters with the kernel's cluster size, block size
+ * and shared memory), or a negative MLA_ERR_*. */
+int mla_cluster_slots(void);
 
 /*
  * The pages' split rule, reproduced for comparison ([K3-MLA]):
@@ -104,17 +105,17 @@ int mla_plan_heuristic(int B, int q_len);
 
 /*
  * Wave-rounding split planner (replaces the rule above; [K3-MLA] shows that
- * rule leaving a partial second wave).  Work units are CTA pairs, one per
- * (virtual request v, split s, row group g) with G = ceil(H*q_len / 128) row
- * groups, launched in that order.  For every S in [1, s_max] the unit costs
+ * rule leaving a partial second wave).  Work units are 4-CTA clusters, one per
+ * (virtual request v, split s, row unit u) with U = ceil(H*q_len / 256) row
+ * units, launched in that order (u fastest).  For every S in [1, s_max] the unit costs
  * pages(v, s) + c0 page tiles, where request v's P_v = ceil(L_v / 64) pages
  * are dealt as floor((s+1) P_v / S) - floor(s P_v / S); the units are list-
- * scheduled onto `slots` pair slots in launch order; the objective is
+ * scheduled onto `slots` cluster slots in launch order; the objective is
  *   J(S) = makespan(S) + lam * S * rows / 1024,   rows = V * q_len * H,
  * (the second term prices the partial outputs each extra split writes and
  * the combine re-reads).  The smallest J wins, ties go to fewer splits.
  *   seq_lens_host  host int32 [V] (V = num_shards * B virtual requests)
- *   slots          concurrent pair slots (> 0)
+ *   slots          concurrent cluster slots (> 0)
  *   s_max          largest split count considered (1..1024)
  *   num_splits_out chosen S;  wave_eff_out: sum(unit cost)/(slots*makespan);
  *   makespan_out   makespan in page tiles (may be NULL)
@@ -125,8 +126,8 @@ int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
                 double* makespan_out);
 
 /*
- * mla_plan_ex with the library's defaults: slots = mla_pair_slots() when
- * num_sms == 0, else num_sms / 2; s_max = 64; c0 = 4; lam = 1.
+ * mla_plan_ex with the library's defaults: slots = mla_cluster_slots() when
+ * num_sms == 0, else num_sms / 4; s_max = 64; c0 = 4; lam = 1.
  *   B, num_shards  requests and context shards (V = B * num_shards);
  *   seq_lens_host  host int32 [num_shards * B] (shard-local lengths).
  */

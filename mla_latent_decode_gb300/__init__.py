@@ -52,7 +52,7 @@ def library() -> ctypes.CDLL:
         sig = {
             "mla_last_error_string": (ctypes.c_char_p, []),
             "mla_num_sms": (i32, [i32]),
-            "mla_pair_slots": (i32, []),
+            "mla_cluster_slots": (i32, []),
             "mla_plan_heuristic": (i32, [i32, i32]),
             "mla_plan_ex": (i32, [i32, i32, i32, p, i32, i32, f64, f64, p, p, p]),
             "mla_plan": (i32, [i32, i32, i32, i32, p, i32, p, p]),
@@ -98,9 +98,10 @@ def num_sms(device: int = 0) -> int:
     return _check(library().mla_num_sms(device))
 
 
-def pair_slots() -> int:
-    """Concurrently resident CTA pairs of the decode kernel on this device."""
-    return _check(library().mla_pair_slots())
+def cluster_slots() -> int:
+    """Concurrently resident work units (4-CTA clusters) of the tensor-core
+    decode kernel on this device."""
+    return _check(library().mla_cluster_slots())
 
 
 def plan_heuristic(B: int, q_len: int) -> int:

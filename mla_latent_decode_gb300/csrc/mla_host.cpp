@@ -116,7 +116,7 @@ int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
     return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
   if (slots < 1 || s_max < 1 || s_max > 1024 || !(c0 >= 0) || !(lam >= 0))
     return fail(MLA_ERR_INVALID_ARG, "slots/s_max/c0/lam out of range");
-  const int G = (H * q_len + MLA_ROWS_PER_PAIR - 1) / MLA_ROWS_PER_PAIR;
+  const int G = (H * q_len + MLA_ROWS_PER_UNIT - 1) / MLA_ROWS_PER_UNIT;
   const double rows = (double)V * q_len * H;
   double bestJ = 0, bestEff = 0, bestMs = 0;
   int bestS = 0;
@@ -157,11 +157,11 @@ int mla_plan(int B, int q_len, int H, int num_shards,
     return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
   int slots;
   if (num_sms > 0) {
-    slots = std::max(1, num_sms / 2);
+    slots = std::max(1, num_sms / 4);
   } else {
-    slots = mla_pair_slots();
+    slots = mla_cluster_slots();
     if (slots < 0) return slots;
-    if (slots == 0) return fail(MLA_ERR_CUDA, "no CTA pair fits on this device");
+    if (slots == 0) return fail(MLA_ERR_CUDA, "no 4-CTA cluster fits on this device");
   }
   return mla_plan_ex(B * num_shards, q_len, H, seq_lens_host, slots, 64, 4.0,
                      1.0, num_splits_out, wave_eff_out, nullptr);

@@ -5,31 +5,34 @@
 // [VRAM-POOL]), partial (O, LSE) per KV split and context shard ([K3-MLA],
 // [K3-SPLIT]), causal among the q_len draft tokens ([K3-INTRO]).
 //
-// Design (GB300, one CTA per SM):
+// Design (GB300, one CTA per SM, clusters of four):
 //   All H*q_len query rows of a request share one latent KV row per token, so
 //   S = Q K^T (576-d) and O = P V (512-d, V = the c_kv columns of the same
 //   row) are dense contractions with M = query rows.  A 128-row fp32 O
-//   accumulator over 512 values fills all 512 TMEM columns of an SM, so one
-//   128-row group is served by a cluster of two CTAs:
-//     rank 0, the "S-CTA": Q_nope (bf16 pairs) in TMEM columns [0, 256),
-//       Q_rope in shared memory, one S buffer of up to 256 columns (an S tile
-//       is up to 4 pages = 256 tokens).  K arrives in 32-KB stages (one
-//       64-dim chunk of the tile's pages, 128-byte swizzled TMA boxes); each
-//       stage feeds 4 MMAs of M=128, N=64*pages, K=16.  Two softmax
-//       warpgroups own two pages each, exchange row maxima once per tile,
-//       keep base-2 running statistics with lazy rescaling, and ship each
-//       page's P (bf16, K-major, 128-byte swizzled) plus rescale factors to
-//       the peer with a bulk shared-memory copy.
-//     rank 1, the "O-CTA": O (128 x 512 fp32) in all of TMEM; V (the c_kv
-//       columns) arrives in 32-KB stages (256 dims of one page); each P
-//       message feeds 8 MMAs of M=128, N=256, K=16 (A = P from shared memory,
-//       B = V MN-major).  Correction warps rescale O rows when the S-CTA
-//       raised a running max, then write the normalised O_part rows.
-//   A barrier wait or a tcgen05.commit costs the single issuing thread
-//   ~70-100 cycles that the tensor pipe does not hide, so every stage is
-//   sized to carry four MMAs of up to 256 columns (512 tensor cycles) per
-//   wait/commit pair.  Every wait is bounded (ptx_sm103.cuh); a timeout sets
-//   MLA_STATUS_WAIT_TIMEOUT and the CTA pair finishes early.
+//   accumulator over 512 values fills all 512 TMEM columns of an SM, so the
+//   scores and the output of a 128-row group live on two SMs.  An SM's TMA
+//   engine lands 64-row KV boxes at ~45 B/clk, while an M = 128 bf16 MMA
+//   consumes 64 B/clk of K, so the KV tile of one MMA is split over two SMs
+//   with the CTA-pair (cta_group::2) MMA, M = 256 rows = two row groups:
+//     ranks 0,1, the "S pair": rank r owns row group 2u + r: Q_nope (bf16
+//       pairs) in TMEM columns [0, 256), Q_rope in shared memory, one S
+//       buffer of 256 columns (an S tile = 4 pages = 256 tokens).  Rank r
+//       loads pages 2r, 2r+1 of every tile in 16-KB stages (one 64-dim chunk
+//       of its two pages, 128-byte swizzled TMA boxes); each stage feeds 4
+//       pair MMAs of M=256, N=256, K=16 issued by rank 0.  Two softmax
+//       warpgroups per CTA own two pages each, exchange row maxima once per
+//       tile, keep base-2 running statistics with lazy rescaling, and ship
+//       each page's P (bf16, K-major, 128-byte swizzled) plus rescale
+//       factors to their O-CTA with a bulk shared-memory copy.
+//     ranks 2,3, the "O pair": rank 2+r holds O (128 x 512 fp32) of row group
+//       2u + r in all of its TMEM and loads half of V: dims [256n + 128r,
+//       +128) of each page for the two 256-wide halves n; each page feeds 8
+//       pair MMAs of M=256, N=256, K=16 (A = P, B = V MN-major) issued by
+//       rank 2.  Correction warps rescale O rows when an S-CTA raised a
+//       running max, then write the normalised O_part rows.
+//   Per SM the TMA then lands 16 KB per 512 tensor cycles.  Every wait is
+//   bounded (ptx_sm103.cuh); a timeout sets MLA_STATUS_WAIT_TIMEOUT and the
+//   cluster finishes early.
 #include <cuda_bf16.h>
 
 #include "mla_tma.cuh"
@@ -41,21 +44,25 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 384;        // 12 warps = 3 warpgroups
-constexpr int kStages = 4;           // 32-KB ring stages (4 boxes each)
-constexpr int kBoxesPerStage = 4;
-constexpr int kTilePages = 4;        // pages per S tile (N <= 256)
+constexpr int kCtas = 4;             // S pair (ranks 0,1) + O pair (ranks 2,3)
+constexpr int kStages = 8;           // 16-KB ring stages (2 boxes each)
+constexpr int kBoxesPerStage = 2;
+constexpr int kTilePages = 4;        // pages per S tile (N = 256), 2 per S-CTA
 constexpr int kNP = 4;               // P message slots (page index mod 4)
-constexpr int kRows = MLA_ROWS_PER_PAIR;  // 128
-constexpr int kPage = MLA_PAGE_SIZE;      // 64 tokens
+constexpr int kRows = MLA_ROWS_PER_UNIT / 2;  // 128 query rows per CTA
+constexpr int kPage = MLA_PAGE_SIZE;           // 64 tokens
 constexpr int kPBytes = kRows * kPage * 2;          // 16384
 constexpr int kAlphaOff = kPBytes;                  // float alpha[128]
 constexpr int kFlagOff = kPBytes + kRows * 4;       // uint32 flags[4]
 constexpr int kPMsgBytes = kFlagOff + 16;           // 16912 = 1057 x 16
+constexpr int kPeerFlagOff = kPMsgBytes;            // rank 2: rank 1's flags
 constexpr int kPSlotStride = 17408;                 // 17 KB, 1024-aligned
 constexpr uint32_t kSCol0 = 256;                    // S buffer columns
 constexpr float kTau = 8.f;          // lazy-rescale threshold (log2 units)
 constexpr uint32_t kFull = 0xffffffffu;
-// Register split of the S-CTA (setmaxnreg): 384 threads launch with 168
+constexpr uint16_t kMaskS = 0x3;     // cluster ranks of the S pair
+constexpr uint16_t kMaskO = 0xC;     // cluster ranks of the O pair
+// Register split of the S-CTAs (setmaxnreg): 384 threads launch with 168
 // registers each (64,512); the producer/MMA warpgroup gives registers away so
 // the two softmax warpgroups can hold a 128 x 256 fp32 score tile.  The split
 // is one-way: nobody asks for registers back before the CTA exits.
@@ -65,10 +72,8 @@ constexpr int kRegsSoftmax = 216;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 
-__host__ __device__ constexpr uint32_t idesc_s(int pages) {
-  return idesc_bf16_f32(128, 64 * pages, false, false);
-}
-constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
+constexpr uint32_t kIdescS = idesc_bf16_f32(256, 256, false, false);
+constexpr uint32_t kIdescO = idesc_bf16_f32(256, 256, false, true);
 
 struct __align__(1024) Smem {
   uint8_t ring[kStages * kBoxesPerStage][kBoxBytes];  // 128 KB
@@ -76,12 +81,19 @@ struct __align__(1024) Smem {
   uint8_t pslot[kNP][kPSlotStride];
   float fin[kRows];
   float xch[2][kRows];      // S-CTA: per-warpgroup row maxima / partial sums
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t sfull, sempty;
-  uint64_t pfull[kNP];
-  uint64_t pempty[kNP];
-  uint64_t drain, corr_done, tail_ready, fin_full, qready;
+  uint64_t full[kStages];   // pair leader: the stage landed in both CTAs
+  uint64_t empty[kStages];  // every CTA: its half of the stage was consumed
+  uint64_t sfull;           // S-CTAs: the S tile is in TMEM
+  uint64_t sempty;          // rank 0: both S-CTAs read the S tile (16 warps)
+  uint64_t pfull[kNP];      // O-CTAs: the P message of slot k landed here
+  uint64_t pready[kNP];     // rank 2: rank 3's message of slot k landed
+  uint64_t pempty[kNP];     // S-CTAs: slot k consumed by the O pair
+  uint64_t drain;           // O-CTAs: all earlier pair MMAs completed
+  uint64_t corr_done;       // rank 2: both O-CTAs finished a rescale
+  uint64_t tail_full;       // O-CTAs: the last, partial page landed here
+  uint64_t tail_ready;      // rank 2: both halves of that page sanitised
+  uint64_t fin_full;        // O-CTAs: 1/l of every row arrived
+  uint64_t qready;          // rank 0: both S-CTAs' Q rows are in place
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -90,6 +102,7 @@ struct __align__(1024) Smem {
 constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kPMsgBytes % 16 == 0, "bulk copy size");
+static_assert(kPeerFlagOff + 16 <= kPSlotStride, "P slot layout");
 
 struct TcParams {
   const uint4* q_nope;     // bf16 [B, q_len, H, 512] as 16-B chunks
@@ -99,7 +112,7 @@ struct TcParams {
   int64_t r2t_stride;
   const int32_t* seq_lens;
   const int32_t* kv_limit;
-  int B, q_len, H, V, num_splits, G;
+  int B, q_len, H, V, num_splits, U;  // U = row pairs (256 rows) per request
   float scale_log2;        // sm_scale * log2(e)
   float* O_part;
   float* LSE_part;
@@ -144,32 +157,62 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Record a failed wait: device status, this CTA's and the peer's abort flag.
+// Arrive on a barrier of the pair leader `lead`: a local arrive when this CTA
+// is the leader, otherwise a release at cluster scope, which publishes this
+// thread's earlier writes (shared memory, TMEM stores) to the leader.
+__device__ __forceinline__ void arrive_leader(uint32_t bar, uint32_t rank,
+                                              uint32_t lead) {
+  if (rank == lead)
+    mbar_arrive(bar);
+  else
+    mbar_arrive_cluster(mapa(bar, lead));
+}
+
+// The same for a signal that only reports completed work: the thread has
+// already waited for its own TMEM loads or stores (tcgen05.wait) or seen the
+// data land on a barrier, so nothing remains to publish and the arrive can be
+// relaxed.  A remote release costs the issuing thread hundreds to thousands
+// of cycles under load; a relaxed remote arrive a few.
+__device__ __forceinline__ void signal_leader(uint32_t bar, uint32_t rank,
+                                              uint32_t lead) {
+  if (rank == lead) {
+    mbar_arrive(bar);
+  } else {
+    asm volatile(
+        "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+            mapa(bar, lead))
+        : "memory");
+  }
+}
+
+// Record a failed wait: device status and every CTA's abort flag.
 __device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
                                              uint32_t rank) {
   if (p.status) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
   s.abort_flag = 1;
-  st_cluster_u32(mapa(smem_u32(&s.abort_flag), rank ^ 1u), 1u);
+  for (uint32_t c = 0; c < kCtas; ++c)
+    if (c != rank) st_cluster_u32(mapa(smem_u32(&s.abort_flag), c), 1u);
 }
 
-// Per-pair work description, identical on both CTAs of the pair.
+// Work of one cluster: (virtual request v, split, row pair u); this CTA's
+// row group is 2u + (rank & 1).
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
   int64_t L, p0;
 };
 
-__device__ __forceinline__ Work pair_work(const TcParams& p) {
+__device__ __forceinline__ Work unit_work(const TcParams& p, uint32_t rank) {
   Work w;
-  int pair = blockIdx.x >> 1;
-  const int g = pair % p.G;
-  pair /= p.G;
-  w.split = pair % p.num_splits;
-  w.v = pair / p.num_splits;
+  int unit = blockIdx.x / kCtas;
+  const int u = unit % p.U;
+  unit /= p.U;
+  w.split = unit % p.num_splits;
+  w.v = unit / p.num_splits;
   w.b = w.v % p.B;
   w.shard = w.v / p.B;
   const int R = p.q_len * p.H;
-  w.r_base = g * kRows;
-  w.nrows = min(kRows, R - w.r_base);
+  w.r_base = (2 * u + (int)(rank & 1)) * kRows;
+  w.nrows = max(0, min(kRows, R - w.r_base));
   int64_t L = p.seq_lens[w.v];
   if (L > p.r2t_stride) L = p.r2t_stride;
   if (L < 0) L = 0;
@@ -185,7 +228,7 @@ __device__ __forceinline__ int tile_pages(const Work& w, int j) {
   return min(kTilePages, w.npages - j * kTilePages);
 }
 
-// Base slot of page m of the pair's range, or -1 if it lies outside the pool.
+// Base slot of page m of the unit's range, or -1 if it lies outside the pool.
 __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
                                              int m) {
   if (m >= w.npages) return 0;
@@ -195,16 +238,22 @@ __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
   return base;
 }
 
-// -------------------------------------------------------- S-CTA producer ---
-// Stage = one 64-dim chunk of the (up to 4) pages of an S tile.  Page bases
-// are read 32 pages ahead (one per lane) so a TMA issue never waits on a
-// dependent global load.
+// ------------------------------------------------------- S-CTA producers ---
+// Rank r loads pages 2r, 2r+1 of every S tile; stage = one 64-dim chunk of
+// those pages (the pair MMA's N = 256 rows: rank 0's 128, then rank 1's).
+// The bytes of both CTAs complete on the leader's full barrier, which the
+// leader arms with the tile's total; each CTA refills a stage once the pair
+// MMA released it (empty, multicast to both).  Page bases are read 32 pages
+// ahead (one per lane) so a TMA issue never waits on a dependent global
+// load.  Pages of a short last tile that are not loaded leave stale bytes in
+// the S columns they feed, which the softmax masks.
 __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
   uint32_t stage = 0, phase = 0;
   int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
+  const uint32_t full0 = mapa(smem_u32(&s.full[0]), 0);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles && ok; ++j) {
     const int m0 = j * kTilePages;
@@ -213,23 +262,26 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
       nxt = page_base(p, w, m0 + 32 + lane);
     }
     const int np = tile_pages(w, j);
-    // Lane q < np owns page q of this tile (a page outside the pool reads a
-    // row past the end, which TMA fills with zeros); the np boxes of a stage
-    // then go out as one TMA instruction across those lanes.
-    const int32_t bq = __shfl_sync(kFull, cur, (m0 + (lane & 3)) & 31);
+    const int mine = min(2, max(0, np - 2 * (int)rank));
+    // Lane q < mine loads page 2r + q of the tile (a page outside the pool
+    // reads a row past the end, which TMA fills with zeros).
+    const int32_t bq =
+        __shfl_sync(kFull, cur, (m0 + 2 * (int)rank + (lane & 1)) & 31);
     const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
-    if (lane < np && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
+    if (lane < mine && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
     for (int c = 0; c < kBf16BoxesPerPage && ok; ++c) {
       if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
-          mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * kBoxBytes);
-        else
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+          if (rank == 0)
+            mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * kBoxBytes);
+        } else {
           ok = false;
+        }
       }
       ok = __shfl_sync(kFull, ok, 0);
-      if (ok && lane < np)
-        tma_load_2d(smem_u32(s.ring[stage * kBoxesPerStage + lane]), map,
-                    smem_u32(&s.full[stage]), c * 64, yq);
+      if (ok && lane < mine)
+        tma_load_2d_pair(smem_u32(s.ring[stage * kBoxesPerStage + lane]), map,
+                         full0 + 8u * stage, c * 64, yq);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
@@ -239,17 +291,21 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
-// -------------------------------------------------------- O-CTA producer ---
-// Stage = 256 c_kv dims of one page (4 boxes): two stages per page.  The
-// request's last page may be partly filled: rows past its length can hold
-// anything (even NaN) and 0 * NaN would poison O = P V, so they are zeroed
-// before the MMA may read them.
+// ------------------------------------------------------- O-CTA producers ---
+// Rank 2+h loads dims [256n + 128h, +128) of every page (2 boxes) for the
+// two N halves n: one stage each, bytes of both CTAs completing on rank 2's
+// full barrier.  A request's last page may be partly filled: rows past its
+// length can hold anything (even NaN) and 0 * NaN would poison O = P V, so
+// that page lands on the CTA's own tail barrier instead, its rows past the
+// length are zeroed, and both CTAs then report to rank 2 (tail_ready).
 __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
   uint32_t stage = 0, phase = 0;
   int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
+  const int h = (int)rank - 2;
+  const uint32_t full0 = mapa(smem_u32(&s.full[0]), 2);
   for (int m = 0; m < w.npages && ok; ++m) {
     if (m % 32 == 0 && m > 0) {
       cur = nxt;
@@ -257,72 +313,77 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     }
     const int32_t b = __shfl_sync(kFull, cur, m & 31);
     const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
-    const uint32_t stage0 = stage, phase0 = phase;
-    for (int h = 0; h < 2 && ok; ++h) {
+    const int64_t t0 = (w.p0 + m) * kPage;
+    const bool partial = t0 + kPage > w.L;
+    const uint32_t stage0 = stage;
+    for (int n = 0; n < 2 && ok; ++n) {
       if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
-          mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
-                                kBoxesPerStage * kBoxBytes);
-        else
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+          if (partial) {
+            if (n == 0)
+              mbar_arrive_expect_tx(smem_u32(&s.tail_full),
+                                    2 * kBoxesPerStage * kBoxBytes);
+          } else if (rank == 2) {
+            mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
+                                  2 * kBoxesPerStage * kBoxBytes);
+          }
+        } else {
           ok = false;
+        }
       }
       ok = __shfl_sync(kFull, ok, 0);
-      // Lane q < 4 loads the 64 dims [256h + 64q, +64) of the page.
-      if (ok && lane < kBoxesPerStage)
-        tma_load_2d(smem_u32(s.ring[stage * kBoxesPerStage + lane]), map,
-                    smem_u32(&s.full[stage]), (4 * h + lane) * 64, y);
+      if (ok && lane < kBoxesPerStage) {
+        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage + lane]);
+        const int x = (256 * n + 128 * h + 64 * lane);
+        if (partial)
+          tma_load_2d(dst, map, smem_u32(&s.tail_full), x, y);
+        else
+          tma_load_2d_pair(dst, map, full0 + 8u * stage, x, y);
+      }
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    if (!ok) break;
-    const int64_t t0 = (w.p0 + m) * kPage;
-    if (t0 + kPage > w.L) {
-      const int keep = (int)(w.L - t0);
-      uint32_t st = stage0, ph = phase0;
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait(smem_u32(&s.full[st]), ph, &s.abort_flag)) ok = false;
-        for (int q = 0; q < kBoxesPerStage; ++q) {
-          uint4* box = reinterpret_cast<uint4*>(s.ring[st * kBoxesPerStage + q]);
-          for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
-            box[k] = make_uint4(0, 0, 0, 0);
-        }
-        if (++st == kStages) {
-          st = 0;
-          ph ^= 1u;
-        }
+    if (!ok || !partial) continue;
+    // The partial page is the request's last: zero its rows past the length.
+    const int keep = (int)(w.L - t0);
+    if (!mbar_wait(smem_u32(&s.tail_full), 0, &s.abort_flag)) ok = false;
+    uint32_t st = stage0;
+    for (int n = 0; n < 2; ++n) {
+      for (int q = 0; q < kBoxesPerStage; ++q) {
+        uint4* box = reinterpret_cast<uint4*>(s.ring[st * kBoxesPerStage + q]);
+        for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
+          box[k] = make_uint4(0, 0, 0, 0);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      ok = __all_sync(kFull, ok);
-      if (ok && lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
+      if (++st == kStages) st = 0;
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    ok = __all_sync(kFull, ok);
+    if (ok && lane == 0) arrive_leader(smem_u32(&s.tail_ready), rank, 2);
   }
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
-// ---------------------------------------------------------- S-CTA: MMA ----
-// Two issuing threads (warps 1 and 2) split every S tile by pages: half h
-// computes the columns of pages 2h, 2h+1 (N = 64 or 128) into TMEM columns
-// [256 + 128h, +128).  The accumulators are disjoint, and each thread's
-// barrier waits and commits overlap the other thread's MMAs.
+// --------------------------------------------------- S pair: MMA (rank 0) ----
+// One thread issues every S-tile MMA of the pair: S[256 rows, 256 tokens] +=
+// Q[:, chunk] x K[tokens, chunk]^T, chunks 0..7 with A = Q_nope from TMEM,
+// chunk 8 with A = Q_rope from shared memory.
 __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
-                                      uint32_t rank, int half) {
+                                      uint32_t rank) {
   if (!mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) {
     signal_abort(s, p, rank);
     return;
   }
   tc_fence_after();
-  const uint32_t d = tmem + kSCol0 + 128u * half;
+  const uint32_t d = tmem + kSCol0;
   const uint64_t qr = sdesc_sw128(smem_u32(s.qrope), 16, 1024);
   uint32_t stage = 0, phase = 0;
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles; ++j) {
-    const int mine = min(2, max(0, tile_pages(w, j) - 2 * half));
-    const uint32_t idesc = idesc_s(mine > 0 ? mine : 1);
-    // the softmax has read the previous tile's S out of TMEM
+    // both S-CTAs have read the previous tile's S out of TMEM
     if (!mbar_wait(smem_u32(&s.sempty), (j & 1) ^ 1u, &s.abort_flag)) {
       signal_abort(s, p, rank);
       return;
@@ -333,37 +394,38 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
         signal_abort(s, p, rank);
         return;
       }
-      if (mine > 0) {
-        const uint64_t b = sdesc_sw128(
-            smem_u32(s.ring[stage * kBoxesPerStage + 2 * half]), 16, 1024);
-        if (c < 8) {
-          // A = Q_nope from TMEM: K step ks = 4c + kk at column 8 ks; each K
-          // step advances B by 32 B (2 descriptor units).
-          mma_ts(d, tmem + 32u * c + 0, b + 0, idesc, c > 0 ? 1u : 0u);
-          mma_ts(d, tmem + 32u * c + 8, b + 2, idesc, 1u);
-          mma_ts(d, tmem + 32u * c + 16, b + 4, idesc, 1u);
-          mma_ts(d, tmem + 32u * c + 24, b + 6, idesc, 1u);
-        } else {
-          // A = Q_rope from shared memory (K-major, 128-B swizzle).
-          mma_ss(d, qr + 0, b + 0, idesc, 1u);
-          mma_ss(d, qr + 2, b + 2, idesc, 1u);
-          mma_ss(d, qr + 4, b + 4, idesc, 1u);
-          mma_ss(d, qr + 6, b + 6, idesc, 1u);
-        }
+      tc_fence_after();
+      const uint64_t b =
+          sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]), 16, 1024);
+      if (c < 8) {
+        // A = Q_nope from TMEM: K step ks = 4c + kk at column 8 ks; each K
+        // step advances B by 32 B (2 descriptor units).
+        mma_ts_pair(d, tmem + 32u * c + 0, b + 0, kIdescS, c > 0 ? 1u : 0u);
+        mma_ts_pair(d, tmem + 32u * c + 8, b + 2, kIdescS, 1u);
+        mma_ts_pair(d, tmem + 32u * c + 16, b + 4, kIdescS, 1u);
+        mma_ts_pair(d, tmem + 32u * c + 24, b + 6, kIdescS, 1u);
+      } else {
+        // A = Q_rope from shared memory (K-major, 128-B swizzle).
+        mma_ss_pair(d, qr + 0, b + 0, kIdescS, 1u);
+        mma_ss_pair(d, qr + 2, b + 2, kIdescS, 1u);
+        mma_ss_pair(d, qr + 4, b + 4, kIdescS, 1u);
+        mma_ss_pair(d, qr + 6, b + 6, kIdescS, 1u);
       }
-      mma_commit(smem_u32(&s.empty[stage]));  // both halves release a stage
+      mma_commit_pair(smem_u32(&s.empty[stage]), kMaskS);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    mma_commit(smem_u32(&s.sfull));
+    mma_commit_pair(smem_u32(&s.sfull), kMaskS);
   }
 }
 
 // ------------------------------------------------------ S-CTA: softmax ----
-// Warps 4..11: warpgroup g = 0 (warps 4-7) owns pages 0,1 of each S tile,
-// g = 1 (warps 8-11) pages 2,3.  Thread = query row r (TMEM lane).
+// Warps 4..11 of each S-CTA: warpgroup g = 0 (warps 4-7) owns pages 0,1 of
+// each S tile, g = 1 (warps 8-11) pages 2,3 (S columns [128g, +128), which
+// the pair MMA fills from both CTAs' halves of the tile).  Thread = query
+// row r (TMEM lane) of this CTA's row group.
 __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
                                         const Work& w, uint32_t tmem,
                                         uint32_t rank, int warp, int lane) {
@@ -411,11 +473,12 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   }
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&s.qready));
+  if (lane == 0) arrive_leader(smem_u32(&s.qready), rank, 0);
 
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
-  const uint32_t peer_pfull0 = mapa(smem_u32(&s.pfull[0]), 1);
+  const uint32_t orank = rank + 2;  // the O-CTA of this row group
+  const uint32_t peer_pfull0 = mapa(smem_u32(&s.pfull[0]), orank);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   const uint32_t bar_wg = 2 + g;  // named barrier of this warpgroup
   const float sc = p.scale_log2;
@@ -437,7 +500,7 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.sempty));
+    if (lane == 0) signal_leader(smem_u32(&s.sempty), rank, 0);
 
     // Visible columns of this row among this warpgroup's 128 columns.
     const int64_t t0 = (w.p0 + (int64_t)j * kTilePages + 2 * g) * kPage;
@@ -549,10 +612,17 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
         reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
       fence_proxy_async_smem();
       named_bar_sync(bar_wg, 128);
-      if ((warp & 3) == 0 && lane == 0 && ok && !s.abort_flag)
-        // The peer armed pfull[k] with the byte count itself.
-        bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
-                          peer_pfull0 + 8u * k);
+      if ((warp & 3) == 0 && lane == 0 && ok && !s.abort_flag) {
+        // The receiver armed pfull[k] with the byte count itself.
+        bulk_copy_to_peer(mapa(smem_u32(stg), orank), smem_u32(stg),
+                          kPMsgBytes, peer_pfull0 + 8u * k);
+        // Rank 2 issues the pair's P x V MMAs and decides on rescales: it
+        // gets rank 1's rescale flags too, counted on its own pfull[k].
+        if (rank == 1)
+          bulk_copy_to_peer(mapa(smem_u32(stg + kPeerFlagOff), 2),
+                            smem_u32(stg + kFlagOff), 16,
+                            mapa(smem_u32(&s.pfull[k]), 2));
+      }
     };
     if (myp > 0) emit_page(pk0, 0);
     if (myp > 1) emit_page(pk1, 1);
@@ -573,9 +643,9 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     fence_proxy_async_smem();
     named_bar_sync(2, 128);
     if (warp == 4 && lane == 0 && !s.abort_flag)
-      bulk_copy_to_peer(mapa(smem_u32(s.fin), 1), smem_u32(s.fin), kRows * 4,
-                        mapa(smem_u32(&s.fin_full), 1));
-    // Before teardown: every P slot released by the peer, so no remote
+      bulk_copy_to_peer(mapa(smem_u32(s.fin), orank), smem_u32(s.fin),
+                        kRows * 4, mapa(smem_u32(&s.fin_full), orank));
+    // Before teardown: every P slot released by the O pair, so no remote
     // arrive can land after this CTA exits.
     for (int m = max(0, w.npages - kNP); m < w.npages && ok; ++m)
       if (!mbar_wait(smem_u32(&s.pempty[m % kNP]), (m / kNP) & 1,
@@ -585,48 +655,61 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   if (!__all_sync(kFull, ok) && lane == 0) signal_abort(s, p, rank);
 }
 
-// ---------------------------------------------------------- O-CTA: MMA ----
+// --------------------------------------------------- O pair: MMA (rank 2) ----
+// One thread issues every P x V MMA of the pair: for each page m (message
+// slot k = m mod 4) it needs the P rows of both O-CTAs (its own pfull, which
+// also counts rank 1's rescale flags, and rank 3's through pready), then
+// O[:, 256n + (0..255)] += P x V for n = 0, 1.
 __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
                                       uint32_t rank) {
   uint32_t stage = 0, phase = 0, ev = 0;
   const bool has_tail = (w.p0 + w.npages) * kPage > w.L;
   bool ok = true;
+  const uint32_t drain3 = mapa(smem_u32(&s.drain), 3);
   // Each P message lands by a bulk copy whose bytes complete on pfull[k];
-  // this CTA arms the barrier (one arrival + the byte count) itself, so the
-  // sender needs no cluster-scope arrive: the first use of each slot is armed
-  // at set-up, the next one as soon as a message has been received.
+  // the receiving CTA arms the barrier (one arrival + the byte count)
+  // itself, so the sender needs no cluster-scope arrive: the first use of
+  // each slot is armed at set-up, the next one as soon as a message has been
+  // received (here for rank 2, by the relay thread for rank 3).
   for (int m = 0; m < w.npages && ok; ++m) {
     const int k = m % kNP;
-    if (!mbar_wait(smem_u32(&s.pfull[k]), (m / kNP) & 1, &s.abort_flag)) {
+    const uint32_t par = (m / kNP) & 1;
+    if (!mbar_wait(smem_u32(&s.pfull[k]), par, &s.abort_flag) ||
+        !mbar_wait(smem_u32(&s.pready[k]), par, &s.abort_flag)) {
       ok = false;
       break;
     }
     if (m + kNP < w.npages)
-      mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes);
+      mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes + 16);
     const uint32_t* fl =
         reinterpret_cast<const uint32_t*>(s.pslot[k] + kFlagOff);
-    if (fl[0] | fl[1] | fl[2] | fl[3]) {
-      // Rows raised their running max: let the correction warps rescale O
-      // once every earlier product has landed.
+    const uint32_t* pf =
+        reinterpret_cast<const uint32_t*>(s.pslot[k] + kPeerFlagOff);
+    if (fl[0] | fl[1] | fl[2] | fl[3] | pf[0] | pf[1] | pf[2] | pf[3]) {
+      // Rows of either O-CTA raised their running max: let both CTAs'
+      // correction warps rescale once every earlier product has landed.
       s.ctl_slot = k;
       s.ctl_final = 0;
-      mma_commit(smem_u32(&s.drain));
+      st_cluster_u32(mapa(smem_u32(&s.ctl_slot), 3), (uint32_t)k);
+      st_cluster_u32(mapa(smem_u32(&s.ctl_final), 3), 0u);
+      mma_commit_pair(smem_u32(&s.drain), kMaskO);
       mbar_arrive(smem_u32(&s.drain));
+      mbar_arrive_cluster(drain3);
       if (!mbar_wait(smem_u32(&s.corr_done), ev & 1, &s.abort_flag)) {
         ok = false;
         break;
       }
       ++ev;
     }
-    if (has_tail && m == w.npages - 1 &&
-        !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
+    const bool tail = has_tail && m == w.npages - 1;
+    if (tail && !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
       ok = false;
       break;
     }
     const uint64_t a = sdesc_sw128(smem_u32(s.pslot[k]), 16, 1024);
-    for (int h = 0; h < 2; ++h) {
-      if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+    for (int n = 0; n < 2; ++n) {
+      if (!tail && !mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
         ok = false;
         break;
       }
@@ -635,27 +718,54 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       // on; each 16-token K step advances 2048 B (128 descriptor units).
       const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]),
                                      kBoxBytes, 1024);
-      const uint32_t d = tmem + 256u * h;
-      mma_ss(d, a + 0, b + 0, kIdescO, m > 0 ? 1u : 0u);
-      mma_ss(d, a + 2, b + 128, kIdescO, 1u);
-      mma_ss(d, a + 4, b + 256, kIdescO, 1u);
-      mma_ss(d, a + 6, b + 384, kIdescO, 1u);
-      mma_commit(smem_u32(&s.empty[stage]));
+      const uint32_t d = tmem + 256u * n;
+      mma_ss_pair(d, a + 0, b + 0, kIdescO, m > 0 ? 1u : 0u);
+      mma_ss_pair(d, a + 2, b + 128, kIdescO, 1u);
+      mma_ss_pair(d, a + 4, b + 256, kIdescO, 1u);
+      mma_ss_pair(d, a + 6, b + 384, kIdescO, 1u);
+      mma_commit_pair(smem_u32(&s.empty[stage]), kMaskO);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    mma_commit_multicast(smem_u32(&s.pempty[k]), (uint16_t)1u);  // S-CTA
+    mma_commit_pair(smem_u32(&s.pempty[k]), kMaskS);  // both S-CTAs
   }
   if (!ok) signal_abort(s, p, rank);
   s.ctl_final = 1;
-  mma_commit(smem_u32(&s.drain));
+  st_cluster_u32(mapa(smem_u32(&s.ctl_final), 3), 1u);
+  mma_commit_pair(smem_u32(&s.drain), kMaskO);
   mbar_arrive(smem_u32(&s.drain));
+  mbar_arrive_cluster(drain3);
+}
+
+// --------------------------------------------------- O pair: relay (rank 3) ----
+// Tells rank 2 when a P message has landed in rank 3 (bulk-copy bytes can
+// only complete on a barrier of the receiving CTA), and re-arms the slot.
+__device__ __forceinline__ void relay_o(Smem& s, const TcParams& p,
+                                        const Work& w, uint32_t rank) {
+  const uint32_t pready0 = mapa(smem_u32(&s.pready[0]), 2);
+  for (int m = 0; m < w.npages; ++m) {
+    const int k = m % kNP;
+    if (!mbar_wait(smem_u32(&s.pfull[k]), (m / kNP) & 1, &s.abort_flag)) {
+      signal_abort(s, p, rank);
+      return;
+    }
+    if (m + kNP < w.npages)
+      mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes);
+    asm volatile(
+        "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+            pready0 + 8u * k)
+        : "memory");
+  }
 }
 
 // ---------------------------------------- O-CTA: correction + epilogue ----
+// Warps 4..7 of each O-CTA, thread = row r of this CTA's row group.  A
+// drain event (every earlier pair MMA complete) either asks for a rescale of
+// the rows whose running max rose (factors in the P slot that triggered it)
+// or, the last one, for the epilogue: O_part = O / l.
 __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
                                                   const Work& w, uint32_t tmem,
                                                   uint32_t rank, int warp,
@@ -688,7 +798,7 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.corr_done));
+    if (lane == 0) signal_leader(smem_u32(&s.corr_done), rank, 2);
   }
   if (ok && !mbar_wait(smem_u32(&s.fin_full), 0, &s.abort_flag)) ok = false;
   if (!__all_sync(kFull, ok)) {
@@ -721,7 +831,7 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
 }
 
 // ------------------------------------------------------------- kernel ----
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                           const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -729,7 +839,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
-  const Work w = pair_work(p);
+  const Work w = unit_work(p, rank);
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -737,23 +847,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.ctl_final = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
-      mbar_init(smem_u32(&s.empty[i]), rank == 0 ? 2 : 1);  // S: two MMA threads
+      mbar_init(smem_u32(&s.empty[i]), 1);
     }
-    mbar_init(smem_u32(&s.sfull), 2);
-    mbar_init(smem_u32(&s.sempty), 8);   // the 8 softmax warps
+    mbar_init(smem_u32(&s.sfull), 1);
+    mbar_init(smem_u32(&s.sempty), 16);  // 8 softmax warps x 2 S-CTAs
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
+      mbar_init(smem_u32(&s.pready[i]), 1);
       mbar_init(smem_u32(&s.pempty[i]), 1);
     }
-    mbar_init(smem_u32(&s.drain), 2);
-    mbar_init(smem_u32(&s.corr_done), 4);
-    mbar_init(smem_u32(&s.tail_ready), 1);
+    mbar_init(smem_u32(&s.drain), 2);      // pair commit + rank 2's arrive
+    mbar_init(smem_u32(&s.corr_done), 8);  // 4 correction warps x 2 O-CTAs
+    mbar_init(smem_u32(&s.tail_full), 1);
+    mbar_init(smem_u32(&s.tail_ready), 2);
     mbar_init(smem_u32(&s.fin_full), 1);
-    mbar_init(smem_u32(&s.qready), 8);
-    if (rank == 1 && w.npages > 0) {
+    mbar_init(smem_u32(&s.qready), 16);
+    if (rank >= 2 && w.npages > 0) {
       mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
+      // rank 2 also receives rank 1's 16 flag bytes per message
       for (int k = 0; k < kNP && k < w.npages; ++k)
-        mbar_arrive_expect_tx(smem_u32(&s.pfull[k]), kPMsgBytes);
+        mbar_arrive_expect_tx(smem_u32(&s.pfull[k]),
+                              kPMsgBytes + (rank == 2 ? 16 : 0));
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
@@ -762,33 +876,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       p.status)
     atomicOr(p.status, MLA_STATUS_BAD_LENGTH);
   if (warp == 1) {
-    tmem_alloc(smem_u32(&s.tmem_base), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&s.tmem_base), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  cluster_sync();  // the peer's barriers exist before any remote operation
+  cluster_sync();  // every CTA's barriers exist before any remote operation
 
   // Teardown, repeated at the end of every role: roles never rejoin, so no
   // warp ever asks setmaxnreg for registers back (a warpgroup that did could
   // take them before the softmax warpgroups got theirs and stall both).
+  // The pair's TMEM is released only after all four CTAs are done with it.
   auto teardown = [&]() {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    cluster_sync();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
     cluster_sync();
   };
 
-  if (w.npages > 0 && rank == 0) {
+  if (w.npages > 0 && rank < 2) {
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-      if (warp == 0)
+      if (warp == 0) {
         producer_s(s, &kv_map, p, w, rank, lane);
-      else if (warp == 1 || warp == 2) {
-        if (lane == 0) mma_s(s, p, w, tmem, rank, warp - 1);
+      } else if (warp == 1 && rank == 0) {
+        if (lane == 0) mma_s(s, p, w, tmem, rank);
         __syncwarp();
       }
       teardown();
@@ -800,22 +916,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
   if (w.npages > 0) {
-    if (warp == 0)
+    if (warp == 0) {
       producer_o(s, &kv_map, p, w, rank, lane);
-    else if (warp == 1) {
-      if (lane == 0) mma_o(s, p, w, tmem, rank);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        if (rank == 2)
+          mma_o(s, p, w, tmem, rank);
+        else
+          relay_o(s, p, w, rank);
+      }
       __syncwarp();
-    } else if (warp >= 4 && warp < 8)
+    } else if (warp >= 4 && warp < 8) {
       correct_and_store(s, p, w, tmem, rank, warp, lane);
+    }
   } else if (warp >= 4 && warp < 8) {
-    // No tokens for this split: O = 0, LSE = -inf.
+    // No tokens for this split: O = 0 (O-CTAs), LSE = -inf (S-CTAs).
     const int r = (warp & 3) * 32 + lane;
     if (r < w.nrows) {
       const int64_t rows = (int64_t)p.B * p.q_len * p.H;
       const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
       const int64_t orow =
           part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r;
-      if (rank == 0) {
+      if (rank < 2) {
         p.LSE_part[orow] = -INFINITY;
       } else {
         float4* d4 = reinterpret_cast<float4*>(p.O_part + orow * MLA_VALUE_DIM);
@@ -845,13 +967,14 @@ int launch_tc(const DecodeArgs& a) {
   p.H = a.H;
   p.V = a.B * a.num_shards;
   p.num_splits = a.num_splits;
-  p.G = (a.q_len * a.H + kRows - 1) / kRows;
+  p.U = (a.q_len * a.H + MLA_ROWS_PER_UNIT - 1) / MLA_ROWS_PER_UNIT;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
   p.O_part = a.O_part;
   p.LSE_part = a.LSE_part;
   p.status = a.status;
-  const int64_t pairs = (int64_t)p.V * p.num_splits * p.G;
-  if (pairs * 2 > 0x7fffffff) return fail(MLA_ERR_INVALID_ARG, "grid too large");
+  const int64_t units = (int64_t)p.V * p.num_splits * p.U;
+  if (units * kCtas > 0x7fffffff)
+    return fail(MLA_ERR_INVALID_ARG, "grid too large");
   CUtensorMap map;
   int rc = make_kv_tensor_map(&map, a.kv, a.kv_dtype, a.num_slots);
   if (rc != MLA_OK) return rc;
@@ -859,7 +982,7 @@ int launch_tc(const DecodeArgs& a) {
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc)");
-  mla_partial_tc_kernel<<<(unsigned)(pairs * 2), kThreads, kSmemBytes,
+  mla_partial_tc_kernel<<<(unsigned)(units * kCtas), kThreads, kSmemBytes,
                           a.stream>>>(map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_kernel");
@@ -868,7 +991,7 @@ int launch_tc(const DecodeArgs& a) {
 
 }  // namespace mla
 
-extern "C" int mla_pair_slots(void) {
+extern "C" int mla_cluster_slots(void) {
   cudaError_t e = cudaFuncSetAttribute(
       mla::mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       mla::kSmemBytes);
@@ -876,10 +999,10 @@ extern "C" int mla_pair_slots(void) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = mla::kCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.gridDim = dim3(mla::kCtas * 1024, 1, 1);
   cfg.blockDim = dim3(mla::kThreads, 1, 1);
   cfg.dynamicSmemBytes = mla::kSmemBytes;
   cfg.attrs = attr;

@@ -11,13 +11,15 @@ sources:
 
 2. A brute-force statement of this library's wave-rounding objective, the
    one the C planner must reproduce exactly:
-     units       one CTA pair per (virtual request v, split s, row group g),
-                 launched in that order (g fastest), G = ceil(H*q_len / 128)
+     units       one work unit per (virtual request v, split s, row unit u),
+                 launched in that order (u fastest), U = ceil(H*q_len / R),
+                 R = rows_per_unit (256: the library's kernel serves 256
+                 query rows with one 4-CTA cluster)
      unit cost   pages(v, s) + c0 page-tiles, where request v's P_v =
                  ceil(L_v / 64) pages are dealt to splits as
                  floor((s+1) P_v / S) - floor(s P_v / S)
      makespan    list scheduling of the units, in launch order, onto `slots`
-                 pair slots (each unit starts on the slot that frees first)
+                 unit slots (each unit starts on the slot that frees first)
      objective   J(S) = makespan(S) + lam * S * rows / 1024, rows = V*q_len*H
                  (the partial outputs each extra split writes and re-reads)
      choice      the S in [1, S_max] with the smallest J; ties go to fewer
@@ -30,7 +32,7 @@ import heapq
 from typing import List, Sequence, Tuple
 
 PAGES_SMS = 148          # B200 SM count used by the pages' heuristic
-ROWS_PER_GROUP = 128     # query rows per CTA pair (one tensor-core M tile)
+ROWS_PER_UNIT = 256      # query rows per work unit of the library's kernel
 
 
 def pages_heuristic_split(B: int, q_len: int, sms: int = PAGES_SMS) -> int:
@@ -66,8 +68,9 @@ def makespan(costs: Sequence[float], slots: int) -> float:
 
 
 def unit_costs(seq_lens: Sequence[int], H: int, q_len: int, S: int,
-               c0: float, page: int = 64) -> List[float]:
-    G = -(-H * q_len // ROWS_PER_GROUP)
+               c0: float, page: int = 64,
+               rows_per_unit: int = ROWS_PER_UNIT) -> List[float]:
+    G = -(-H * q_len // rows_per_unit)
     out = []
     for L in seq_lens:
         P = -(-L // page)

@@ -51,13 +51,13 @@ def test_pages_rule_matches_reference(lib):
 
 def test_planner_matches_brute_force(lib):
     rng = random.Random(7)
-    cases = [([100_000] * B, 96, 5, 76) for B in (1, 2, 4, 8, 12, 16, 20, 24)]
-    cases += [([12_500] * 1024, 96, 5, 76), ([256], 16, 1, 76)]
+    cases = [([100_000] * B, 96, 5, 38) for B in (1, 2, 4, 8, 12, 16, 20, 24)]
+    cases += [([12_500] * 1024, 96, 5, 38), ([256], 16, 1, 38)]
     for _ in range(40):
         V = rng.randint(1, 30)
         lens = [int(np.exp(rng.uniform(np.log(5), np.log(200_000)))) for _ in range(V)]
         cases.append((lens, rng.choice([16, 96, 128]), rng.randint(1, 6),
-                      rng.choice([1, 7, 74, 76])))
+                      rng.choice([1, 7, 37, 38, 76])))
     for lens, H, q, slots in cases:
         c0, lam = rng.choice([(4.0, 1.0), (0.0, 0.0), (2.5, 3.0)])
         S, eff, ms = mla.plan_ex(lens, q, H, slots, 64, c0, lam)
@@ -67,7 +67,8 @@ def test_planner_matches_brute_force(lib):
 
 
 def test_planner_leaves_no_partial_wave_tail(lib):
-    # 152 SMs -> 76 pair slots; 96 heads x q_len 5 -> 4 row groups per request
+    # 152 SMs -> 38 cluster slots; 96 heads x q_len 5 -> 2 row units of 256
+    # per request
     for B in (1, 2, 4, 8, 12, 16, 20, 24):
         for L in (100_000, 400_000):
             S, eff = mla.plan(B, 5, 96, [L] * B, num_sms=152)

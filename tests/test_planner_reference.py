@@ -47,11 +47,11 @@ def test_wave_rounded_estimates_scale_by_cta_count(est):
 
 
 def test_brute_force_plan_fills_whole_waves_for_uniform_batches():
-    # 76 pair slots (152 SMs / 2), 96 heads x q_len 5 = 4 row groups:
-    # 76 = 4 x 19, so 19 splits give exactly B waves for any B.
+    # 38 cluster slots (152 SMs / 4), 96 heads x q_len 5 = 480 rows = 2 row
+    # units of 256: 38 = 2 x 19, so 19 splits give exactly B waves for any B.
     for B in (1, 2, 4, 8, 12, 16, 20, 24):
         for L in (100_000, 400_000):
-            S, eff, _ = ref.plan([L] * B, 96, 5, slots=76)
+            S, eff, _ = ref.plan([L] * B, 96, 5, slots=38)
             assert eff >= 0.9, (B, L, S, eff)
 
 
@@ -60,4 +60,5 @@ def test_makespan_is_list_scheduling():
     assert ref.makespan([5, 1, 1, 1, 1, 1], 2) == 5
     assert ref.makespan([], 4) == 0
     costs = ref.unit_costs([128], 96, 5, 2, c0=0)
-    assert costs == [1] * 8  # 2 pages dealt 1 + 1, four row groups each
+    assert costs == [1] * 4  # 2 pages dealt 1 + 1, two row units each
+    assert ref.unit_costs([128], 96, 5, 2, c0=0, rows_per_unit=128) == [1] * 8
