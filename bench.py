@@ -56,6 +56,13 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="wave-quantisation sweep: B in 1..24 x context "
+                         "{100k, 400k}, the pages' split rule vs the planner "
+                         "(one JSON line per point)")
+    ap.add_argument("--sweep-scan", default="",
+                    help="extra comma-separated split counts to time at "
+                         "every sweep point")
     return ap.parse_args()
 
 
@@ -244,10 +251,88 @@ def run_reference(args):
     return 0
 
 
+def time_pair(mla, batch, wl, S, iters, warmup=3):
+    """Median device time (ms) of one partial-decode + combine pair at S
+    splits, CUDA events on the launching stream."""
+    import torch
+    dev = batch.q_nope.device
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
+                         dtype=torch.float32, device=dev)
+    LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
+                           dtype=torch.float32, device=dev)
+    out = torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.B, wl.q_len, wl.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+                           batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
+                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status)
+        mla.lse_combine(O_part, LSE_part, out, lse)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    """Wave-quantisation sweep: for every (B, context) point, the pair timed
+    with the pages' split rule and with the planner's split (and any extra
+    split counts asked for), one JSON line per point.  Inputs larger than L2
+    (>= 115 MB of KV at B = 1, 100k) so no flush is needed."""
+    import torch
+
+    import mla_latent_decode_gb300 as mla
+    from mla_latent_decode_gb300 import synth
+
+    mla.library()
+    extra = [int(x) for x in args.sweep_scan.split(",") if x.strip()]
+    slots = mla.cluster_slots()
+    for L in (100_000, 400_000):
+        for B in (1, 2, 4, 8, 12, 16, 20, 24):
+            wl = synth.config(f"sweep_B{B}_L{L}")
+            batch = synth.make_batch(wl, seed=0, device="cuda")
+            lens = mla.batch_lengths(batch)
+            S_plan, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards)
+            S_rule = mla.plan_heuristic(wl.B, wl.q_len)
+            fl = wl.flops()
+            iters = max(5, min(args.steps, int(2000 / max(1, B * L / 100_000))))
+            res = {}
+            for S in sorted({S_plan, S_rule, *extra}):
+                ms = time_pair(mla, batch, wl, S, iters)
+                res[S] = {"us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12}
+            print(json.dumps({
+                "impl": "sweep", "B": B, "context": L, "q_len": wl.q_len,
+                "H": wl.H, "cluster_slots": slots,
+                "pages_rule": {"splits": S_rule, **res[S_rule]},
+                "planner": {"splits": S_plan, "wave_eff": eff, **res[S_plan]},
+                "scan": {str(k): v for k, v in sorted(res.items())},
+                "unit": "us per layer (partial + combine), attention TFLOP/s",
+            }), flush=True)
+            del batch
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     rank, world, local = dist_env()
     import torch
 

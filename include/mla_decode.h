@@ -127,7 +127,9 @@ int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
 
 /*
  * mla_plan_ex with the library's defaults: slots = mla_cluster_slots() when
- * num_sms == 0, else num_sms / 4; s_max = 64; c0 = 4; lam = 1.
+ * num_sms == 0, else num_sms / 4; s_max = 64; c0 = 32; lam = 1 (fitted to
+ * the tensor-core kernel's measured times on GB300, B = 1..24 requests x
+ * 100k / 400k tokens: a work unit costs about 32 pages beyond its own).
  *   B, num_shards  requests and context shards (V = B * num_shards);
  *   seq_lens_host  host int32 [num_shards * B] (shard-local lengths).
  */

@@ -69,6 +69,16 @@ int check_decode_args(const DecodeArgs& a) {
   return MLA_OK;
 }
 
+// Default cost constants of mla_plan, in units of one page of one work unit
+// (about 0.9 us on a GB300): a work unit's fixed cost (launch, Q load,
+// pipeline fill, O_part write, wave hand-over) and the price of one more split
+// per 1024 query rows (partial outputs written and re-read by the combine).
+// Fitted to the decode kernel's measured times over B = 1..24 requests x
+// {100k, 400k} tokens x {1, 2, 3, 4, 6, 9, 18} splits, where they choose the
+// fastest measured split count at every point.
+constexpr double kPlanUnitCost = 32.0;
+constexpr double kPlanSplitCost = 1.0;
+
 // List-scheduling makespan of units in launch order on `slots` slots.
 static double makespan(const std::vector<double>& costs, int slots) {
   if (costs.empty()) return 0.0;
@@ -163,8 +173,9 @@ int mla_plan(int B, int q_len, int H, int num_shards,
     if (slots < 0) return slots;
     if (slots == 0) return fail(MLA_ERR_CUDA, "no 4-CTA cluster fits on this device");
   }
-  return mla_plan_ex(B * num_shards, q_len, H, seq_lens_host, slots, 64, 4.0,
-                     1.0, num_splits_out, wave_eff_out, nullptr);
+  return mla_plan_ex(B * num_shards, q_len, H, seq_lens_host, slots, 64,
+                     kPlanUnitCost, kPlanSplitCost, num_splits_out,
+                     wave_eff_out, nullptr);
 }
 
 int mla_check_page_table(const int32_t* r2t, int64_t stride,

@@ -67,12 +67,15 @@ def test_planner_matches_brute_force(lib):
 
 
 def test_planner_leaves_no_partial_wave_tail(lib):
-    # 152 SMs -> 38 cluster slots; 96 heads x q_len 5 -> 2 row units of 256
-    # per request
+    """The pages' rule leaves a partial second wave (B=16: 160 CTAs on 148
+    SMs).  The planner's grid either fits in one wave or fills its waves to
+    at least 90%.  152 SMs -> 38 cluster slots; 96 heads x q_len 5 -> 2 row
+    units of 256 per request."""
     for B in (1, 2, 4, 8, 12, 16, 20, 24):
         for L in (100_000, 400_000):
             S, eff = mla.plan(B, 5, 96, [L] * B, num_sms=152)
-            assert eff >= 0.9, (B, L, S, eff)
+            units = B * S * 2
+            assert units <= 38 or eff >= 0.9, (B, L, S, eff)
 
 
 def test_page_table_check(lib):
