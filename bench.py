@@ -306,7 +306,8 @@ def run_sweep(args):
             wl = synth.config(f"sweep_B{B}_L{L}")
             batch = synth.make_batch(wl, seed=0, device="cuda")
             lens = mla.batch_lengths(batch)
-            S_plan, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards)
+            S_plan, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
+                                   kv_dtype=wl.kv_dtype)
             S_rule = mla.plan_heuristic(wl.B, wl.q_len)
             fl = wl.flops()
             iters = max(5, min(args.steps, int(2000 / max(1, B * L / 100_000))))
@@ -355,7 +356,8 @@ def main():
     elif wl.num_splits:
         S, eff = wl.num_splits, None
     else:
-        S, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards)
+        S, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
+                          kv_dtype=wl.kv_dtype)
     S_pages = mla.plan_heuristic(wl.B, wl.q_len)
 
     dev = torch.device("cuda", local)

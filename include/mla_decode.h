@@ -80,7 +80,8 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 #define MLA_ROPE_DIM 64   /* qk_rope_head_dim */
 #define MLA_VALUE_DIM 512
 #define MLA_PAGE_SIZE 64  /* the only page size the kernels are built for */
-#define MLA_ROWS_PER_UNIT 256 /* query rows one work unit (a 4-CTA cluster) owns */
+#define MLA_ROWS_PER_UNIT 256 /* query rows one BF16 work unit (a 4-CTA cluster) owns;
+                                 an FP8 unit (a 2-CTA cluster) owns half */
 
 /* Last error message of this thread ("" if none).  Owned by the library. */
 const char* mla_last_error_string(void);
@@ -105,35 +106,42 @@ int mla_plan_heuristic(int B, int q_len);
 
 /*
  * Wave-rounding split planner (replaces the rule above; [K3-MLA] shows that
- * rule leaving a partial second wave).  Work units are 4-CTA clusters, one per
- * (virtual request v, split s, row unit u) with U = ceil(H*q_len / 256) row
- * units, launched in that order (u fastest).  For every S in [1, s_max] the unit costs
+ * rule leaving a partial second wave).  Work units are decode clusters, one
+ * per (virtual request v, split s, row unit u) with U = ceil(H*q_len /
+ * rows_per_unit) row units, launched in that order (u fastest): the BF16
+ * kernel serves 256 rows with a 4-CTA cluster, the FP8 kernel 128 rows with
+ * a 2-CTA cluster.  For every S in [1, s_max] the unit costs
  * pages(v, s) + c0 page tiles, where request v's P_v = ceil(L_v / 64) pages
  * are dealt as floor((s+1) P_v / S) - floor(s P_v / S); the units are list-
  * scheduled onto `slots` cluster slots in launch order; the objective is
  *   J(S) = makespan(S) + lam * S * rows / 1024,   rows = V * q_len * H,
  * (the second term prices the partial outputs each extra split writes and
  * the combine re-reads).  The smallest J wins, ties go to fewer splits.
+ *   rows_per_unit  query rows per work unit (> 0)
  *   seq_lens_host  host int32 [V] (V = num_shards * B virtual requests)
  *   slots          concurrent cluster slots (> 0)
  *   s_max          largest split count considered (1..1024)
  *   num_splits_out chosen S;  wave_eff_out: sum(unit cost)/(slots*makespan);
  *   makespan_out   makespan in page tiles (may be NULL)
  */
-int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
-                int slots, int s_max, double c0, double lam,
-                int* num_splits_out, float* wave_eff_out,
+int mla_plan_ex(int V, int q_len, int H, int rows_per_unit,
+                const int32_t* seq_lens_host, int slots, int s_max, double c0,
+                double lam, int* num_splits_out, float* wave_eff_out,
                 double* makespan_out);
 
 /*
- * mla_plan_ex with the library's defaults: slots = mla_cluster_slots() when
- * num_sms == 0, else num_sms / 4; s_max = 64; c0 = 32; lam = 1 (fitted to
- * the tensor-core kernel's measured times on GB300, B = 1..24 requests x
- * 100k / 400k tokens: a work unit costs about 32 pages beyond its own).
+ * mla_plan_ex with the library's defaults for the kernel that serves
+ * kv_dtype: BF16 -> rows_per_unit = 256 and slots = mla_cluster_slots() (or
+ * num_sms / 4 when num_sms > 0); FP8 E4M3 -> rows_per_unit = 128 and the
+ * resident 2-CTA clusters of the FP8 kernel (or num_sms / 2); s_max = 64;
+ * c0 = 32; lam = 1 (fitted to the BF16 kernel's measured times on GB300,
+ * B = 1..24 requests x 100k / 400k tokens: a work unit costs about 32 pages
+ * beyond its own).
  *   B, num_shards  requests and context shards (V = B * num_shards);
+ *   kv_dtype       MLA_KV_BF16 or MLA_KV_FP8_E4M3 (else MLA_ERR_INVALID_ARG)
  *   seq_lens_host  host int32 [num_shards * B] (shard-local lengths).
  */
-int mla_plan(int B, int q_len, int H, int num_shards,
+int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
              const int32_t* seq_lens_host, int num_sms, int* num_splits_out,
              float* wave_eff_out);
 
@@ -170,7 +178,7 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   q_rope           bf16 [B, q_len, H, 64], contiguous, 16-B aligned
  *   kv_pages         [num_slots, 576]: bf16 (1152-B rows) or E4M3 bytes
  *                    (576-B rows); 16-B aligned; num_slots >= page_size
- *   kv_scale         fp32 [num_slots] (FP8), NULL for BF16
+ *   kv_scale         fp32 [num_slots] (FP8), 16-B aligned; NULL for BF16
  *   req_to_token     int32 [num_shards*B, r2t_stride]; only the entry of the
  *                    first token of each page is read (see
  *                    mla_check_page_table for the contract)

@@ -22,6 +22,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
 ROW_DIM, NOPE_DIM, ROPE_DIM, VALUE_DIM, PAGE_SIZE = 576, 512, 64, 512, 64
 KV_BF16, KV_FP8_E4M3 = 0, 1
+_KV_DTYPE = {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3}
+ROWS_PER_UNIT = 256  # query rows per work unit of the BF16 tensor-core kernel
 STATUS_WAIT_TIMEOUT, STATUS_BAD_LENGTH, STATUS_BAD_SLOT = 1, 2, 4
 
 _lib = None
@@ -54,8 +56,8 @@ def library() -> ctypes.CDLL:
             "mla_num_sms": (i32, [i32]),
             "mla_cluster_slots": (i32, []),
             "mla_plan_heuristic": (i32, [i32, i32]),
-            "mla_plan_ex": (i32, [i32, i32, i32, p, i32, i32, f64, f64, p, p, p]),
-            "mla_plan": (i32, [i32, i32, i32, i32, p, i32, p, p]),
+            "mla_plan_ex": (i32, [i32, i32, i32, i32, p, i32, i32, f64, f64, p, p, p]),
+            "mla_plan": (i32, [i32, i32, i32, i32, i32, p, i32, p, p]),
             "mla_check_page_table": (i32, [p, i64, p, p, i32, i32, i32, i64]),
             "mla_decode_partial": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
                                          i32, i32, i32, i32, f32, i32, p, p, p, p]),
@@ -110,24 +112,27 @@ def plan_heuristic(B: int, q_len: int) -> int:
 
 
 def plan_ex(seq_lens: Sequence[int], q_len: int, H: int, slots: int,
-            s_max: int = 64, c0: float = 4.0, lam: float = 1.0):
+            s_max: int = 64, c0: float = 32.0, lam: float = 1.0,
+            rows_per_unit: int = ROWS_PER_UNIT):
     """Wave-rounding planner: returns (num_splits, wave_eff, makespan)."""
     arr = _host_i32(seq_lens)
     S, eff, ms = ctypes.c_int(), ctypes.c_float(), ctypes.c_double()
-    _check(library().mla_plan_ex(len(arr), q_len, H, arr, slots, s_max,
-                                 float(c0), float(lam), ctypes.byref(S),
-                                 ctypes.byref(eff), ctypes.byref(ms)))
+    _check(library().mla_plan_ex(len(arr), q_len, H, rows_per_unit, arr,
+                                 slots, s_max, float(c0), float(lam),
+                                 ctypes.byref(S), ctypes.byref(eff),
+                                 ctypes.byref(ms)))
     return S.value, eff.value, ms.value
 
 
 def plan(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
-         num_sms: int = 0):
-    """Planner with the library defaults; num_sms=0 asks the device."""
+         num_sms: int = 0, kv_dtype: str = "bf16"):
+    """Planner with the library defaults for the kernel that serves
+    `kv_dtype`; num_sms=0 asks the device."""
     arr = _host_i32(seq_lens)
     assert len(arr) == B * num_shards
     S, eff = ctypes.c_int(), ctypes.c_float()
-    _check(library().mla_plan(B, q_len, H, num_shards, arr, num_sms,
-                              ctypes.byref(S), ctypes.byref(eff)))
+    _check(library().mla_plan(B, q_len, H, num_shards, _KV_DTYPE[kv_dtype],
+                              arr, num_sms, ctypes.byref(S), ctypes.byref(eff)))
     return S.value, eff.value
 
 
@@ -218,7 +223,8 @@ def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
     wl = batch.wl
     if num_splits is None:
         num_splits = wl.num_splits or plan(
-            wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards)[0]
+            wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards,
+            kv_dtype=wl.kv_dtype)[0]
     O_part, LSE_part = decode_partial(
         batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
         batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,

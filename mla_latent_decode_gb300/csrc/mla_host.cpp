@@ -62,10 +62,10 @@ int check_decode_args(const DecodeArgs& a) {
       !aligned(a.O_part, 16) || !aligned(a.LSE_part, 4) ||
       !aligned(a.req_to_token, 4) || !aligned(a.seq_lens, 4) ||
       (a.kv_limit && !aligned(a.kv_limit, 4)) ||
-      (a.kv_scale && !aligned(a.kv_scale, 4)) ||
+      (a.kv_scale && !aligned(a.kv_scale, 16)) ||
       (a.status && !aligned(a.status, 4)))
     return fail(MLA_ERR_MISALIGNED,
-                "q/kv/O_part need 16-B alignment, the int/float arrays 4-B");
+                "q/kv/kv_scale/O_part need 16-B alignment, the other arrays 4-B");
   return MLA_OK;
 }
 
@@ -118,15 +118,17 @@ int mla_plan_heuristic(int B, int q_len) {
   return std::max(1, std::min(148 / B / (q_len * 2), 32));
 }
 
-int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
-                int slots, int s_max, double c0, double lam,
-                int* num_splits_out, float* wave_eff_out,
+int mla_plan_ex(int V, int q_len, int H, int rows_per_unit,
+                const int32_t* seq_lens_host, int slots, int s_max, double c0,
+                double lam, int* num_splits_out, float* wave_eff_out,
                 double* makespan_out) {
   if (V < 1 || q_len < 1 || H < 1 || !seq_lens_host || !num_splits_out)
     return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
-  if (slots < 1 || s_max < 1 || s_max > 1024 || !(c0 >= 0) || !(lam >= 0))
-    return fail(MLA_ERR_INVALID_ARG, "slots/s_max/c0/lam out of range");
-  const int G = (H * q_len + MLA_ROWS_PER_UNIT - 1) / MLA_ROWS_PER_UNIT;
+  if (rows_per_unit < 1 || slots < 1 || s_max < 1 || s_max > 1024 ||
+      !(c0 >= 0) || !(lam >= 0))
+    return fail(MLA_ERR_INVALID_ARG,
+                "rows_per_unit/slots/s_max/c0/lam out of range");
+  const int G = (H * q_len + rows_per_unit - 1) / rows_per_unit;
   const double rows = (double)V * q_len * H;
   double bestJ = 0, bestEff = 0, bestMs = 0;
   int bestS = 0;
@@ -160,22 +162,28 @@ int mla_plan_ex(int V, int q_len, int H, const int32_t* seq_lens_host,
   return MLA_OK;
 }
 
-int mla_plan(int B, int q_len, int H, int num_shards,
+int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
              const int32_t* seq_lens_host, int num_sms, int* num_splits_out,
              float* wave_eff_out) {
   if (B < 1 || num_shards < 1)
     return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  // BF16: 256 query rows per 4-CTA cluster; E4M3: 128 rows per 2-CTA cluster.
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const int ctas = fp8 ? 2 : 4;
   int slots;
   if (num_sms > 0) {
-    slots = std::max(1, num_sms / 4);
+    slots = std::max(1, num_sms / ctas);
   } else {
-    slots = mla_cluster_slots();
+    slots = fp8 ? pair_slots_fp8() : mla_cluster_slots();
     if (slots < 0) return slots;
-    if (slots == 0) return fail(MLA_ERR_CUDA, "no 4-CTA cluster fits on this device");
+    if (slots == 0) return fail(MLA_ERR_CUDA, "no decode cluster fits on this device");
   }
-  return mla_plan_ex(B * num_shards, q_len, H, seq_lens_host, slots, 64,
-                     kPlanUnitCost, kPlanSplitCost, num_splits_out,
-                     wave_eff_out, nullptr);
+  return mla_plan_ex(B * num_shards, q_len, H,
+                     fp8 ? MLA_ROWS_PER_UNIT / 2 : MLA_ROWS_PER_UNIT,
+                     seq_lens_host, slots, 64, kPlanUnitCost, kPlanSplitCost,
+                     num_splits_out, wave_eff_out, nullptr);
 }
 
 int mla_check_page_table(const int32_t* r2t, int64_t stride,

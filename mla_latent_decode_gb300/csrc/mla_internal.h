@@ -54,6 +54,8 @@ int check_decode_args(const DecodeArgs& a);
 
 // Launchers (defined next to their kernels).
 int launch_simt(const DecodeArgs& a);
-int launch_tc(const DecodeArgs& a);
+int launch_tc(const DecodeArgs& a);       // BF16 KV: 4-CTA clusters
+int launch_tc_fp8(const DecodeArgs& a);   // E4M3 KV: 2-CTA clusters
+int pair_slots_fp8();                     // resident 2-CTA clusters (FP8)
 
 }  // namespace mla

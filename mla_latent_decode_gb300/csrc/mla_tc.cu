@@ -952,8 +952,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_tc(const DecodeArgs& a) {
-  if (a.kv_dtype != MLA_KV_BF16)
-    return fail(MLA_ERR_UNSUPPORTED, "tensor-core path: FP8 KV not built yet");
+  if (a.kv_dtype == MLA_KV_FP8_E4M3) return launch_tc_fp8(a);
   TcParams p;
   p.q_nope = static_cast<const uint4*>(a.q_nope);
   p.q_rope = static_cast<const uint4*>(a.q_rope);

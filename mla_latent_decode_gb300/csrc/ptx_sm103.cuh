@@ -77,18 +77,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Slow path of mbar_wait: spin with a time limit.  (Inlined: kernels that
-// rebalance registers with setmaxnreg cannot make real calls there.)
+// try_wait that lets the hardware suspend the thread (up to `hint_ns`) until
+// the phase completes, instead of returning at once: a waiting warp then
+// takes no issue slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar,
+                                                      uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
+      "%3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSuspendNs = 20000;  // 20 us per suspended try
+
+// Slow path of mbar_wait: suspended tries with a time limit.  (Inlined:
+// kernels that rebalance registers with setmaxnreg cannot make real calls
+// there.)
 static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar,
                                                       uint32_t parity,
                                                       volatile int* abort) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it != 0; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitNs) return false;
-    }
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+    if (*abort) return false;
+    if ((it & 7) == 0 && globaltimer() - t0 > kWaitNs) return false;
   }
   return false;
 }

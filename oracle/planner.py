@@ -81,12 +81,14 @@ def unit_costs(seq_lens: Sequence[int], H: int, q_len: int, S: int,
 
 
 def plan(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
-         s_max: int = 64, c0: float = 4.0, lam: float = 1.0):
+         s_max: int = 64, c0: float = 4.0, lam: float = 1.0,
+         rows_per_unit: int = ROWS_PER_UNIT):
     """Brute-force planner: returns (S, wave_efficiency, makespan)."""
     rows = len(seq_lens) * q_len * H
     best = None
     for S in range(1, s_max + 1):
-        costs = unit_costs(seq_lens, H, q_len, S, c0)
+        costs = unit_costs(seq_lens, H, q_len, S, c0,
+                           rows_per_unit=rows_per_unit)
         ms = makespan(costs, slots)
         J = ms + lam * S * rows / 1024.0
         if best is None or J < best[0] - 1e-9:

@@ -30,6 +30,61 @@ def oracle_rows(batch, hb, rows, shard=None, lo=None, hi=None):
                                   wl.sm_scale, rows, lo, hi)
 
 
+def compact_unsharded(batch, reqs):
+    """Host oracle inputs for requests `reqs` of a (possibly sharded) batch,
+    unsharded: each request's tokens in logical order (token p of request b
+    is local token p // S of shard p % S, the interleaving of the pages'
+    context-parallel layout), gathered from the very bytes the kernel reads
+    into a compact pool.  Returns (host dict for oracle.mla_decode_rows,
+    B' = len(reqs))."""
+    wl = batch.wl
+    S, B = wl.num_shards, wl.B
+    dev = batch.kv.device
+    rows, scales, lens = [], [], []
+    for b in reqs:
+        L = wl.seq_lens[b]
+        p = torch.arange(L, device=dev, dtype=torch.int64)
+        if S == 1:
+            slots = batch.req_to_token[b, p]
+        else:
+            slots = batch.req_to_token[(p % S) * B + b, p // S]
+        slots = slots.to(torch.int64)
+        rows.append(batch.kv.index_select(0, slots))
+        if batch.kv_is_fp8:
+            scales.append(batch.kv_scale.index_select(0, slots))
+        lens.append(L)
+    pool = torch.cat(rows)
+    stride = max(lens)
+    r2t = np.zeros((len(reqs), stride), np.int32)
+    off = 0
+    for i, L in enumerate(lens):
+        r2t[i, :L] = off + np.arange(L, dtype=np.int32)
+        off += L
+    idx = torch.tensor(reqs, device=batch.q_nope.device)
+
+    def bits16(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view("uint16")
+    host = dict(q_nope=bits16(batch.q_nope.index_select(0, idx)),
+                q_rope=bits16(batch.q_rope.index_select(0, idx)),
+                req_to_token=r2t, seq_lens=np.array(lens, np.int32),
+                kv_limit=None)
+    if batch.kv_is_fp8:
+        host["kv"] = pool.cpu().numpy()
+        host["kv_scale"] = torch.cat(scales).cpu().numpy()
+    else:
+        host["kv"] = bits16(pool)
+        host["kv_scale"] = None
+    return host, len(reqs)
+
+
+def oracle_rows_host(host, Bq, wl, kv_is_fp8, rows):
+    """Oracle O/LSE for flat rows of the [Bq, q, H] layout of a host dict."""
+    return oracle.mla_decode_rows(host["q_nope"], host["q_rope"], host["kv"],
+                                  kv_is_fp8, host["kv_scale"],
+                                  host["req_to_token"], host["seq_lens"], None,
+                                  Bq, wl.q_len, wl.H, wl.sm_scale, rows)
+
+
 def split_range(L, S, s, page=64):
     P = -(-L // page)
     return (s * P // S) * page, min(((s + 1) * P // S) * page, L)

@@ -60,8 +60,9 @@ def test_planner_matches_brute_force(lib):
                       rng.choice([1, 7, 37, 38, 76])))
     for lens, H, q, slots in cases:
         c0, lam = rng.choice([(4.0, 1.0), (0.0, 0.0), (2.5, 3.0)])
-        S, eff, ms = mla.plan_ex(lens, q, H, slots, 64, c0, lam)
-        S2, eff2, ms2 = ref.plan(lens, H, q, slots, 64, c0, lam)
+        rpu = rng.choice([128, 256])
+        S, eff, ms = mla.plan_ex(lens, q, H, slots, 64, c0, lam, rows_per_unit=rpu)
+        S2, eff2, ms2 = ref.plan(lens, H, q, slots, 64, c0, lam, rows_per_unit=rpu)
         assert (S, ms) == (S2, ms2), (lens[:4], H, q, slots)
         assert eff == pytest.approx(eff2, rel=1e-6)
 

@@ -12,7 +12,8 @@ import torch
 
 import mla_latent_decode_gb300 as mla
 from mla_latent_decode_gb300 import build, synth
-from parity import check_close, f64, oracle_rows, split_range
+from parity import (check_close, compact_unsharded, f64, oracle_rows,
+                    oracle_rows_host, split_range)
 
 pytestmark = pytest.mark.gpu
 
@@ -164,3 +165,104 @@ def test_tc_full_size_dp16_sampled_rows():
     m = check_close(got, f64(lse).reshape(-1)[rows], O_ref, l_ref, "bf16",
                     f"dp16 S={S}")
     print("dp16", S, m)
+
+
+def test_tc_full_size_dcp_sampled_rows_vs_unsharded_oracle():
+    """128 requests x q_len 5 x 96 heads x 100k tokens in 8 token-interleaved
+    shards (12.5k local tokens each, 14.7 GB of KV), planner splits, one
+    launch over all shards, then the LSE combine over 8 x S parts.  Sampled
+    rows of three requests are compared with the unsharded oracle on the
+    same bytes."""
+    wl = synth.config("dcp")
+    batch = synth.make_batch(wl, seed=0, device="cuda")
+    st = _status()
+    out, lse, S = mla.decode(batch, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    reqs = [0, 77, 127]
+    host, Bq = compact_unsharded(batch, reqs)
+    R = wl.q_len * wl.H
+    rng = np.random.default_rng(1)
+    local = np.unique(np.concatenate([rng.choice(Bq * R, 30, replace=False),
+                                      [0, R - 1, R, 2 * R + 479]]))
+    O_ref, l_ref = oracle_rows_host(host, Bq, wl, False, local)
+    flat_out = f64(out).reshape(wl.B * R, 512)
+    flat_lse = f64(lse).reshape(wl.B * R)
+    glob = np.array([reqs[r // R] * R + r % R for r in local])
+    m = check_close(flat_out[glob], flat_lse[glob], O_ref, l_ref, "bf16",
+                    f"dcp S={S}")
+    print("dcp", S, m)
+
+
+# ----------------------------------------------------------- FP8 E4M3 KV ----
+FP8_CASES = [
+    ("fp8_tiny", synth.Workload("t8", 1, 1, 16, [256], kv_dtype="fp8_e4m3"), 1),
+    ("fp8_small", synth.Workload("s8", 3, 5, 96, [1000, 257, 5], kv_dtype="fp8_e4m3"), 3),
+    ("fp8_heads16_q3", synth.Workload("h8", 2, 3, 16, [130, 3], kv_dtype="fp8_e4m3"), 7),
+    ("fp8_peaked", synth.Workload("p8", 2, 5, 96, [3000, 333], kv_dtype="fp8_e4m3",
+                                  q_scale=8.0), 4),
+    ("fp8_empty_splits", synth.Workload("e8", 2, 5, 32, [64, 200], kv_dtype="fp8_e4m3"), 9),
+]
+
+
+@pytest.mark.parametrize("name,wl,S", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+def test_tc_fp8_decode_matches_oracle(name, wl, S):
+    batch = synth.make_batch(wl, seed=13, device="cuda")
+    hb = synth.host_bits(batch)
+    st = _status()
+    out, lse, _ = mla.decode(batch, num_splits=S, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O_ref, l_ref = oracle_rows(batch, hb, None)
+    m = check_close(f64(out).reshape(-1, 512), f64(lse).reshape(-1), O_ref, l_ref,
+                    "fp8_e4m3", name)
+    print(name, m)
+
+
+def test_tc_fp8_shards_match_unsharded_oracle():
+    sh = synth.Workload("dcp8", 3, 5, 96, [517, 64, 9], num_shards=8,
+                        kv_dtype="fp8_e4m3")
+    batch = synth.make_batch(sh, seed=5, device="cuda")
+    st = _status()
+    out, lse, _ = mla.decode(batch, num_splits=2, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    host, Bq = compact_unsharded(batch, [0, 1, 2])
+    O_ref, l_ref = oracle_rows_host(host, Bq, sh, True, None)
+    check_close(f64(out).reshape(-1, 512), f64(lse).reshape(-1), O_ref, l_ref,
+                "fp8_e4m3", "fp8 sharded")
+
+
+def test_tc_fp8_agrees_with_cuda_core_path():
+    wl = synth.Workload("x8", 4, 5, 96, [2000, 1500, 64, 777], q_scale=3.0,
+                        kv_dtype="fp8_e4m3")
+    batch = synth.make_batch(wl, seed=6, device="cuda")
+    a, la, _ = mla.decode(batch, num_splits=3)
+    b, lb, _ = mla.decode(batch, num_splits=3, simt=True)
+    torch.cuda.synchronize()
+    check_close(f64(a).reshape(-1, 512), f64(la).reshape(-1), f64(b).reshape(-1, 512),
+                f64(lb).reshape(-1), "fp8_e4m3", "fp8 tc vs simt")
+
+
+def test_tc_fp8_full_size_ragged_sampled_rows():
+    """24 requests x q_len 5 x 96 heads, contexts log-uniform in [1k, 200k],
+    E4M3 KV with per-token scales, planner splits; rows sampled across
+    requests (short and long) compared with the oracle on the stored bytes."""
+    wl = synth.config("ragged_fp8")
+    batch = synth.make_batch(wl, seed=0, device="cuda")
+    st = _status()
+    out, lse, S = mla.decode(batch, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    order = np.argsort(wl.seq_lens)
+    reqs = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    host, Bq = compact_unsharded(batch, reqs)
+    R = wl.q_len * wl.H
+    rng = np.random.default_rng(2)
+    local = np.unique(np.concatenate([rng.choice(Bq * R, 30, replace=False),
+                                      [0, R - 1, Bq * R - 1]]))
+    O_ref, l_ref = oracle_rows_host(host, Bq, wl, True, local)
+    glob = np.array([reqs[r // R] * R + r % R for r in local])
+    m = check_close(f64(out).reshape(-1, 512)[glob], f64(lse).reshape(-1)[glob],
+                    O_ref, l_ref, "fp8_e4m3", f"ragged_fp8 S={S}")
+    print("ragged_fp8", S, [wl.seq_lens[r] for r in reqs], m)
