@@ -26,9 +26,9 @@
 //       factors to their O-CTA with a bulk shared-memory copy.
 //     ranks 2,3, the "O pair": rank 2+r holds O (128 x 512 fp32) of row group
 //       2u + r in all of its TMEM and loads half of V: dims [256n + 128r,
-//       +128) of each page for the two 256-wide halves n; each page feeds 8
-//       pair MMAs of M=256, N=256, K=16 (A = P, B = V MN-major) issued by
-//       rank 2.  Correction warps rescale O rows when an S-CTA raised a
+//       +128) of each page for the two 256-wide halves n, one 32-KB stage
+//       per page; each page feeds 8 pair MMAs of M=256, N=256, K=16 (A = P,
+//       B = V MN-major) issued by rank 2.  Correction warps rescale O rows when an S-CTA raised a
 //       running max, then write the normalised O_part rows.
 //   Per SM the TMA then lands 16 KB per 512 tensor cycles.  Every wait is
 //   bounded (ptx_sm103.cuh); a timeout sets MLA_STATUS_WAIT_TIMEOUT and the
@@ -45,8 +45,10 @@ using namespace ptx;
 
 constexpr int kThreads = 384;        // 12 warps = 3 warpgroups
 constexpr int kCtas = 4;             // S pair (ranks 0,1) + O pair (ranks 2,3)
-constexpr int kStages = 8;           // 16-KB ring stages (2 boxes each)
+constexpr int kStages = 8;           // S-CTA: 16-KB ring stages (2 boxes each)
 constexpr int kBoxesPerStage = 2;
+constexpr int kStagesO = 4;          // O-CTA: 32-KB stages (4 boxes, a page)
+constexpr int kBoxesO = 4;
 constexpr int kTilePages = 4;        // pages per S tile (N = 256), 2 per S-CTA
 constexpr int kNP = 4;               // P message slots (page index mod 4)
 constexpr int kRows = MLA_ROWS_PER_UNIT / 2;  // 128 query rows per CTA
@@ -292,12 +294,13 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
 }
 
 // ------------------------------------------------------- O-CTA producers ---
-// Rank 2+h loads dims [256n + 128h, +128) of every page (2 boxes) for the
-// two N halves n: one stage each, bytes of both CTAs completing on rank 2's
-// full barrier.  A request's last page may be partly filled: rows past its
-// length can hold anything (even NaN) and 0 * NaN would poison O = P V, so
-// that page lands on the CTA's own tail barrier instead, its rows past the
-// length are zeroed, and both CTAs then report to rank 2 (tail_ready).
+// Rank 2+h loads dims [256n + 128h, +128) of every page for n = 0, 1: one
+// stage of 4 boxes (box 2n + i = dims 256n + 128h + 64i), bytes of both CTAs
+// completing on rank 2's full barrier.  A request's last page may be partly
+// filled: rows past its length can hold anything (even NaN) and 0 * NaN
+// would poison O = P V, so that page lands on the CTA's own tail barrier
+// instead, its rows past the length are zeroed, and both CTAs then report to
+// rank 2 (tail_ready).
 __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
@@ -315,48 +318,39 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
     const int64_t t0 = (w.p0 + m) * kPage;
     const bool partial = t0 + kPage > w.L;
-    const uint32_t stage0 = stage;
-    for (int n = 0; n < 2 && ok; ++n) {
-      if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
-          if (partial) {
-            if (n == 0)
-              mbar_arrive_expect_tx(smem_u32(&s.tail_full),
-                                    2 * kBoxesPerStage * kBoxBytes);
-          } else if (rank == 2) {
-            mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
-                                  2 * kBoxesPerStage * kBoxBytes);
-          }
-        } else {
-          ok = false;
-        }
-      }
-      ok = __shfl_sync(kFull, ok, 0);
-      if (ok && lane < kBoxesPerStage) {
-        const uint32_t dst = smem_u32(s.ring[stage * kBoxesPerStage + lane]);
-        const int x = (256 * n + 128 * h + 64 * lane);
+    if (lane == 0) {
+      if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
         if (partial)
-          tma_load_2d(dst, map, smem_u32(&s.tail_full), x, y);
-        else
-          tma_load_2d_pair(dst, map, full0 + 8u * stage, x, y);
+          mbar_arrive_expect_tx(smem_u32(&s.tail_full), kBoxesO * kBoxBytes);
+        else if (rank == 2)
+          mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
+                                2 * kBoxesO * kBoxBytes);
+      } else {
+        ok = false;
       }
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    if (ok && lane < kBoxesO) {
+      const uint32_t dst = smem_u32(s.ring[stage * kBoxesO + lane]);
+      const int x = 256 * (lane >> 1) + 128 * h + 64 * (lane & 1);
+      if (partial)
+        tma_load_2d(dst, map, smem_u32(&s.tail_full), x, y);
+      else
+        tma_load_2d_pair(dst, map, full0 + 8u * stage, x, y);
+    }
+    const uint32_t st0 = stage;
+    if (++stage == kStagesO) {
+      stage = 0;
+      phase ^= 1u;
     }
     if (!ok || !partial) continue;
     // The partial page is the request's last: zero its rows past the length.
     const int keep = (int)(w.L - t0);
     if (!mbar_wait(smem_u32(&s.tail_full), 0, &s.abort_flag)) ok = false;
-    uint32_t st = stage0;
-    for (int n = 0; n < 2; ++n) {
-      for (int q = 0; q < kBoxesPerStage; ++q) {
-        uint4* box = reinterpret_cast<uint4*>(s.ring[st * kBoxesPerStage + q]);
-        for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
-          box[k] = make_uint4(0, 0, 0, 0);
-      }
-      if (++st == kStages) st = 0;
+    for (int q = 0; q < kBoxesO; ++q) {
+      uint4* box = reinterpret_cast<uint4*>(s.ring[st0 * kBoxesO + q]);
+      for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
+        box[k] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -703,33 +697,29 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       ++ev;
     }
     const bool tail = has_tail && m == w.npages - 1;
-    if (tail && !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
+    if (tail ? !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)
+             : !mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
       ok = false;
       break;
     }
+    tc_fence_after();
     const uint64_t a = sdesc_sw128(smem_u32(s.pslot[k]), 16, 1024);
     for (int n = 0; n < 2; ++n) {
-      if (!tail && !mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       // B = V: MN-major, next 64 dims one box (8 KB) on, next 8 tokens 1 KB
       // on; each 16-token K step advances 2048 B (128 descriptor units).
-      const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]),
-                                     kBoxBytes, 1024);
+      const uint64_t b = sdesc_sw128(
+          smem_u32(s.ring[stage * kBoxesO + 2 * n]), kBoxBytes, 1024);
       const uint32_t d = tmem + 256u * n;
       mma_ss_pair(d, a + 0, b + 0, kIdescO, m > 0 ? 1u : 0u);
       mma_ss_pair(d, a + 2, b + 128, kIdescO, 1u);
       mma_ss_pair(d, a + 4, b + 256, kIdescO, 1u);
       mma_ss_pair(d, a + 6, b + 384, kIdescO, 1u);
-      mma_commit_pair(smem_u32(&s.empty[stage]), kMaskO);
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
     }
-    if (!ok) break;
+    mma_commit_pair(smem_u32(&s.empty[stage]), kMaskO);
+    if (++stage == kStagesO) {
+      stage = 0;
+      phase ^= 1u;
+    }
     mma_commit_pair(smem_u32(&s.pempty[k]), kMaskS);  // both S-CTAs
   }
   if (!ok) signal_abort(s, p, rank);
