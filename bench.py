@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--config", default="dp16")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--splits", type=int, default=0, help="0: planner")
+    ap.add_argument("--parts-cut", type=int, default=0,
+                    help="two parts per request, the first of this many pages "
+                         "(reproduces a larger workload's per-request plan on "
+                         "fewer requests, e.g. for a traffic capture)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -251,7 +255,7 @@ def run_reference(args):
     return 0
 
 
-def time_pair(mla, batch, wl, S, iters, warmup=3):
+def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None):
     """Median device time (ms) of one partial-decode + combine pair at S
     splits, CUDA events on the launching stream."""
     import torch
@@ -268,7 +272,8 @@ def time_pair(mla, batch, wl, S, iters, warmup=3):
     def run():
         mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
                            batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
-                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status)
+                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status,
+                           split_pages=split_pages)
         mla.lse_combine(O_part, LSE_part, out, lse)
 
     for _ in range(warmup):
@@ -315,11 +320,19 @@ def run_sweep(args):
             for S in sorted({S_plan, S_rule, *extra}):
                 ms = time_pair(mla, batch, wl, S, iters)
                 res[S] = {"us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12}
+            S_parts, bnd, eff_parts = mla.plan_parts(
+                wl.B, wl.q_len, wl.H, lens, wl.num_shards, kv_dtype=wl.kv_dtype)
+            ms = time_pair(mla, batch, wl, S_parts, iters,
+                           split_pages=torch.from_numpy(bnd).to(batch.q_nope.device))
+            parts = {"splits": S_parts, "wave_eff": eff_parts,
+                     "first_part_pages": int(bnd[0][1]), "us": ms * 1e3,
+                     "tflops": fl / (ms * 1e-3) / 1e12}
             print(json.dumps({
                 "impl": "sweep", "B": B, "context": L, "q_len": wl.q_len,
                 "H": wl.H, "cluster_slots": slots,
                 "pages_rule": {"splits": S_rule, **res[S_rule]},
                 "planner": {"splits": S_plan, "wave_eff": eff, **res[S_plan]},
+                "parts_planner": parts,
                 "scan": {str(k): v for k, v in sorted(res.items())},
                 "unit": "us per layer (partial + combine), attention TFLOP/s",
             }), flush=True)
@@ -351,16 +364,30 @@ def main():
     batch = synth.make_batch(wl, seed=rank, device="cuda")
     lens = mla.batch_lengths(batch)
     slots = mla.cluster_slots()
-    if args.splits > 0:
+    dev = torch.device("cuda", local)
+    split_pages, plan_desc = None, "uniform deal"
+    if args.parts_cut > 0:
+        import numpy as np
+        P = [-(-L // 64) for L in lens]
+        bnd = np.array([[0, min(p, args.parts_cut), p] for p in P], dtype=np.int32)
+        S, eff = 2, None
+        split_pages = torch.from_numpy(bnd).to(dev)
+        plan_desc = f"two parts per request, first {args.parts_cut} pages (fixed)"
+    elif args.splits > 0:
         S, eff = args.splits, None
     elif wl.num_splits:
         S, eff = wl.num_splits, None
     else:
-        S, eff = mla.plan(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
-                          kv_dtype=wl.kv_dtype)
+        # the library's per-request split planner (part of the per-batch plan,
+        # computed before timing like the split count)
+        S, bnd, eff = mla.plan_parts(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
+                                     kv_dtype=wl.kv_dtype)
+        split_pages = torch.from_numpy(bnd).to(dev)
+        plan_desc = (f"per-request parts, first-part boundaries "
+                     f"{sorted({r[1] for r in bnd.tolist()})[:4]}"
+                     if S > 1 else "one part")
     S_pages = mla.plan_heuristic(wl.B, wl.q_len)
 
-    dev = torch.device("cuda", local)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
                          dtype=torch.float32, device=dev)
@@ -375,7 +402,8 @@ def main():
             ev[0].record(stream)
         mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
                            batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
-                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status)
+                           wl.sm_scale, wl.num_shards, O_part, LSE_part, status,
+                           split_pages=split_pages)
         if ev is not None:
             ev[1].record(stream)
         mla.lse_combine(O_part, LSE_part, out, lse)
@@ -460,7 +488,7 @@ def main():
             ds.copy_(hs, non_blocking=True)
             mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
                                batch.kv_limit, S, wl.sm_scale, wl.num_shards,
-                               O_part, LSE_part, status)
+                               O_part, LSE_part, status, split_pages=split_pages)
             mla.lse_combine(O_part, LSE_part, out, lse)
             ho.copy_(out, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
@@ -500,6 +528,7 @@ def main():
                 "workload": workload_desc(wl), "B": wl.B, "q_len": wl.q_len,
                 "H": wl.H, "context": wl.seq_lens[0] if len(set(wl.seq_lens)) == 1 else "ragged",
                 "num_shards": wl.num_shards, "num_splits": S,
+                "split_plan": plan_desc,
                 "planner_wave_eff": eff, "pages_rule_splits": S_pages,
                 "cluster_slots": slots,
                 "l2": (f"KV {kv_bytes / 1e6:.1f} MB < 2 x L2: 256-MB L2 flush between timed steps, value from per-step event spans"

@@ -108,7 +108,8 @@ int mla_plan_heuristic(int B, int q_len);
  * Wave-rounding split planner (replaces the rule above; [K3-MLA] shows that
  * rule leaving a partial second wave).  Work units are decode clusters, one
  * per (virtual request v, split s, row unit u) with U = ceil(H*q_len /
- * rows_per_unit) row units, launched in that order (u fastest): the BF16
+ * rows_per_unit) row units, launched split-major (s slowest, then v, u
+ * fastest): the BF16
  * kernel serves 256 rows with a 4-CTA cluster, the FP8 kernel 128 rows with
  * a 2-CTA cluster.  For every S in [1, s_max] the unit costs
  * pages(v, s) + c0 page tiles, where request v's P_v = ceil(L_v / 64) pages
@@ -146,6 +147,41 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
              float* wave_eff_out);
 
 /*
+ * Split planner with per-request boundaries (work balanced over the resident
+ * clusters, [K3-MLA]'s wave-aware rounding taken further).  Candidates, all
+ * scored like mla_plan_ex (list scheduling of the work units on `slots` in
+ * launch order, which is part-major: every request's part s before any part
+ * s + 1; a unit costs its pages + c0, an empty unit 1; J = makespan +
+ * lam * S * rows / 1024), the first of equal J kept:
+ *   1. the uniform deal for S = 1 .. s_max;
+ *   2. for S = 2 .. max_parts and 32 caps b = ceil(Pmax * k / 32): part 0 of
+ *      request v = min(P_v, b) pages, the other P_v - part0 pages dealt
+ *      over parts 1 .. S-1 (boundary m = part0 + floor((m-1) rest / (S-1))).
+ * Writes S = *num_parts_out and the boundaries as [V][S + 1] int32 at the
+ * start of split_pages_out (a HOST buffer of at least V * (s_max + 1)
+ * entries), for mla_decode_partial's split_pages.
+ *   rows_per_unit, seq_lens_host, slots, s_max, c0, lam: as mla_plan_ex
+ *   max_parts      largest part count of the capped family (1..s_max)
+ *   wave_eff_out   sum(unit cost) / (slots * makespan), may be NULL
+ *   makespan_out   makespan in pages, may be NULL
+ */
+int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
+                      const int32_t* seq_lens_host, int slots, int s_max,
+                      int max_parts, double c0, double lam,
+                      int32_t* split_pages_out, int* num_parts_out,
+                      float* wave_eff_out, double* makespan_out);
+
+/*
+ * mla_plan_parts_ex with mla_plan's defaults (rows per unit and slots of the
+ * kernel that serves kv_dtype, s_max = 64, c0 = 32, lam = 1).
+ * split_pages_out: HOST int32 buffer of at least num_shards * B * 65 entries.
+ */
+int mla_plan_parts(int B, int q_len, int H, int num_shards,
+                   mla_kv_dtype kv_dtype, const int32_t* seq_lens_host,
+                   int num_sms, int max_parts, int32_t* split_pages_out,
+                   int* num_parts_out, float* wave_eff_out);
+
+/*
  * Host-side check of a page table (optional validation mode).  All
  * pointers are HOST copies.  Checks, for every virtual request v < V:
  * 1 <= q_len; 0 <= seq_lens[v] <= stride; without kv_limit seq_lens[v] >=
@@ -172,7 +208,8 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   s_t  = sm_scale * <x, k_t>
  *   LSE_part[s,c,b,i,h] = ln sum_t exp(s_t)            (-inf if no token)
  *   O_part[s,c,b,i,h,:] = sum_t exp(s_t - LSE) k_t[:512] (0 if no token)
- * Split s of a request with P pages covers pages [s*P/S, (s+1)*P/S).
+ * Split s of a request with P pages covers pages [s*P/S, (s+1)*P/S), or the
+ * pages of split_pages when it is given.
  *
  *   q_nope_absorbed  bf16 [B, q_len, H, 512], contiguous, 16-B aligned
  *   q_rope           bf16 [B, q_len, H, 64], contiguous, 16-B aligned
@@ -190,6 +227,16 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   sm_scale         softmax scale, finite and > 0 (1/sqrt(192) for the
  *                    192-d pre-absorption query/key head)
  *   num_splits       KV splits per request, >= 1 (see mla_plan)
+ *   split_pages      device int32 [num_shards*B, num_splits + 1] or NULL:
+ *                    part s of virtual request v covers pages
+ *                    [split_pages[v][s], split_pages[v][s+1]) (clamped to
+ *                    [0, ceil(L_v / 64)]; empty when the upper bound is not
+ *                    above the lower; see mla_plan_parts).  The rows must
+ *                    partition each request's pages (non-decreasing from 0
+ *                    to ceil(L_v / 64)) for the combine to be the full
+ *                    result; NULL deals the pages uniformly.
+ *                    Work is launched split by split (all first parts, then
+ *                    all second parts, ...).
  *   O_part           fp32 [num_splits, num_shards, B, q_len, H, 512], 16-B al.
  *   LSE_part         fp32 [num_splits, num_shards, B, q_len, H]
  *   status           device int or NULL (MLA_STATUS_* bits are OR-ed in)
@@ -202,7 +249,8 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* req_to_token, int64_t r2t_stride,
                        const int32_t* seq_lens, const int32_t* kv_limit,
                        int B, int q_len, int H, int num_shards, int page_size,
-                       float sm_scale, int num_splits, float* O_part,
+                       float sm_scale, int num_splits,
+                       const int32_t* split_pages, float* O_part,
                        float* LSE_part, int* status, mla_stream_t stream);
 
 /*
@@ -217,6 +265,7 @@ int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
                             const int32_t* seq_lens, const int32_t* kv_limit,
                             int B, int q_len, int H, int num_shards,
                             int page_size, float sm_scale, int num_splits,
+                            const int32_t* split_pages,
                             float* O_part, float* LSE_part, int* status,
                             mla_stream_t stream);
 

@@ -58,12 +58,17 @@ def library() -> ctypes.CDLL:
             "mla_plan_heuristic": (i32, [i32, i32]),
             "mla_plan_ex": (i32, [i32, i32, i32, i32, p, i32, i32, f64, f64, p, p, p]),
             "mla_plan": (i32, [i32, i32, i32, i32, i32, p, i32, p, p]),
+            "mla_plan_parts_ex": (i32, [i32, i32, i32, i32, p, i32, i32, i32, f64,
+                                        f64, p, p, p, p]),
+            "mla_plan_parts": (i32, [i32, i32, i32, i32, i32, p, i32, i32, p, p,
+                                     p]),
             "mla_check_page_table": (i32, [p, i64, p, p, i32, i32, i32, i64]),
             "mla_decode_partial": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
-                                         i32, i32, i32, i32, f32, i32, p, p, p, p]),
+                                         i32, i32, i32, i32, f32, i32, p, p, p, p,
+                                         p]),
             "mla_decode_partial_simt": (i32, [p, p, p, p, i32, i64, p, i64, p, p,
                                               i32, i32, i32, i32, i32, f32, i32, p,
-                                              p, p, p]),
+                                              p, p, p, p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
         }
@@ -136,6 +141,42 @@ def plan(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
     return S.value, eff.value
 
 
+def plan_parts_ex(seq_lens: Sequence[int], q_len: int, H: int, slots: int,
+                  s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
+                  lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT):
+    """Per-request split planner: returns (S, boundaries np.int32 [V, S+1],
+    wave_eff, makespan)."""
+    import numpy as np
+    arr = _host_i32(seq_lens)
+    V = len(arr)
+    out = (ctypes.c_int32 * (V * (s_max + 1)))()
+    S, eff, ms = ctypes.c_int(), ctypes.c_float(), ctypes.c_double()
+    _check(library().mla_plan_parts_ex(V, q_len, H, rows_per_unit, arr, slots,
+                                       s_max, max_parts, float(c0), float(lam),
+                                       out, ctypes.byref(S), ctypes.byref(eff),
+                                       ctypes.byref(ms)))
+    bnd = np.frombuffer(out, dtype=np.int32)[:V * (S.value + 1)]
+    return S.value, bnd.reshape(V, S.value + 1).copy(), eff.value, ms.value
+
+
+def plan_parts(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
+               num_sms: int = 0, kv_dtype: str = "bf16", max_parts: int = 8):
+    """Per-request split planner with the library defaults for the kernel
+    that serves `kv_dtype`: returns (S, boundaries np.int32 [V, S+1],
+    wave_eff); num_sms=0 asks the device."""
+    import numpy as np
+    arr = _host_i32(seq_lens)
+    V = len(arr)
+    assert V == B * num_shards
+    out = (ctypes.c_int32 * (V * 65))()
+    S, eff = ctypes.c_int(), ctypes.c_float()
+    _check(library().mla_plan_parts(B, q_len, H, num_shards, _KV_DTYPE[kv_dtype],
+                                    arr, num_sms, max_parts, out,
+                                    ctypes.byref(S), ctypes.byref(eff)))
+    bnd = np.frombuffer(out, dtype=np.int32)[:V * (S.value + 1)]
+    return S.value, bnd.reshape(V, S.value + 1).copy(), eff.value
+
+
 def check_page_table(req_to_token, seq_lens, kv_limit, q_len: int,
                      num_slots: int, page_size: int = PAGE_SIZE) -> None:
     """Host validation of a page table (raises MlaError on a bad entry)."""
@@ -159,8 +200,10 @@ def _kv_dtype(kv: torch.Tensor) -> int:
 def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
                    kv_limit, num_splits: int, sm_scale: float,
                    num_shards: int = 1, O_part=None, LSE_part=None,
-                   status=None, simt: bool = False, stream=None):
+                   status=None, simt: bool = False, stream=None,
+                   split_pages=None):
     """Partial (O, LSE) per split and shard; see mla_decode_partial.
+    `split_pages`: device int32 [num_shards*B, num_splits+1] or None.
 
     Returns (O_part fp32 [S, shards, B, q, H, 512], LSE_part fp32 [S, shards,
     B, q, H]); outputs are allocated with torch unless given.
@@ -178,7 +221,8 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
               _kv_dtype(kv), kv.shape[0], _ptr(req_to_token),
               req_to_token.stride(0), _ptr(seq_lens), _ptr(kv_limit), B, q_len,
               H, num_shards, PAGE_SIZE, float(sm_scale), num_splits,
-              _ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream)))
+              _ptr(split_pages), _ptr(O_part), _ptr(LSE_part), _ptr(status),
+              _stream(stream)))
     return O_part, LSE_part
 
 
@@ -215,21 +259,27 @@ def debug_gather(kv, req_to_token, seq_lens, row_offset, total_rows: int,
 
 
 def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
-           status=None, stream=None):
+           status=None, stream=None, split_pages=None):
     """One decode step of a synth.Batch-like object: partial + combine.
 
-    Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H], num_splits).
+    Without num_splits the per-request split planner chooses the parts
+    (mla_plan_parts); with num_splits and no split_pages the pages are dealt
+    uniformly.  Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H],
+    num_splits).
     """
     wl = batch.wl
+    if num_splits is None and wl.num_splits:
+        num_splits = wl.num_splits
     if num_splits is None:
-        num_splits = wl.num_splits or plan(
+        num_splits, bnd, _ = plan_parts(
             wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards,
-            kv_dtype=wl.kv_dtype)[0]
+            kv_dtype=wl.kv_dtype)
+        split_pages = torch.from_numpy(bnd).to(batch.q_nope.device)
     O_part, LSE_part = decode_partial(
         batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
         batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,
         wl.sm_scale, num_shards=wl.num_shards, status=status, simt=simt,
-        stream=stream)
+        stream=stream, split_pages=split_pages)
     out, lse = lse_combine(O_part, LSE_part, stream=stream)
     return out, lse, num_splits
 

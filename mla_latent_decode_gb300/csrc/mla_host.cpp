@@ -63,7 +63,8 @@ int check_decode_args(const DecodeArgs& a) {
       !aligned(a.req_to_token, 4) || !aligned(a.seq_lens, 4) ||
       (a.kv_limit && !aligned(a.kv_limit, 4)) ||
       (a.kv_scale && !aligned(a.kv_scale, 16)) ||
-      (a.status && !aligned(a.status, 4)))
+      (a.status && !aligned(a.status, 4)) ||
+      (a.split_pages && !aligned(a.split_pages, 4)))
     return fail(MLA_ERR_MISALIGNED,
                 "q/kv/kv_scale/O_part need 16-B alignment, the other arrays 4-B");
   return MLA_OK;
@@ -136,10 +137,10 @@ int mla_plan_ex(int V, int q_len, int H, int rows_per_unit,
   for (int S = 1; S <= s_max; ++S) {
     costs.clear();
     double total = 0;
-    for (int v = 0; v < V; ++v) {
-      const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
-      const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-      for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < S; ++s) {
+      for (int v = 0; v < V; ++v) {
+        const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
+        const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
         const double c = (double)((s + 1) * P / S - s * P / S) + c0;
         for (int g = 0; g < G; ++g) {
           costs.push_back(c);
@@ -184,6 +185,130 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
                      fp8 ? MLA_ROWS_PER_UNIT / 2 : MLA_ROWS_PER_UNIT,
                      seq_lens_host, slots, 64, kPlanUnitCost, kPlanSplitCost,
                      num_splits_out, wave_eff_out, nullptr);
+}
+
+// One split schedule (boundaries bnd[v * (S + 1) + k]) in launch order: part
+// s of every request before part s + 1, row units innermost; a unit costs its
+// pages + c0, an empty one c_empty.  Returns the list-scheduling makespan on
+// `slots` and adds the unit costs to *total.
+static double schedule_makespan(const std::vector<int64_t>& P, int U, int S,
+                                const std::vector<int64_t>& bnd, int slots,
+                                double c0, double c_empty, double* total) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+  const size_t V = P.size();
+  const size_t n = std::min<size_t>((size_t)slots, V * (size_t)S * (size_t)U);
+  for (size_t k = 0; k < n; ++k) heap.push(0.0);
+  double end = 0.0, tot = 0.0;
+  for (int s = 0; s < S; ++s)
+    for (size_t v = 0; v < V; ++v) {
+      const int64_t pages = bnd[v * (S + 1) + s + 1] - bnd[v * (S + 1) + s];
+      const double c = pages > 0 ? (double)pages + c0 : c_empty;
+      for (int u = 0; u < U; ++u) {
+        const double t = heap.top() + c;
+        heap.pop();
+        end = std::max(end, t);
+        heap.push(t);
+        tot += c;
+      }
+    }
+  *total = tot;
+  return end;
+}
+
+int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
+                      const int32_t* seq_lens_host, int slots, int s_max,
+                      int max_parts, double c0, double lam,
+                      int32_t* split_pages_out, int* num_parts_out,
+                      float* wave_eff_out, double* makespan_out) {
+  if (V < 1 || q_len < 1 || H < 1 || !seq_lens_host || !split_pages_out ||
+      !num_parts_out)
+    return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
+  if (rows_per_unit < 1 || slots < 1 || s_max < 1 || s_max > 1024 ||
+      max_parts < 1 || max_parts > s_max || !(c0 >= 0) || !(lam >= 0))
+    return fail(MLA_ERR_INVALID_ARG,
+                "rows_per_unit/slots/s_max/max_parts/c0/lam out of range");
+  const int U = (H * q_len + rows_per_unit - 1) / rows_per_unit;
+  const double rows = (double)V * q_len * H;
+  std::vector<int64_t> P(V);
+  int64_t Pmax = 0;
+  for (int v = 0; v < V; ++v) {
+    const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
+    P[v] = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+    Pmax = std::max(Pmax, P[v]);
+  }
+  constexpr int kCaps = 32;
+  constexpr double kEmpty = 1.0;
+  double bestJ = 0, bestMs = 0, bestTot = 0;
+  int bestS = 0;
+  std::vector<int64_t> bnd, best;
+  auto consider = [&](int S) {
+    double tot = 0;
+    const double ms = schedule_makespan(P, U, S, bnd, slots, c0, kEmpty, &tot);
+    const double J = ms + lam * S * rows / 1024.0;
+    if (bestS == 0 || J < bestJ - 1e-9) {
+      bestJ = J;
+      bestS = S;
+      bestMs = ms;
+      bestTot = tot;
+      best = bnd;
+    }
+  };
+  // Uniform deals.
+  for (int S = 1; S <= s_max; ++S) {
+    bnd.assign((size_t)V * (S + 1), 0);
+    for (int v = 0; v < V; ++v)
+      for (int k = 0; k <= S; ++k) bnd[(size_t)v * (S + 1) + k] = k * P[v] / S;
+    consider(S);
+  }
+  // First part capped at b pages, the rest dealt over S - 1 parts.
+  for (int S = 2; S <= max_parts; ++S) {
+    int64_t prev = -1;
+    for (int k = 1; k <= kCaps; ++k) {
+      const int64_t b = (Pmax * k + kCaps - 1) / kCaps;
+      if (b == prev || b < 1) continue;
+      prev = b;
+      bnd.assign((size_t)V * (S + 1), 0);
+      for (int v = 0; v < V; ++v) {
+        const int64_t first = std::min(P[v], b), rest = P[v] - first;
+        int64_t* row = &bnd[(size_t)v * (S + 1)];
+        row[0] = 0;
+        for (int m = 1; m <= S; ++m) row[m] = first + (m - 1) * rest / (S - 1);
+      }
+      consider(S);
+    }
+  }
+  for (size_t i = 0; i < best.size(); ++i)
+    split_pages_out[i] = (int32_t)best[i];
+  *num_parts_out = bestS;
+  if (wave_eff_out)
+    *wave_eff_out = bestMs > 0 ? (float)(bestTot / ((double)slots * bestMs)) : 1.f;
+  if (makespan_out) *makespan_out = bestMs;
+  return MLA_OK;
+}
+
+int mla_plan_parts(int B, int q_len, int H, int num_shards,
+                   mla_kv_dtype kv_dtype, const int32_t* seq_lens_host,
+                   int num_sms, int max_parts, int32_t* split_pages_out,
+                   int* num_parts_out, float* wave_eff_out) {
+  if (B < 1 || num_shards < 1)
+    return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const int ctas = fp8 ? 2 : 4;
+  int slots;
+  if (num_sms > 0) {
+    slots = std::max(1, num_sms / ctas);
+  } else {
+    slots = fp8 ? pair_slots_fp8() : mla_cluster_slots();
+    if (slots < 0) return slots;
+    if (slots == 0) return fail(MLA_ERR_CUDA, "no decode cluster fits on this device");
+  }
+  return mla_plan_parts_ex(B * num_shards, q_len, H,
+                           fp8 ? MLA_ROWS_PER_UNIT / 2 : MLA_ROWS_PER_UNIT,
+                           seq_lens_host, slots, 64, max_parts, kPlanUnitCost,
+                           kPlanSplitCost, split_pages_out, num_parts_out,
+                           wave_eff_out, nullptr);
 }
 
 int mla_check_page_table(const int32_t* r2t, int64_t stride,
@@ -231,12 +356,13 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* req_to_token, int64_t r2t_stride,
                        const int32_t* seq_lens, const int32_t* kv_limit, int B,
                        int q_len, int H, int num_shards, int page_size,
-                       float sm_scale, int num_splits, float* O_part,
+                       float sm_scale, int num_splits,
+                       const int32_t* split_pages, float* O_part,
                        float* LSE_part, int* status, mla_stream_t stream) {
   DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
                num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
                B,               q_len,     H,        num_shards, page_size,
-               sm_scale,        num_splits, O_part,  LSE_part,  status,
+               sm_scale,        num_splits, split_pages, O_part,  LSE_part,  status,
                (cudaStream_t)stream};
   int rc = check_decode_args(a);
   if (rc != MLA_OK) return rc;
@@ -250,12 +376,13 @@ int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
                             const int32_t* seq_lens, const int32_t* kv_limit,
                             int B, int q_len, int H, int num_shards,
                             int page_size, float sm_scale, int num_splits,
+                            const int32_t* split_pages,
                             float* O_part, float* LSE_part, int* status,
                             mla_stream_t stream) {
   DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
                num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
                B,               q_len,     H,        num_shards, page_size,
-               sm_scale,        num_splits, O_part,  LSE_part,  status,
+               sm_scale,        num_splits, split_pages, O_part,  LSE_part,  status,
                (cudaStream_t)stream};
   int rc = check_decode_args(a);
   if (rc != MLA_OK) return rc;

@@ -42,11 +42,31 @@ struct DecodeArgs {
   int B, q_len, H, num_shards, page_size;
   float sm_scale;
   int num_splits;
+  const int32_t* split_pages;  // device [V, num_splits + 1] or NULL
   float* O_part;
   float* LSE_part;
   int* status;
   cudaStream_t stream;
 };
+
+// Pages [p0, p1) of split s of a request with P pages.  With a split table
+// (`row` = the request's S + 1 boundaries) the boundaries are clamped to
+// [0, P] and a part with p1 <= p0 is empty; without one the pages are dealt
+// uniformly, floor(s P / S) .. floor((s + 1) P / S).
+__host__ __device__ inline void split_page_range(const int32_t* row, int S,
+                                                 int s, int64_t P, int64_t& p0,
+                                                 int64_t& p1) {
+  if (row) {
+    int64_t a = row[s], b = row[s + 1];
+    a = a < 0 ? 0 : (a > P ? P : a);
+    b = b < a ? a : (b > P ? P : b);
+    p0 = a;
+    p1 = b;
+  } else {
+    p0 = (int64_t)s * P / S;
+    p1 = (int64_t)(s + 1) * P / S;
+  }
+}
 
 // Host checks common to every partial-decode launch; returns MLA_OK or an
 // error code with the message set.

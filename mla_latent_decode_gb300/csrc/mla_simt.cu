@@ -33,6 +33,7 @@ struct SimtParams {
   int64_t r2t_stride;
   const int32_t* seq_lens;
   const int32_t* kv_limit;
+  const int32_t* split_pages;  // [V, num_splits + 1] page boundaries or NULL
   int B, q_len, H, V, num_splits, row_blocks;
   float scale_log2;  // sm_scale * log2(e): scores are kept in base 2
   float* O_part;
@@ -90,11 +91,14 @@ __global__ void __launch_bounds__(kWarps * 32)
                          : L - p.q_len + 1 + i;
   n = n > L ? L : (n < 0 ? 0 : n);
 
-  // This split's pages: [s*P/S, (s+1)*P/S).
+  // This split's pages (the caller's table or the uniform deal).
   const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-  const int64_t t_lo = split * P / p.num_splits * MLA_PAGE_SIZE;
-  const int64_t t_hi =
-      min((int64_t)((split + 1) * P / p.num_splits) * MLA_PAGE_SIZE, L);
+  int64_t pg0, pg1;
+  mla::split_page_range(
+      p.split_pages ? p.split_pages + (int64_t)v * (p.num_splits + 1) : nullptr,
+      p.num_splits, split, P, pg0, pg1);
+  const int64_t t_lo = pg0 * MLA_PAGE_SIZE;
+  const int64_t t_hi = min(pg1 * MLA_PAGE_SIZE, L);
 
   const int64_t qrow = (int64_t)b * p.q_len * p.H + row_in_req;
   for (int d = lane; d < MLA_ROW_DIM; d += 32) {
@@ -193,6 +197,7 @@ int launch_simt(const DecodeArgs& a) {
   p.r2t_stride = a.r2t_stride;
   p.seq_lens = a.seq_lens;
   p.kv_limit = a.kv_limit;
+  p.split_pages = a.split_pages;
   p.B = a.B;
   p.q_len = a.q_len;
   p.H = a.H;

@@ -114,6 +114,7 @@ struct TcParams {
   int64_t r2t_stride;
   const int32_t* seq_lens;
   const int32_t* kv_limit;
+  const int32_t* split_pages;  // [V, num_splits + 1] page boundaries or NULL
   int B, q_len, H, V, num_splits, U;  // U = row pairs (256 rows) per request
   float scale_log2;        // sm_scale * log2(e)
   float* O_part;
@@ -196,8 +197,10 @@ __device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
     if (c != rank) st_cluster_u32(mapa(smem_u32(&s.abort_flag), c), 1u);
 }
 
-// Work of one cluster: (virtual request v, split, row pair u); this CTA's
-// row group is 2u + (rank & 1).
+// Work of one cluster: (split, virtual request v, row pair u), launched in
+// that order (split slowest: the planner's list schedule puts every
+// request's first part before any second part); this CTA's row group is
+// 2u + (rank & 1).
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
   int64_t L, p0;
@@ -208,8 +211,8 @@ __device__ __forceinline__ Work unit_work(const TcParams& p, uint32_t rank) {
   int unit = blockIdx.x / kCtas;
   const int u = unit % p.U;
   unit /= p.U;
-  w.split = unit % p.num_splits;
-  w.v = unit / p.num_splits;
+  w.v = unit % p.V;
+  w.split = unit / p.V;
   w.b = w.v % p.B;
   w.shard = w.v / p.B;
   const int R = p.q_len * p.H;
@@ -220,8 +223,10 @@ __device__ __forceinline__ Work unit_work(const TcParams& p, uint32_t rank) {
   if (L < 0) L = 0;
   w.L = L;
   const int64_t P = (L + kPage - 1) / kPage;
-  w.p0 = (int64_t)w.split * P / p.num_splits;
-  const int64_t p1 = (int64_t)(w.split + 1) * P / p.num_splits;
+  int64_t p1;
+  split_page_range(
+      p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
+      p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
   return w;
 }
@@ -951,6 +956,7 @@ int launch_tc(const DecodeArgs& a) {
   p.r2t_stride = a.r2t_stride;
   p.seq_lens = a.seq_lens;
   p.kv_limit = a.kv_limit;
+  p.split_pages = a.split_pages;
   p.B = a.B;
   p.q_len = a.q_len;
   p.H = a.H;

@@ -108,6 +108,7 @@ struct TcParams {
   int64_t r2t_stride;
   const int32_t* seq_lens;
   const int32_t* kv_limit;
+  const int32_t* split_pages;  // [V, num_splits + 1] page boundaries or NULL
   int B, q_len, H, V, num_splits, G;
   float scale_log2;        // sm_scale * log2(e)
   float* O_part;
@@ -190,11 +191,12 @@ struct Work {
 
 __device__ __forceinline__ Work pair_work(const TcParams& p) {
   Work w;
+  // launch order (split, virtual request v, row group g), split slowest
   int pair = blockIdx.x >> 1;
   const int g = pair % p.G;
   pair /= p.G;
-  w.split = pair % p.num_splits;
-  w.v = pair / p.num_splits;
+  w.v = pair % p.V;
+  w.split = pair / p.V;
   w.b = w.v % p.B;
   w.shard = w.v / p.B;
   const int R = p.q_len * p.H;
@@ -205,8 +207,10 @@ __device__ __forceinline__ Work pair_work(const TcParams& p) {
   if (L < 0) L = 0;
   w.L = L;
   const int64_t P = (L + kPage - 1) / kPage;
-  w.p0 = (int64_t)w.split * P / p.num_splits;
-  const int64_t p1 = (int64_t)(w.split + 1) * P / p.num_splits;
+  int64_t p1;
+  split_page_range(
+      p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
+      p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
   return w;
 }
@@ -1005,6 +1009,7 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.r2t_stride = a.r2t_stride;
   p.seq_lens = a.seq_lens;
   p.kv_limit = a.kv_limit;
+  p.split_pages = a.split_pages;
   p.B = a.B;
   p.q_len = a.q_len;
   p.H = a.H;

@@ -11,7 +11,7 @@ sources:
 
 2. A brute-force statement of this library's wave-rounding objective, the
    one the C planner must reproduce exactly:
-     units       one work unit per (virtual request v, split s, row unit u),
+     units       one work unit per (split s, virtual request v, row unit u),
                  launched in that order (u fastest), U = ceil(H*q_len / R),
                  R = rows_per_unit (256: the library's kernel serves 256
                  query rows with one 4-CTA cluster)
@@ -70,11 +70,13 @@ def makespan(costs: Sequence[float], slots: int) -> float:
 def unit_costs(seq_lens: Sequence[int], H: int, q_len: int, S: int,
                c0: float, page: int = 64,
                rows_per_unit: int = ROWS_PER_UNIT) -> List[float]:
+    """Unit costs in launch order: split s of every request before split
+    s + 1, row units innermost."""
     G = -(-H * q_len // rows_per_unit)
     out = []
-    for L in seq_lens:
-        P = -(-L // page)
-        for s in range(S):
+    for s in range(S):
+        for L in seq_lens:
+            P = -(-L // page)
             c = split_pages(P, S, s) + c0
             out.extend([c] * G)
     return out
@@ -94,3 +96,63 @@ def plan(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
         if best is None or J < best[0] - 1e-9:
             best = (J, S, sum(costs) / (slots * ms), ms)
     return best[1], best[2], best[3]
+
+
+# ---------------------------------------------------------------- parts
+N_CAPS = 32        # cap candidates b = ceil(Pmax * k / 32), k = 1..32
+EMPTY_COST = 1.0   # an empty work unit
+
+
+def parts_makespan(P: Sequence[int], U: int, S: int, bnd: List[List[int]],
+                   slots: int, c0: float):
+    """List-scheduling makespan of a per-request split schedule in launch
+    order (part s of every request before part s + 1, row units innermost);
+    a unit costs its pages + c0, an empty one EMPTY_COST.  Returns
+    (makespan, total cost)."""
+    costs = []
+    for s in range(S):
+        for v in range(len(P)):
+            pages = bnd[v][s + 1] - bnd[v][s]
+            c = float(pages) + c0 if pages > 0 else EMPTY_COST
+            costs.extend([c] * U)
+    return makespan(costs, slots), sum(costs)
+
+
+def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
+               s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
+               lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT,
+               page: int = 64):
+    """Brute force over the two candidate families (uniform deals for
+    S = 1..s_max; first part capped at b, the rest dealt over S - 1 parts for
+    S = 2..max_parts), scored by makespan + lam * S * rows / 1024, first of
+    equal scores kept.  Returns (S, boundaries [V][S+1], wave_eff, makespan)."""
+    U = -(-H * q_len // rows_per_unit)
+    rows = len(seq_lens) * q_len * H
+    P = [-(-max(L, 0) // page) for L in seq_lens]
+    pmax = max(P)
+    best = None
+
+    def consider(S, bnd):
+        nonlocal best
+        ms, tot = parts_makespan(P, U, S, bnd, slots, c0)
+        J = ms + lam * S * rows / 1024.0
+        if best is None or J < best[0] - 1e-9:
+            best = (J, S, bnd, tot / (slots * ms) if ms > 0 else 1.0, ms)
+
+    for S in range(1, s_max + 1):
+        consider(S, [[k * p // S for k in range(S + 1)] for p in P])
+    for S in range(2, max_parts + 1):
+        prev = -1
+        for k in range(1, N_CAPS + 1):
+            b = (pmax * k + N_CAPS - 1) // N_CAPS
+            if b == prev or b < 1:
+                continue
+            prev = b
+            bnd = []
+            for p in P:
+                first = min(p, b)
+                rest = p - first
+                bnd.append([0] + [first + (m - 1) * rest // (S - 1)
+                                  for m in range(1, S + 1)])
+            consider(S, bnd)
+    return best[1], best[2], best[3], best[4]

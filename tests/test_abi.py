@@ -118,7 +118,7 @@ def _call_partial(lib, **over):
     return lib.mla_decode_partial(p(a["qn"]), p(a["qr"]), p(a["kv"]), p(a["ks"]),
                                   a["dt"], a["ns"], p(a["r2t"]), a["st"], p(a["sl"]),
                                   p(a["kl"]), a["B"], a["q"], a["H"], a["shards"],
-                                  a["ps"], a["scale"], a["S"], p(a["O"]),
+                                  a["ps"], a["scale"], a["S"], None, p(a["O"]),
                                   p(a["L"]), p(a["status"]), None)
 
 
@@ -138,3 +138,39 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert lib.mla_debug_gather(ctypes.c_void_p(16), 0, 4096, ctypes.c_void_p(16),
                                 64, ctypes.c_void_p(16), ctypes.c_void_p(16), 1,
                                 16, ctypes.c_void_p(16), None) == -2
+
+
+def test_parts_planner_matches_brute_force(lib):
+    rng = random.Random(11)
+    cases = [([100_000] * 16, 96, 5, 36, 256), ([100_000] * 4, 96, 5, 36, 256),
+             ([400_000] * 20, 96, 5, 36, 256), ([256], 16, 1, 36, 256)]
+    for _ in range(12):
+        V = rng.randint(1, 12)
+        lens = [int(np.exp(rng.uniform(np.log(5), np.log(200_000)))) for _ in range(V)]
+        cases.append((lens, rng.choice([16, 96]), rng.randint(1, 5),
+                      rng.choice([7, 36, 76]), rng.choice([128, 256])))
+    for lens, H, q, slots, rpu in cases:
+        c0, lam = rng.choice([(32.0, 1.0), (4.0, 1.0), (0.0, 0.5)])
+        S, bnd, eff, ms = mla.plan_parts_ex(lens, q, H, slots, 16, 4, c0, lam,
+                                            rows_per_unit=rpu)
+        S2, bnd2, eff2, ms2 = ref.plan_parts(lens, H, q, slots, 16, 4, c0, lam,
+                                             rows_per_unit=rpu)
+        assert (S, ms) == (S2, ms2), (lens[:4], H, q, slots, rpu)
+        assert bnd.tolist() == bnd2
+        assert eff == pytest.approx(eff2, rel=1e-6)
+        # every row partitions the request's pages
+        for L, row in zip(lens, bnd.tolist()):
+            assert row[0] == 0 and row[-1] == -(-L // 64)
+            assert all(a <= b for a, b in zip(row, row[1:]))
+
+
+def test_parts_planner_fills_idle_slots_at_dp16():
+    """16 requests x 100k on 36 cluster slots: the best uniform plan runs 32
+    units (4 slots idle); capping the first part and dealing the rest to the
+    idle slots shortens the modelled makespan (c0 = 32, lam = 1)."""
+    lens = [100_000] * 16
+    S_u, _, ms_u = ref.plan(lens, 96, 5, 36, 64, 32.0, 1.0)
+    S_p, bnd, _, ms_p = ref.plan_parts(lens, 96, 5, 36, 64, 8, 32.0, 1.0)
+    assert S_u == 1 and ms_u == 1563 + 32
+    assert S_p >= 2 and ms_p < 0.93 * ms_u
+    assert len({tuple(r) for r in bnd}) == 1   # same cut for every request

@@ -266,3 +266,63 @@ def test_tc_fp8_full_size_ragged_sampled_rows():
     m = check_close(f64(out).reshape(-1, 512)[glob], f64(lse).reshape(-1)[glob],
                     O_ref, l_ref, "fp8_e4m3", f"ragged_fp8 S={S}")
     print("ragged_fp8", S, [wl.seq_lens[r] for r in reqs], m)
+
+
+# ------------------------------------------------- per-request split tables ----
+def _ragged_table(wl, S, seed):
+    """Random non-decreasing boundaries 0 = b0 <= ... <= bS = P per request,
+    with some empty parts."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for L in (wl.seq_lens * wl.num_shards if wl.num_shards == 1 else
+              [synth.shard_lengths(L, wl.q_len, wl.num_shards, s)[0]
+               for s in range(wl.num_shards) for L in wl.seq_lens]):
+        P = -(-L // 64)
+        cuts = sorted(rng.integers(0, P + 1, size=S - 1).tolist())
+        rows.append([0] + cuts + [P])
+    return np.array(rows, dtype=np.int32)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_tc_split_table_parts_and_combine_match_oracle(kv_dtype):
+    wl = synth.Workload("tbl", 3, 5, 96, [3000, 700, 90], kv_dtype=kv_dtype)
+    batch = synth.make_batch(wl, seed=21, device="cuda")
+    hb = synth.host_bits(batch)
+    S = 4
+    table = _ragged_table(wl, S, 3)
+    sp = torch.from_numpy(table).cuda()
+    st = _status()
+    O_part, LSE_part = mla.decode_partial(
+        batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale, batch.req_to_token,
+        batch.seq_lens, batch.kv_limit, S, wl.sm_scale, status=st, split_pages=sp)
+    out, lse = mla.lse_combine(O_part, LSE_part)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = np.arange(wl.rows)
+    b_of = rows // (wl.q_len * wl.H)
+    for s in range(S):
+        lo = np.array([min(table[b][s] * 64, wl.seq_lens[b]) for b in b_of])
+        hi = np.array([min(table[b][s + 1] * 64, wl.seq_lens[b]) for b in b_of])
+        O_ref, l_ref = oracle_rows(batch, hb, rows, lo=lo, hi=hi)
+        check_close(f64(O_part[s, 0]).reshape(-1, 512), f64(LSE_part[s, 0]).reshape(-1),
+                    O_ref, l_ref, kv_dtype, f"part {s}")
+    O_ref, l_ref = oracle_rows(batch, hb, None)
+    check_close(f64(out).reshape(-1, 512), f64(lse).reshape(-1), O_ref, l_ref,
+                kv_dtype, "combined")
+
+
+def test_simt_split_table_matches_tensor_core():
+    wl = synth.Workload("tbl2", 2, 5, 96, [1500, 333], num_shards=8)
+    batch = synth.make_batch(wl, seed=22, device="cuda")
+    S = 3
+    sp = torch.from_numpy(_ragged_table(wl, S, 4)).cuda()
+    a, la = mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, None,
+                               batch.req_to_token, batch.seq_lens, batch.kv_limit,
+                               S, wl.sm_scale, num_shards=8, split_pages=sp)
+    b, lb = mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, None,
+                               batch.req_to_token, batch.seq_lens, batch.kv_limit,
+                               S, wl.sm_scale, num_shards=8, split_pages=sp, simt=True)
+    torch.cuda.synchronize()
+    fa, fb = f64(a).reshape(-1, 512), f64(b).reshape(-1, 512)
+    check_close(fa, f64(la).reshape(-1), fb, f64(lb).reshape(-1), "bf16",
+                "tc vs simt, split table")
