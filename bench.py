@@ -94,26 +94,26 @@ def measured_peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(fp8=False):
+    """Hash of the sources the BF16 (or FP8) tensor-core kernel compiles from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_decode_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.startswith("mla_tc") or f in ("ptx_sm103.cuh", "mla_tma.cuh"):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ("mla_tc_fp8.cu" if fp8 else "mla_tc.cu", "ptx_sm103.cuh",
+              "mla_tma.cuh", "mla_internal.h"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_name, units):
+def profiled_traffic(config_name, units, fp8=False):
     """DRAM bytes per launch from a committed ncu summary, only if it was
-    taken on the current kernel source; scaled by units if captured smaller."""
+    taken on the current source of the kernel the workload runs; scaled by
+    units if captured smaller."""
     try:
         d = json.load(open(PROFILE_TRAFFIC))
     except Exception:
         return None
-    if d.get("kernel_source_hash") != kernel_source_hash():
-        return None
     e = d.get("workloads", {}).get(config_name)
-    if not e:
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(fp8):
         return None
     return e["dram_bytes_per_launch"] * units / e.get("units", units)
 
@@ -464,8 +464,11 @@ def main():
     peaks, peak_kind = measured_peaks()
     part_mean = statistics.mean(part_ms)
     achieved = fl / (part_mean * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
-    traffic = profiled_traffic(args.config, 1)
+    fp8 = wl.kv_dtype != "bf16"
+    # The FP8 kernel's contractions are kind::f8f6f4 MMAs: their dense peak is
+    # the measured BF16 one times the nominal FP8/BF16 ratio (4.5 / 2.25).
+    peak = float(peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)
+    traffic = profiled_traffic(args.config, 1, fp8)
 
     # end to end through the public API from pinned host buffers
     e2e = None
@@ -522,7 +525,8 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if wl.kv_dtype == "bf16" else "f16 (E4M3 KV converted on chip)",
+            "dtype": ("e4m3 (FP8 tensor-core MMAs on the stored KV bytes; bf16 Q and "
+                      "the probabilities each split into two 8-bit parts)") if fp8 else "bf16",
             "data": "synthetic",
             "config": {
                 "workload": workload_desc(wl), "B": wl.B, "q_len": wl.q_len,
@@ -543,8 +547,16 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": traffic,
-                         "kernel": "mla_partial_tc_kernel",
-                         "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)"},
+                         "kernel": ("mla_partial_tc_fp8_kernel" if fp8
+                                    else "mla_partial_tc_kernel"),
+                         "peak_kind": (f"{peak_kind} bf16 burst (cuBLAS) x 2, the "
+                                       "nominal FP8/BF16 dense ratio" if fp8 else
+                                       f"{peak_kind} bf16 burst (cuBLAS)"),
+                         **({"mma_work_per_flop": 2,
+                             "note": "two FP8 MMAs per product (hi/lo split): "
+                                     "the tensor pipe executes 2x the algorithmic "
+                                     "FLOPs, so this design's ceiling is frac 0.5"}
+                            if fp8 else {})},
             "hbm_frac": (sum(wl.seq_lens) * wl.kv_row_bytes() / (part_mean * 1e-3)
                          / 1e9) / float(peaks["hbm_gbs"]),
             "clocks": clk,

@@ -242,6 +242,13 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   status           device int or NULL (MLA_STATUS_* bits are OR-ed in)
  * Rows of slots beyond a request's length (the tail of its last page) are
  * never used, whatever they hold.
+ * Precision with FP8 KV: the contractions run on FP8 tensor cores over the
+ * stored E4M3 bytes.  Each query row is represented as 2^e (hi + lo), two
+ * E4M3 parts with a power-of-two row scale: exact for every element at least
+ * 2^-9 of the row's largest |q|, off by at most 2^-17 of it otherwise.  The
+ * probabilities (times the token's scale) are represented as E4M3 + E5M2
+ * parts, 2^-7 relative error at most.  kv_scale must be finite; its
+ * magnitude may lie anywhere in [2^-100, 2^100].
  */
 int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        const void* kv_pages, const float* kv_scale,

@@ -51,20 +51,21 @@ int make_kv_tensor_map(CUtensorMap* map, const void* kv, mla_kv_dtype dtype,
   return MLA_OK;
 }
 
-int make_kv_tensor_map_fp8_plain(CUtensorMap* map, const void* kv,
-                                 int64_t num_slots) {
+int make_kv_tensor_map_fp8_rope(CUtensorMap* map, const void* kv,
+                                int64_t num_slots) {
   auto fn = encode_fn();
   if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[2] = {(cuuint64_t)MLA_ROW_DIM, (cuuint64_t)num_slots};
   cuuint64_t strides[1] = {(cuuint64_t)MLA_ROW_DIM};
-  cuuint32_t box[2] = {64u, (cuuint32_t)kBoxRows};
+  cuuint32_t box[2] = {(cuuint32_t)MLA_ROPE_DIM, (cuuint32_t)kBoxRows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled (fp8) failed (%d)", (int)r);
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled (fp8 rope) failed (%d)",
+                (int)r);
   return MLA_OK;
 }
 

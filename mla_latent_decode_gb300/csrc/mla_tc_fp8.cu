@@ -1,27 +1,43 @@
 // mla_tc_fp8.cu -- tensor-core partial MLA decode over an FP8 (E4M3) KV
-// cache with one fp32 scale per token.
+// cache with one fp32 scale per token, on FP8 tensor-core MMAs.
 //
 // Same computation as the BF16 path (include/mla_decode.h,
 // mla_decode_partial; [VRAM-KV], [K3-MLA], [K3-SPLIT], [K3-INTRO]) with
 // k_t = e4m3(byte) * kv_scale[slot].
 //
 // Design (GB300, clusters of two CTAs, one CTA per SM):
-//   FP8 halves the KV bytes, so one SM's TMA engine (~45 B/clk for 64-row
-//   boxes) can feed an M = 128 MMA by itself and the kernel keeps the simple
-//   layout of one S-CTA (rank 0) and one O-CTA (rank 1) per 128-row group,
-//   with single-CTA MMAs.  The tensor cores multiply f16 by f16: TMA lands
-//   unswizzled 64-byte-wide E4M3 boxes (64 tokens x 64 dims) in a staging
-//   ring (plus, on the S side, each page's 64 scales); two converter warps
-//   per CTA turn them into f16 tiles (E4M3 values are exact in f16) in the
-//   128-byte-swizzled layout the MMA reads, writing zeros for rows past a
-//   request's length.  On the S side the per-token scale stays outside the
-//   MMA, s_t = scale_t * (q . e4m3_t) in fp32 on each score column, so no
-//   rounding touches the scores (and the LSE); on the O side the converters
-//   write V as f16(e4m3 * scale), one rounding that only O sees.  The S-CTA holds Q (converted to
-//   f16, exact for bf16 values in f16 range) in TMEM / shared memory and
-//   issues M=128, N=64*pages (up to 256) MMAs from one thread; the softmax
-//   and the O-CTA are those of the BF16 pair design, with P shipped as f16.
-//   Every wait is bounded (ptx_sm103.cuh).
+//   The KV bytes go from TMA straight into the operand layout of
+//   tcgen05.mma.kind::f8f6f4, untouched: K tiles K-major with the 128-byte
+//   swizzle (dims 0..511) and the 64-byte swizzle (the 64 RoPE dims), V tiles
+//   MN-major with the 128-byte swizzle.  The other operand of each product is
+//   split in two 8-bit parts so that the result keeps the precision of the
+//   BF16 path:
+//   * Q (bf16) = 2^e (Qhi + Qlo), Qhi = e4m3(Q 2^-e), Qlo = e4m3(Q 2^-e - Qhi),
+//     with a power-of-two row scale 2^e that puts the row's largest |Q| in
+//     [128, 256).  A bf16 value has 8 significant bits; Qhi holds 4 and the
+//     remainder is exact in Qlo for every element at least 2^-9 of the row's
+//     largest; a smaller one is off by at most 2^-17 of it (E4M3's smallest
+//     step, 2^-9, is the floor).  So q . k = 2^e (Qhi . k + Qlo . k): two
+//     MMAs into one fp32 accumulator.  A row whose elements span more than
+//     2^9 therefore carries score errors up to sm_scale * 2^-17 * max|q| *
+//     sum|k| (a bound, reached only by aligned errors).
+//   * The token's scale moves from V to P: P' = p * scale_t * 2^g = Phi +
+//     Plo, Phi = e4m3(P'), Plo = e5m2(P' - Phi) (E5M2's wider exponent keeps
+//     the small remainders), at most 2^-7 relative error per element, like a
+//     bf16 P.  P' . e4m3(V) = (Phi + Plo) . e4m3(V): two MMAs.  The S-CTA
+//     ships p as f16 together with the page's f16 factors scale_t * 2^g, and
+//     four packer warps of the O-CTA (each owns a row) form P' and split it:
+//     the per-token factors and the 8-bit conversions stay off the softmax.
+//   Each product thus takes two 8-bit MMAs, as long as one 16-bit MMA, and
+//   the tensor cores read the E4M3 bytes with no conversion pass.
+//   Rank 0 (S-CTA) holds Qhi/Qlo (TMEM columns [0, 256) for the 512 c_kv
+//   dims, shared memory for the 64 RoPE dims) and one 256-column S tile;
+//   rank 1 (O-CTA) holds O (128 rows x 512 fp32 = all 512 TMEM columns).
+//   g is the exponent with max|scale| 2^g in [0.5, 1) over the tokens seen
+//   so far (a scale warp tracks it per tile), so P' <= p <= 2^8 stays inside
+//   E4M3's range whatever the scales' magnitude; O is kept in units of
+//   2^(m_ref - g), l in units of 2^m_ref.  Every wait is bounded
+//   (ptx_sm103.cuh).
 #include <cuda_bf16.h>
 
 #include "mla_tma.cuh"
@@ -33,28 +49,27 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 512;        // 16 warps = 4 warpgroups
-constexpr int kStages = 2;           // f16 operand stages (4 chunks, 32 KB)
-constexpr int kBoxesPerStage = 4;
-constexpr int kStages8 = 4;          // E4M3 staging stages
-constexpr int kBox8Bytes = 64 * 64;  // 64 tokens x 64 bytes
-constexpr int kScaleBytes = 64 * 4;  // one page's fp32 scales
-constexpr int kStage8Bytes = kBoxesPerStage * (kBox8Bytes + kScaleBytes);
-constexpr int kChunksPerPage = 9;    // 576 dims = 9 x 64
+constexpr int kStages = 4;           // operand ring slots
+constexpr int kStageBytes = 32768;   // S: 4 pages x 128 dims; O: one page of V
+constexpr int kBlocksPerTile = 5;    // S tile: 4 blocks of 128 dims + RoPE
+constexpr int kRopeBoxBytes = MLA_PAGE_SIZE * MLA_ROPE_DIM;  // 4 KB
 constexpr int kTilePages = 4;        // pages per S tile (N <= 256)
 constexpr int kNP = 4;               // P message slots (page index mod 4)
 constexpr int kRows = 128;           // query rows per CTA pair
 constexpr int kPage = MLA_PAGE_SIZE;      // 64 tokens
-constexpr int kPBytes = kRows * kPage * 2;          // 16384
-constexpr int kAlphaOff = kPBytes;                  // float alpha[128]
-constexpr int kFlagOff = kPBytes + kRows * 4;       // uint32 flags[4]
-constexpr int kPMsgBytes = kFlagOff + 16;           // 16912 = 1057 x 16
-constexpr int kPSlotStride = 17408;                 // 17 KB, 1024-aligned
-constexpr uint32_t kSCol0 = 256;                    // S buffer columns
-constexpr float kTau = 8.f;          // lazy-rescale threshold (log2 units)
+constexpr int kPBytes = kRows * 128;      // per row: 64 f16 p, then Phi | Plo
+constexpr int kAlphaOff = kPBytes;        // float alpha[128]
+constexpr int kFlagOff = kPBytes + kRows * 4;  // uint32 flags[4]
+constexpr int kSGOff = kFlagOff + 16;          // f16 scale * 2^g of 64 tokens
+constexpr int kPMsgBytes = kSGOff + 128;       // 17040 = 1065 x 16
+constexpr int kPSlotStride = 17408;            // 17 KB, 1024-aligned
+constexpr uint32_t kQLoCol = 128;   // Qlo columns (Qhi at 0)
+constexpr uint32_t kSCol0 = 256;    // S buffer columns
+constexpr float kTau = 8.f;         // lazy-rescale threshold (log2 units)
 constexpr uint32_t kFull = 0xffffffffu;
 // Register split of the S-CTA (setmaxnreg): 512 threads launch with 128
-// registers each (65,536); the producer/MMA/converter warpgroups (warps 0-3
-// and 12-15) give registers away so the two softmax warpgroups can hold a
+// registers each (65,536); the producer/MMA/scale warpgroups (warps 0-3 and
+// 12-15) give registers away so the two softmax warpgroups can hold a
 // 128 x 256 fp32 score tile.  The split is one-way.
 constexpr int kRegsLaunch = 128;
 constexpr int kRegsControl = 40;
@@ -62,33 +77,38 @@ constexpr int kRegsSoftmax = 216;
 static_assert(256 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 
-// kind::f16 with f16 A and B (format 0) and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn) {
-  return (1u << 4) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// kind::f8f6f4 instruction descriptor: fp32 accumulator, A format a_fmt
+// (0 = E4M3, 1 = E5M2), B E4M3, A K-major, B K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N, uint32_t a_fmt,
+                                               bool b_mn) {
+  return (1u << 4) | (a_fmt << 7) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_s(int pages) {
-  return idesc_f16_f32(128, 64 * pages, false);
+  return idesc_f8(128, 64 * pages, 0u, false);
 }
-constexpr uint32_t kIdescO = idesc_f16_f32(128, 256, true);
+constexpr uint32_t kIdescOHi = idesc_f8(128, 256, 0u, true);  // Phi: E4M3
+constexpr uint32_t kIdescOLo = idesc_f8(128, 256, 1u, true);  // Plo: E5M2
 
 struct __align__(1024) Smem {
-  uint8_t ring[kStages * kBoxesPerStage][kBoxBytes];  // 64 KB f16 operands
-  uint8_t ring8[kStages8][kStage8Bytes];              // 66 KB E4M3 + scales
-  uint8_t qrope[kRows * 128];                         // S-CTA: Q_rope rows
-  float tscale[4][kTilePages][64];  // S-CTA: token scales of tiles j % 4
+  uint8_t ring[kStages][kStageBytes];       // 128 KB operand ring
+  uint8_t qrope[2][kRows * MLA_ROPE_DIM];   // S-CTA: Qhi, Qlo RoPE (64-B swizzle)
+  float tscale[4][kTilePages * kPage];      // S-CTA: token scales of tile j % 4
   uint8_t pslot[kNP][kPSlotStride];
+  uint32_t tsg[4][kTilePages * kPage / 2];  // S-CTA: f16 pairs scale * 2^g
+  int tg[4];                // S-CTA: scale exponent g of tile j % 4
   float fin[kRows];
-  float xch[2][kRows];      // S-CTA: per-warpgroup row maxima / partial sums
-  uint64_t full[kStages];   // converters -> MMA (one arrival per converter warp)
-  uint64_t empty[kStages];  // MMA -> converters
-  uint64_t full8[kStages8]; // TMA -> converters (bytes)
-  uint64_t empty8[kStages8];// converters -> producer (one per converter warp)
-  uint64_t tsready[4];      // S-CTA: tscale[j % 4] written (converter warps)
+  float xch[2][kRows];      // S-CTA: per-warpgroup row values
+  uint64_t full[kStages];   // TMA -> MMA (bytes)
+  uint64_t empty[kStages];  // MMA -> producer
+  uint64_t scfull[4];       // S-CTA: scale bulk copies landed
+  uint64_t scempty[4];      // S-CTA: softmax done with tscale[j % 4]
+  uint64_t tsready[4];      // S-CTA: tscale, tsg, tg of tile j % 4 written
   uint64_t sfull, sempty;
   uint64_t pfull[kNP];
+  uint64_t packed[kNP];     // O-CTA: P' of slot k split into Phi | Plo
   uint64_t pempty[kNP];
-  uint64_t drain, corr_done, fin_full, qready;
+  uint64_t drain, corr_done, fin_full, qready, tail_go, tail_ready;
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -97,7 +117,8 @@ struct __align__(1024) Smem {
 constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kPMsgBytes % 16 == 0, "bulk copy size");
-static_assert(kStage8Bytes % 128 == 0, "staging stage alignment");
+static_assert(kTilePages * kBoxBytes == kStageBytes, "S stage = 4 pages");
+static_assert(4 * kBoxBytes == kStageBytes, "O stage = one page of V");
 
 struct TcParams {
   const uint4* q_nope;     // bf16 [B, q_len, H, 512] as 16-B chunks
@@ -122,15 +143,16 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  uint32_t y;
-  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(y) : "f"(lo), "f"(hi));
-  return y;
+// F with x in [2^(F-1), 2^F) for a positive finite x (a subnormal x counts
+// as 2^-126).
+__device__ __forceinline__ int exponent_of(float x) {
+  const int f = (int)((__float_as_uint(x) >> 23) & 0xFFu);
+  return (f == 0 ? 1 : f) - 126;
 }
 
-// Packed bf16 pair -> packed f16 pair (both halves rounded to nearest).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  return pack_f16(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+// 2^k as a float, k in [-126, 127].
+__device__ __forceinline__ float exp2i(int k) {
+  return __int_as_float((k + 127) << 23);
 }
 
 // Three-operand maximum (one ALU instruction on sm_100 and later).
@@ -165,6 +187,80 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// |x| maximum of the 8 bf16 values of a 16-byte chunk.
+__device__ __forceinline__ float absmax_bf16x8(uint4 x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    m = max3(m, fabsf(__uint_as_float(w[k] << 16)),
+             fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+  return m;
+}
+
+// Q split: values a (element 2c) and b (element 2c + 1), already multiplied
+// by the row's 2^-e, become hi = e4m3 pair and lo = e4m3 pair of the
+// remainders (lower byte = element 2c).  The remainder a - hi(a) is exact in
+// fp32, so lo rounds it once.
+__device__ __forceinline__ void split_q_pair(float a, float b, uint32_t& hi,
+                                             uint32_t& lo) {
+  asm("{\n\t.reg .b16 h, l, h0, h1;\n\t.reg .b32 hf;\n\t.reg .f32 fa, fb;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %3, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 hf, h;\n\t"
+      "mov.b32 {h0, h1}, hf;\n\t"
+      "cvt.f32.f16 fa, h0;\n\tcvt.f32.f16 fb, h1;\n\t"
+      "sub.rn.f32 fa, %2, fa;\n\tsub.rn.f32 fb, %3, fb;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, fb, fa;\n\t"
+      "cvt.u32.u16 %0, h;\n\tcvt.u32.u16 %1, l;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "f"(a), "f"(b));
+}
+
+// 8 bf16 Q values (one 16-byte chunk) times 2^-e -> 8 Qhi bytes and 8 Qlo
+// bytes, in element order.
+__device__ __forceinline__ void split_q8(uint4 x, float inv, uint2& hi,
+                                         uint2& lo) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    split_q_pair(__uint_as_float(w[k] << 16) * inv,
+                 __uint_as_float(w[k] & 0xFFFF0000u) * inv, h[k], l[k]);
+  hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+  lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+}
+
+// P split of four consecutive f16 values (two f16x2 words, P' < 256):
+// hi = their 4 E4M3 bytes, lo = 4 E5M2 bytes of P' - hi (exact in f16).
+__device__ __forceinline__ void split_p4(uint32_t w0, uint32_t w1, uint32_t& hi,
+                                         uint32_t& lo) {
+  asm("{\n\t.reg .b32 b0, b1, r0, r1;\n\t.reg .b16 h0, h1, l0, l1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 h0, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 h1, %3;\n\t"
+      "cvt.rn.f16x2.e4m3x2 b0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 b1, h1;\n\t"
+      "sub.rn.f16x2 r0, %2, b0;\n\t"
+      "sub.rn.f16x2 r1, %3, b1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f16x2 l0, r0;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f16x2 l1, r1;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t"
+      "mov.b32 %1, {l0, l1};\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "r"(w0), "r"(w1));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t y;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t y;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(y) : "f"(lo), "f"(hi));
+  return y;
+}
+
 // Record a failed wait: device status, this CTA's and the peer's abort flag.
 __device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
                                              uint32_t rank) {
@@ -187,6 +283,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
   int64_t L, p0;
+  bool tail;  // the split's last page is the request's partial last page
 };
 
 __device__ __forceinline__ Work pair_work(const TcParams& p) {
@@ -212,6 +309,7 @@ __device__ __forceinline__ Work pair_work(const TcParams& p) {
       p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
       p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
+  w.tail = w.npages > 0 && p1 == P && (L % kPage) != 0;
   return w;
 }
 
@@ -230,12 +328,14 @@ __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
 }
 
 // ------------------------------------------------------------ producers ---
-// S-CTA staging stage = chunk c (64 dims) of the (up to 4) pages of an S tile,
-// each box in slot q of the stage together with its page's 64 scales;
-// O-CTA staging stage = chunks 4h..4h+3 of one page (the value dims) with
-// the page's scales in slot 0.
-// Page bases are read 32 pages ahead (one per lane).
+// S-CTA: per S tile (up to 4 pages) the pages' 64 scales each into
+// tscale[j % 4] by bulk copy (zeros, written here, for a page outside the
+// pool), then 5 ring stages: dims 128c..128c+127 of the tile's pages
+// (c = 0..3, one 8-KB box per page) and the RoPE dims (one 4-KB box per page).
+// Page bases are read 32 pages ahead (one per lane).  A page outside the
+// pool is loaded from row num_slots: TMA fills it with zeros.
 __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
+                                           const CUtensorMap* map_rope,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
   uint32_t stage = 0, phase = 0;
@@ -252,25 +352,39 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
     const int32_t bq = __shfl_sync(kFull, cur, (m0 + (lane & 3)) & 31);
     const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
     if (lane < np && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
-    for (int c = 0; c < kChunksPerPage && ok; ++c) {
+    const int ts = j & 3;
+    if (lane == 0 &&
+        !mbar_wait(smem_u32(&s.scempty[ts]), ((j >> 2) & 1) ^ 1u, &s.abort_flag))
+      ok = false;
+    ok = __shfl_sync(kFull, ok, 0);
+    if (!ok) break;
+    const bool bad = lane < np && bq < 0;
+    if (bad) {
+      for (int e = 0; e < kPage; ++e) s.tscale[ts][lane * kPage + e] = 0.f;
+      fence_proxy_async_smem();
+    }
+    const uint32_t good = __ballot_sync(kFull, lane < np && bq >= 0);
+    if (lane == 0)
+      mbar_arrive_expect_tx(smem_u32(&s.scfull[ts]),
+                            (uint32_t)__popc(good) * kPage * 4);
+    __syncwarp();
+    if (lane < np && bq >= 0)
+      bulk_load(smem_u32(&s.tscale[ts][lane * kPage]), p.kv_scale + bq,
+                kPage * 4, smem_u32(&s.scfull[ts]));
+    for (int c = 0; c < kBlocksPerTile && ok; ++c) {
+      const bool rope = c == kBlocksPerTile - 1;
+      const uint32_t box = rope ? kRopeBoxBytes : kBoxBytes;
       if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty8[stage]), phase ^ 1u, &s.abort_flag))
-          mbar_arrive_expect_tx(smem_u32(&s.full8[stage]),
-                                np * (kBox8Bytes + kScaleBytes));
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
+          mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * box);
         else
           ok = false;
       }
       ok = __shfl_sync(kFull, ok, 0);
-      if (ok && lane < np) {
-        uint8_t* st = s.ring8[stage];
-        const uint32_t bar = smem_u32(&s.full8[stage]);
-        tma_load_2d(smem_u32(st + lane * kBox8Bytes), map, bar, c * 64, yq);
-        // scales of a page outside the pool: read those of page 0 (unused)
-        const int64_t sb = bq < 0 ? 0 : bq;
-        bulk_load(smem_u32(st + kBoxesPerStage * kBox8Bytes + lane * kScaleBytes),
-                  p.kv_scale + sb, kScaleBytes, bar);
-      }
-      if (++stage == kStages8) {
+      if (ok && lane < np)
+        tma_load_2d(smem_u32(s.ring[stage]) + lane * box, rope ? map_rope : map,
+                    smem_u32(&s.full[stage]), rope ? MLA_NOPE_DIM : 128 * c, yq);
+      if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -279,6 +393,7 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
+// O-CTA: one ring stage per page, the 512 value dims as 4 boxes of 128.
 __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
@@ -292,158 +407,77 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     }
     const int32_t b = __shfl_sync(kFull, cur, m & 31);
     const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
-    for (int h = 0; h < 2 && ok; ++h) {
-      if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty8[stage]), phase ^ 1u, &s.abort_flag))
-          mbar_arrive_expect_tx(smem_u32(&s.full8[stage]),
-                                kBoxesPerStage * kBox8Bytes + kScaleBytes);
-        else
-          ok = false;
-      }
-      ok = __shfl_sync(kFull, ok, 0);
-      if (ok && lane < kBoxesPerStage) {
-        uint8_t* st = s.ring8[stage];
-        const uint32_t bar = smem_u32(&s.full8[stage]);
-        tma_load_2d(smem_u32(st + lane * kBox8Bytes), map, bar,
-                    (4 * h + lane) * 64, y);
-        if (lane == 0)
-          bulk_load(smem_u32(st + kBoxesPerStage * kBox8Bytes),
-                    p.kv_scale + (b < 0 ? 0 : b), kScaleBytes, bar);
-      }
-      if (++stage == kStages8) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    if (lane == 0) {
+      if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
+        mbar_arrive_expect_tx(smem_u32(&s.full[stage]), kStageBytes);
+      else
+        ok = false;
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    if (ok && lane < 4)
+      tma_load_2d(smem_u32(s.ring[stage]) + lane * kBoxBytes, map,
+                  smem_u32(&s.full[stage]), 128 * lane, y);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
-// ----------------------------------------------------------- converters ---
-// Warps 2, 3, 12, 13 of the S-CTA and 2, 3, 8, 9 of the O-CTA (NT = 128).
-// A stage holds 4 slots x 64 token rows x 64 E4M3 bytes = 1024 items of 16
-// bytes: item (slot q, n) is row r = n / 4, quarter h = n % 4 of slot q.
-// Thread t takes, slot by slot, the 256 / NT items n = t + k*NT, all loaded
-// before any is converted (a load issued after a store that may alias it
-// would wait for it), converts each exactly to 16 f16 (cvt e4m3x2 -> f16x2)
-// and stores them as 16-byte groups 2h, 2h+1 of row r in the
-// 128-byte-swizzled f16 chunk of slot q.  Rows at or past a page's length
-// (and slots of pages a short tile does not have) become zeros: 0 * NaN in
-// P V must not see undefined rows.  The O side multiplies by the token's
-// scale in f16 (V' = e4m3 * scale); on the S side, chunk 0 of a tile
-// publishes the tile's token scales (tscale[j % 4], tsready) for the
-// softmax instead.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t& lo,
-                                                uint32_t& hi) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(four));
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t y;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
-  return y;
-}
-
-template <int NT>
-__device__ __forceinline__ void converter(Smem& s, const TcParams& p,
-                                          const Work& w, uint32_t rank, int t,
-                                          int lane) {
-  constexpr int kPer = 256 / NT;  // items per thread per slot
-  uint32_t st8 = 0, ph8 = 0, st = 0, ph = 0;
+// S-CTA warp 2: per tile, zero the scales of tokens at or past the request's
+// length (their slots are undefined; 0 keeps every product finite) and of
+// pages the tile lacks; track the running max |scale| over the split and its
+// exponent g (max |scale| 2^g in [0.5, 1)); publish the tile's scale * 2^g
+// as f16 pairs (the factor the packers apply to p) and g.
+__device__ __forceinline__ void scale_warp(Smem& s, const TcParams& p,
+                                           const Work& w, uint32_t rank,
+                                           int lane) {
   bool ok = true;
-  // stages in order: S-CTA: tile j, chunk c; O-CTA: page m, half h
+  float smax = 0.f;
+  int g = 0;
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
-  const int nst = rank == 0 ? ntiles * kChunksPerPage : w.npages * 2;
-  for (int u = 0; u < nst && ok; ++u) {
-    // Tokens of the stage's first slot that exist: slot q of an S stage is
-    // page q of the tile; all slots of an O stage are the same page.
-    int64_t left;
-    int np;
-    if (rank == 0) {
-      const int j = u / kChunksPerPage;
-      np = tile_pages(w, j);
-      left = w.L - (w.p0 + (int64_t)j * kTilePages) * kPage;
-    } else {
-      np = kBoxesPerStage;
-      left = w.L - (w.p0 + (int64_t)(u >> 1)) * kPage;
-    }
-    const int left0 =
-        left <= 0 ? 0 : (left >= 4 * kPage ? 4 * kPage : (int)left);
-    if (!mbar_wait(smem_u32(&s.full8[st8]), ph8, &s.abort_flag) ||
-        !mbar_wait(smem_u32(&s.empty[st]), ph ^ 1u, &s.abort_flag)) {
+  for (int j = 0; j < ntiles; ++j) {
+    const int ts = j & 3;
+    if (!mbar_wait(smem_u32(&s.scfull[ts]), (j >> 2) & 1, &s.abort_flag)) {
       ok = false;
       break;
     }
-    const uint8_t* src = s.ring8[st8];
-    uint8_t* dst = s.ring[st * kBoxesPerStage];
-    const float* scl =
-        reinterpret_cast<const float*>(src + kBoxesPerStage * kBox8Bytes);
-#pragma unroll 1
-    for (int q = 0; q < kBoxesPerStage; ++q) {
-      const int vq = q >= np ? 0 : (rank == 0 ? left0 - q * kPage : left0);
-      const uint8_t* sq = src + q * kBox8Bytes;
-      uint8_t* dq = dst + q * kBoxBytes;
-      uint4 x[kPer];
+    const int np = tile_pages(w, j);
+    const int64_t left = w.L - (w.p0 + (int64_t)j * kTilePages) * kPage;
+    const int valid = (int)(left < (int64_t)np * kPage ? left : (int64_t)np * kPage);
+    float v[8];
+    float mx = 0.f;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k)
-        x[k] = *reinterpret_cast<const uint4*>(sq + (t + k * NT) * 16);
+    for (int i = 0; i < 4; ++i) {  // token pair q = lane + 32 i
+      const int t = 2 * (lane + 32 * i);
+      const float2 x = *reinterpret_cast<const float2*>(&s.tscale[ts][t]);
+      v[2 * i] = t < valid ? x.x : 0.f;
+      v[2 * i + 1] = t + 1 < valid ? x.y : 0.f;
+      *reinterpret_cast<float2*>(&s.tscale[ts][t]) = make_float2(v[2 * i], v[2 * i + 1]);
+      mx = max3(mx, fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+    }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int n = t + k * NT, r = n >> 2, h = n & 3;
-        if (r >= vq) x[k] = make_uint4(0, 0, 0, 0);  // E4M3 0 -> f16 +0
-        uint4 lo, hi;
-        e4m3x4_to_f16x4(x[k].x, lo.x, lo.y);
-        e4m3x4_to_f16x4(x[k].y, lo.z, lo.w);
-        e4m3x4_to_f16x4(x[k].z, hi.x, hi.y);
-        e4m3x4_to_f16x4(x[k].w, hi.z, hi.w);
-        if (rank == 1) {
-          // rows past the length: scale 0, not the slot's (undefined) one
-          const float sv = r < vq ? scl[r] : 0.f;
-          const uint32_t s2 = pack_f16(sv, sv);
-          lo = make_uint4(hmul2(lo.x, s2), hmul2(lo.y, s2), hmul2(lo.z, s2),
-                          hmul2(lo.w, s2));
-          hi = make_uint4(hmul2(hi.x, s2), hmul2(hi.y, s2), hmul2(hi.z, s2),
-                          hmul2(hi.w, s2));
-        }
-        uint8_t* d = dq + (r >> 3) * 1024;
-        *reinterpret_cast<uint4*>(d + box_chunk_offset(r & 7, 2 * h)) = lo;
-        *reinterpret_cast<uint4*>(d + box_chunk_offset(r & 7, 2 * h + 1)) = hi;
-      }
-    }
-    const bool scales = rank == 0 && u % kChunksPerPage == 0;
-    const int tj = (u / kChunksPerPage) & 3;
-    if (scales) {
-      for (int idx = t; idx < kTilePages * 64; idx += NT) {
-        const int q = idx >> 6, r = idx & 63;
-        const int vq = q >= np ? 0 : left0 - q * kPage;
-        s.tscale[tj][q][r] = r < vq ? scl[idx] : 0.f;
-      }
-    }
-    fence_proxy_async_smem();
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    smax = fmaxf(smax, mx);
+    if (smax > 0.f) g = min(126, max(-126, -exponent_of(smax)));
+    const float G = exp2i(g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      s.tsg[ts][lane + 32 * i] = pack_f16(v[2 * i] * G, v[2 * i + 1] * G);
+    if (lane == 0) s.tg[ts] = g;
+    fence_proxy_async_smem();  // tscale is the next bulk copy's target
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(smem_u32(&s.full[st]));
-      mbar_arrive(smem_u32(&s.empty8[st8]));
-      if (scales) mbar_arrive(smem_u32(&s.tsready[tj]));
-    }
-    if (++st8 == kStages8) {
-      st8 = 0;
-      ph8 ^= 1u;
-    }
-    if (++st == kStages) {
-      st = 0;
-      ph ^= 1u;
-    }
+    if (lane == 0) mbar_arrive(smem_u32(&s.tsready[ts]));
   }
-  if (!__all_sync(kFull, ok) && lane == 0) signal_abort(s, p, rank);
+  if (!ok && lane == 0) signal_abort(s, p, rank);
 }
 
 // ---------------------------------------------------------- S-CTA: MMA ----
-// One issuing thread: per f16 stage (chunk c of the tile's pages) 4 MMAs of
-// M=128, N=64*pages, K=16 into TMEM columns [256, 256 + 64*pages).
+// One issuing thread.  Per tile: for each 128-dim block 4 K steps of 32,
+// each Qhi then Qlo (A from TMEM) against the same K rows; then the RoPE
+// block, 2 K steps, A from shared memory.  M=128, N=64*pages, into TMEM
+// columns [256, 256 + 64*pages).
 __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
                                       uint32_t rank) {
@@ -453,7 +487,8 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
   }
   tc_fence_after();
   const uint32_t d = tmem + kSCol0;
-  const uint64_t qr = sdesc_sw128(smem_u32(s.qrope), 16, 1024);
+  const uint64_t qr_hi = sdesc_sw64(smem_u32(s.qrope[0]), 16, 512);
+  const uint64_t qr_lo = sdesc_sw64(smem_u32(s.qrope[1]), 16, 512);
   uint32_t stage = 0, phase = 0;
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles; ++j) {
@@ -463,24 +498,27 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
       return;
     }
     tc_fence_after();
-    for (int c = 0; c < kChunksPerPage; ++c) {
+    for (int c = 0; c < kBlocksPerTile; ++c) {
       if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
         signal_abort(s, p, rank);
         return;
       }
       tc_fence_after();
-      const uint64_t b =
-          sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]), 16, 1024);
-      if (c < 8) {
-        mma_ts(d, tmem + 32u * c + 0, b + 0, idesc, c > 0 ? 1u : 0u);
-        mma_ts(d, tmem + 32u * c + 8, b + 2, idesc, 1u);
-        mma_ts(d, tmem + 32u * c + 16, b + 4, idesc, 1u);
-        mma_ts(d, tmem + 32u * c + 24, b + 6, idesc, 1u);
+      if (c < kBlocksPerTile - 1) {
+        const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t col = 32u * c + 8u * kk;
+          mma_ts_f8(d, tmem + col, b + 2 * kk, idesc, (c | kk) ? 1u : 0u);
+          mma_ts_f8(d, tmem + kQLoCol + col, b + 2 * kk, idesc, 1u);
+        }
       } else {
-        mma_ss(d, qr + 0, b + 0, idesc, 1u);
-        mma_ss(d, qr + 2, b + 2, idesc, 1u);
-        mma_ss(d, qr + 4, b + 4, idesc, 1u);
-        mma_ss(d, qr + 6, b + 6, idesc, 1u);
+        const uint64_t b = sdesc_sw64(smem_u32(s.ring[stage]), 16, 512);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          mma_ss_f8(d, qr_hi + 2 * kk, b + 2 * kk, idesc, 1u);
+          mma_ss_f8(d, qr_lo + 2 * kk, b + 2 * kk, idesc, 1u);
+        }
       }
       mma_commit(smem_u32(&s.empty[stage]));
       if (++stage == kStages) {
@@ -494,9 +532,7 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
 
 // ------------------------------------------------------ S-CTA: softmax ----
 // Warps 4..11: warpgroup g = 0 (warps 4-7) owns pages 0,1 of each S tile,
-// g = 1 (warps 8-11) pages 2,3.  Thread = query row r (TMEM lane).  Q is
-// converted to f16 on the way in (TMEM / shared memory) and P leaves as f16
-// pairs: the MMAs of this kernel multiply f16 by f16.
+// g = 1 (warps 8-11) pages 2,3.  Thread = query row r (TMEM lane).
 __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
                                         const Work& w, uint32_t tmem,
                                         uint32_t rank, int warp, int lane) {
@@ -514,33 +550,59 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     n = n > w.L ? w.L : (n < 0 ? 0 : n);
   }
   const int64_t qrow = (int64_t)w.b * p.q_len * p.H + rr;
+  const uint4 zero4 = make_uint4(0, 0, 0, 0);
 
-  // Q row: nope part -> TMEM columns [0, 256) (column c holds elements 2c,
-  // 2c+1), rope part -> shared memory in the K-major 128-B swizzled layout.
+  // Row scale 2^e: the row's largest |q| (both warpgroups' parts) lands in
+  // [128, 256) after multiplying by 2^-e.
+  float amax = 0.f;
+  if (g == 0) {
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k)
+      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_nope[qrow * 64 + k] : zero4));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_rope[qrow * 8 + k] : zero4));
+  }
+  s.xch[g][r] = amax;
+  named_bar_sync(1, 256);
+  amax = fmaxf(s.xch[0][r], s.xch[1][r]);
+  named_bar_sync(1, 256);
+  const int e = amax > 0.f ? min(126, max(-126, exponent_of(amax) - 8)) : 0;
+  const float inv = exp2i(-e);
+  const float crow = p.scale_log2 * exp2i(e);
+
+  // Qhi / Qlo: c_kv dims -> TMEM columns [0, 128) and [128, 256) (column c
+  // holds elements 4c..4c+3), RoPE dims -> shared memory, K-major rows of 64
+  // bytes with the 64-byte swizzle.
   if (g == 0) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t v[32];
-      const uint4* src = p.q_nope + qrow * 64 + c * 8;
+    for (int c = 0; c < 4; ++c) {  // 128 dims = 32 columns per step
+      uint32_t vh[32], vl[32];
+      const uint4* src = p.q_nope + qrow * 64 + c * 16;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 x = row_ok ? src[k] : make_uint4(0, 0, 0, 0);
-        v[4 * k] = bf16x2_to_f16x2(x.x);
-        v[4 * k + 1] = bf16x2_to_f16x2(x.y);
-        v[4 * k + 2] = bf16x2_to_f16x2(x.z);
-        v[4 * k + 3] = bf16x2_to_f16x2(x.w);
+      for (int k = 0; k < 16; ++k) {
+        uint2 h, l;
+        split_q8(row_ok ? src[k] : zero4, inv, h, l);
+        vh[2 * k] = h.x;
+        vh[2 * k + 1] = h.y;
+        vl[2 * k] = l.x;
+        vl[2 * k + 1] = l.y;
       }
-      tmem_st32(tmem + lane_base + 32u * c, v);
+      tmem_st32(tmem + lane_base + 32u * c, vh);
+      tmem_st32(tmem + lane_base + kQLoCol + 32u * c, vl);
     }
     tmem_wait_st();
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 x = row_ok ? p.q_rope[qrow * 8 + k] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(s.qrope + (r >> 3) * 1024 +
-                                box_chunk_offset(r & 7, k)) =
-          make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                     bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+    for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk cc = elements 16cc..16cc+15
+      uint2 h0, l0, h1, l1;
+      split_q8(row_ok ? p.q_rope[qrow * 8 + 2 * cc] : zero4, inv, h0, l0);
+      split_q8(row_ok ? p.q_rope[qrow * 8 + 2 * cc + 1] : zero4, inv, h1, l1);
+      const uint32_t off = (r >> 3) * 512 + (r & 7) * 64 +
+                           (((cc ^ (r >> 1)) & 3) << 4);
+      *reinterpret_cast<uint4*>(s.qrope[0] + off) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+      *reinterpret_cast<uint4*>(s.qrope[1] + off) = make_uint4(l0.x, l0.y, l1.x, l1.y);
     }
     fence_proxy_async_smem();
   }
@@ -548,12 +610,15 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&s.qready));
 
+  // Running state: m_ref (log2 units, lazy), l in units of 2^m_ref, and the
+  // split's scale exponent g_cur: O accumulates p * scale * 2^g_cur, so it
+  // is kept in units of 2^(m_ref - g_cur).
   float m_ref = -INFINITY, l = 0.f;
+  int g_cur = 0;
   bool ok = true;
   const uint32_t peer_pfull0 = mapa(smem_u32(&s.pfull[0]), 1);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   const uint32_t bar_wg = 2 + g;  // named barrier of this warpgroup
-  const float sc = p.scale_log2;
   for (int j = 0; j < ntiles; ++j) {
     const int np = tile_pages(w, j);
     const int myp = min(2, max(0, np - 2 * g));  // pages this warpgroup owns
@@ -574,12 +639,11 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.sempty));
 
-    // Token scales of this warpgroup's 128 columns (pages 2g, 2g+1 of the
-    // tile): s_t = scale_t * (q . e4m3_t).  Broadcast reads.
+    // Token scales of this warpgroup's 128 columns: raw -> raw * scale_t.
     if (ok && !mbar_wait(smem_u32(&s.tsready[j & 3]), (j >> 2) & 1,
                          &s.abort_flag))
       ok = false;
-    const float* tsc = &s.tscale[j & 3][2 * g][0];
+    const float* tsc = &s.tscale[j & 3][128 * g];
     auto apply_scale = [&](uint32_t (&a)[32], int c0) {
 #pragma unroll
       for (int c = 0; c < 32; c += 4) {
@@ -609,9 +673,7 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     const int64_t nv = n - t0;
     const int nvis = nv <= 0 ? 0 : (nv >= 64 * myp ? 64 * myp : (int)nv);
     // Columns this row may not see become -inf (a select: garbage or NaN in
-    // a masked column never propagates).  Only the tiles at the end of the
-    // split need it; on every other tile all 128 columns of every row of the
-    // warp are visible and the scores are used as loaded.
+    // a masked column never propagates).
     if (!__all_sync(kFull, nvis == 128)) {
       auto mask = [&](uint32_t (&a)[32], int c0) {
 #pragma unroll
@@ -627,8 +689,8 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
       return __uint_as_float(c < 32 ? s0[c] : c < 64 ? s1[c - 32]
                                     : c < 96 ? s2[c - 64] : s3[c - 96]);
     };
-    // Row maximum of the raw scores; the scale is positive, so the maximum
-    // of the scaled scores is the scaled maximum (rounding is monotone).
+    // Row maximum of raw * scale; the row factor crow is positive, so the
+    // maximum of the scores is crow times it (rounding is monotone).
     float mx[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c)
@@ -639,46 +701,50 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     const float m5c = max3(mx[6], mx[7], mx[8]), m5d = max3(mx[9], mx[10], mx[11]);
     const float m5e = max3(mx[12], mx[13], mx[14]);
     const float mt_own =
-        max3(max3(m5a, m5b, m5c), max3(m5d, m5e, mx[15]), -INFINITY) * sc;
-    // Row maximum over the whole tile: exchange with the other warpgroup.
+        max3(max3(m5a, m5b, m5c), max3(m5d, m5e, mx[15]), -INFINITY) * crow;
     s.xch[g][r] = mt_own;
     named_bar_sync(1, 256);
     const float mt = fmaxf(mt_own, s.xch[g ^ 1][r]);
     named_bar_sync(1, 256);  // both read before the next tile overwrites
+
+    // g of this tile (from the scale warp: max |scale| so far times 2^g in
+    // [0.5, 1)).  alpha is O's factor, 2^((m_ref - m_new) + (g_new - g)).
+    const int g_new = s.tg[j & 3];
+    float m_new = m_ref;
+    if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kTau)) m_new = mt;
     float alpha = 1.f;
-    if (mt > -INFINITY) {
-      if (m_ref == -INFINITY) {
-        m_ref = mt;  // first visible token of this row: O is still zero
-      } else if (mt > m_ref + kTau) {
-        alpha = ex2(m_ref - mt);
-        l *= alpha;
-        m_ref = mt;
-      }
+    if (m_ref > -INFINITY && (m_new != m_ref || g_new != g_cur)) {
+      if (m_new != m_ref) l *= ex2(m_ref - m_new);
+      alpha = ex2((m_ref - m_new) + (float)(g_new - g_cur));
     }
+    m_ref = m_new;
+    g_cur = g_new;
     // A row with nothing visible yet keeps m_ref = -inf: shift by 0 instead
     // so every p is ex2(-inf) = 0, not NaN.
     const float shift = m_ref == -INFINITY ? 0.f : m_ref;
 
-    // P of both pages, packed f16 pairs, computed before any wait for a
-    // message slot so the exponentials stay off the cross-SM round trip.
+    // p = 2^(raw*scale*crow - m_ref) <= 2^tau, l += p, p as packed f16 pairs
+    // (32 words per page); the packers multiply by scale * 2^g.
     uint32_t pk0[32], pk1[32];
-    // p = 2^(x * scale - m_ref): one packed FMA per pair of columns, the row
-    // sum in two packed accumulators.
-    const uint64_t sc2 = f2pack(sc, sc), nshift2 = f2pack(-shift, -shift);
+    const uint64_t c2 = f2pack(crow, crow), nshift2 = f2pack(-shift, -shift);
     auto make_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
                          uint32_t (&pk)[32]) {
       uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int c0 = 2 * c;
-        const float xa = __uint_as_float(c0 < 32 ? lo[c0] : hi[c0 - 32]);
-        const float xb = __uint_as_float(c0 + 1 < 32 ? lo[c0 + 1] : hi[c0 - 31]);
-        float ya, yb;
-        f2unpack(ffma2(f2pack(xa, xb), sc2, nshift2), ya, yb);
-        const float pa = ex2(ya), pb = ex2(yb);
-        if (c & 1) acc1 = fadd2(acc1, f2pack(pa, pb));
-        else acc0 = fadd2(acc0, f2pack(pa, pb));
-        pk[c] = pack_f16(pa, pb);
+      for (int c = 0; c < 16; ++c) {  // columns 4c..4c+3 of the page
+        const int cc = 4 * c;
+        const float x0 = __uint_as_float(cc < 32 ? lo[cc] : hi[cc - 32]);
+        const float x1 = __uint_as_float(cc < 32 ? lo[cc + 1] : hi[cc - 31]);
+        const float x2 = __uint_as_float(cc < 32 ? lo[cc + 2] : hi[cc - 30]);
+        const float x3 = __uint_as_float(cc < 32 ? lo[cc + 3] : hi[cc - 29]);
+        float y0, y1, y2, y3;
+        f2unpack(ffma2(f2pack(x0, x1), c2, nshift2), y0, y1);
+        f2unpack(ffma2(f2pack(x2, x3), c2, nshift2), y2, y3);
+        const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
+        acc0 = fadd2(acc0, f2pack(p0, p1));
+        acc1 = fadd2(acc1, f2pack(p2, p3));
+        pk[2 * c] = pack_f16(p0, p1);
+        pk[2 * c + 1] = pack_f16(p2, p3);
       }
       float a0, a1, b0, b1;
       f2unpack(acc0, a0, a1);
@@ -699,10 +765,10 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
           !mbar_wait(smem_u32(&s.pempty[k]), (u - 1) & 1, &s.abort_flag))
         ok = false;
       uint8_t* stg = s.pslot[k];
+      // Row r's 128 bytes (8-row groups 1024 B apart): 16-B chunk cc =
+      // f16 p of tokens 8cc..8cc+7 at position cc ^ (r % 8).
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
-        // K-major, 128-B swizzle: 8-row groups 1024 B apart, 16-B chunk cc
-        // of row r at position cc ^ (r % 8) within its 128-B row.
         *reinterpret_cast<uint4*>(stg + (r >> 3) * 1024 +
                                   box_chunk_offset(r & 7, cc)) =
             make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
@@ -712,6 +778,9 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
       const bool any = __any_sync(kFull, first && alpha != 1.f);
       if (lane == 0)
         reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
+      if (quad == 1)  // the page's 64 factors scale * 2^g (f16 pairs)
+        reinterpret_cast<uint32_t*>(stg + kSGOff)[lane] =
+            s.tsg[j & 3][(2 * g + q) * 32 + lane];
       fence_proxy_async_smem();
       named_bar_sync(bar_wg, 128);
       if ((warp & 3) == 0 && lane == 0 && ok && !s.abort_flag)
@@ -721,6 +790,9 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     };
     if (myp > 0) emit_page(pk0, 0);
     if (myp > 1) emit_page(pk1, 1);
+    // Done with tscale, tsg and tg of tile j % 4.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.scempty[j & 3]));
   }
 
   // Final statistics: l = sum of both warpgroups' partial sums.
@@ -734,7 +806,8 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
       p.LSE_part[part * rows + qrow] =
           lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
     }
-    s.fin[r] = lt > 0.f ? 1.f / lt : 0.f;
+    // O (units 2^(m_ref - g)) / l (units 2^m_ref) = O 2^-g / l
+    s.fin[r] = lt > 0.f ? exp2i(-g_cur) / lt : 0.f;
     fence_proxy_async_smem();
     named_bar_sync(2, 128);
     if (warp == 4 && lane == 0 && !s.abort_flag)
@@ -750,6 +823,80 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   if (!__all_sync(kFull, ok) && lane == 0) signal_abort(s, p, rank);
 }
 
+// ------------------------------------------------- O-CTA: tail page zeros -
+// The request's partial last page: rows at or past the length hold
+// undefined bytes (NaN in E4M3 would survive 0 * NaN in P V'), so warp 2
+// zeroes them in the ring stage before the MMA reads it.  The MMA thread,
+// which waits on the ring in order, hands the landed page over (tail_go).
+__device__ __forceinline__ void tail_warp(Smem& s, const TcParams& p,
+                                          const Work& w, uint32_t rank,
+                                          int lane) {
+  if (!w.tail) return;
+  const int m = w.npages - 1;
+  const int stage = m % kStages;
+  if (!mbar_wait(smem_u32(&s.tail_go), 0, &s.abort_flag)) {
+    if (lane == 0) signal_abort(s, p, rank);
+    return;
+  }
+  const int valid = (int)(w.L - (w.p0 + m) * kPage);  // 1..63
+  const int nz = kPage - valid;
+  // 4 boxes x nz rows x 8 chunks of 16 bytes; a row's 128 bytes are
+  // contiguous (the swizzle permutes chunks within the row).
+  for (int idx = lane; idx < 4 * nz * 8; idx += 32) {
+    const int bx = idx / (nz * 8), rem = idx % (nz * 8);
+    const int row = valid + rem / 8, ch = rem % 8;
+    *reinterpret_cast<uint4*>(s.ring[stage] + bx * kBoxBytes + (row >> 3) * 1024 +
+                              (row & 7) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
+}
+
+// ------------------------------------------------------- O-CTA: packers ---
+// Warps 8..11: thread = row r of every P message.  The row's 64 f16 p (8
+// chunks of 16 bytes in the 128-byte-swizzled row) are all loaded and
+// multiplied by the page's factors scale_t * 2^g (P' = p * scale_t * 2^g,
+// f16), then written back in place as the MMA's A operand: chunks 0-3 = Phi
+// (E4M3) of tokens 0..63, chunks 4-7 = Plo (E5M2).
+__device__ __forceinline__ void packer(Smem& s, const TcParams& p,
+                                       const Work& w, uint32_t rank, int warp,
+                                       int lane) {
+  const int r = (warp - 8) * 32 + lane;
+  bool ok = true;
+  for (int m = 0; m < w.npages; ++m) {
+    const int k = m % kNP;
+    if (!mbar_wait(smem_u32(&s.pfull[k]), (m / kNP) & 1, &s.abort_flag)) {
+      ok = false;
+      break;
+    }
+    uint8_t* row = s.pslot[k] + (r >> 3) * 1024;
+    const uint4* sg = reinterpret_cast<const uint4*>(s.pslot[k] + kSGOff);
+    uint4 x[8];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + box_chunk_offset(r & 7, cc));
+      const uint4 f = sg[cc];  // factors of tokens 8cc..8cc+7 (broadcast)
+      x[cc] = make_uint4(hmul2(v.x, f.x), hmul2(v.y, f.y), hmul2(v.z, f.z),
+                         hmul2(v.w, f.w));
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {  // tokens 16h..16h+15 = input chunks 2h, 2h+1
+      uint4 hi, lo;
+      split_p4(x[2 * h].x, x[2 * h].y, hi.x, lo.x);
+      split_p4(x[2 * h].z, x[2 * h].w, hi.y, lo.y);
+      split_p4(x[2 * h + 1].x, x[2 * h + 1].y, hi.z, lo.z);
+      split_p4(x[2 * h + 1].z, x[2 * h + 1].w, hi.w, lo.w);
+      *reinterpret_cast<uint4*>(row + box_chunk_offset(r & 7, h)) = hi;
+      *reinterpret_cast<uint4*>(row + box_chunk_offset(r & 7, 4 + h)) = lo;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.packed[k]));
+  }
+  if (!ok && lane == 0) signal_abort(s, p, rank);
+}
+
 // ---------------------------------------------------------- O-CTA: MMA ----
 __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
@@ -759,10 +906,11 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
   // Each P message lands by a bulk copy whose bytes complete on pfull[k];
   // this CTA arms the barrier (one arrival + the byte count) itself, so the
   // sender needs no cluster-scope arrive: the first use of each slot is armed
-  // at set-up, the next one as soon as a message has been received.
+  // at set-up, the next one once the packers have split the message
+  // (packed[k]).
   for (int m = 0; m < w.npages && ok; ++m) {
     const int k = m % kNP;
-    if (!mbar_wait(smem_u32(&s.pfull[k]), (m / kNP) & 1, &s.abort_flag)) {
+    if (!mbar_wait(smem_u32(&s.packed[k]), (m / kNP) & 1, &s.abort_flag)) {
       ok = false;
       break;
     }
@@ -771,8 +919,8 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
     const uint32_t* fl =
         reinterpret_cast<const uint32_t*>(s.pslot[k] + kFlagOff);
     if (fl[0] | fl[1] | fl[2] | fl[3]) {
-      // Rows raised their running max: let the correction warps rescale O
-      // once every earlier product has landed.
+      // Rows changed their units: let the correction warps rescale O once
+      // every earlier product has landed.
       s.ctl_slot = k;
       s.ctl_final = 0;
       mma_commit(smem_u32(&s.drain));
@@ -783,29 +931,39 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       }
       ++ev;
     }
-    const uint64_t a = sdesc_sw128(smem_u32(s.pslot[k]), 16, 1024);
-    for (int h = 0; h < 2; ++h) {
-      if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+    if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+      ok = false;
+      break;
+    }
+    if (w.tail && m == w.npages - 1) {
+      mbar_arrive(smem_u32(&s.tail_go));
+      if (!mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      // B = V (f16): MN-major, next 64 dims one chunk (8 KB) on, next 8
-      // tokens 1 KB on; each 16-token K step advances 2048 B (128 units).
-      const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage * kBoxesPerStage]),
-                                     kBoxBytes, 1024);
+    }
+    tc_fence_after();
+    // A = P (K-major, 128-B swizzle): +2 units per 32 tokens, Plo 64 bytes
+    // after Phi.  B = V (E4M3, MN-major): next 128 dims one box (8 KB) on,
+    // next 8 tokens 1 KB on; 32 tokens = 4 KB (256 units), 256 dims = 16 KB.
+    const uint64_t a = sdesc_sw128(smem_u32(s.pslot[k]), 16, 1024);
+    const uint64_t b = sdesc_sw128(smem_u32(s.ring[stage]), kBoxBytes, 1024);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
       const uint32_t d = tmem + 256u * h;
-      mma_ss(d, a + 0, b + 0, kIdescO, m > 0 ? 1u : 0u);
-      mma_ss(d, a + 2, b + 128, kIdescO, 1u);
-      mma_ss(d, a + 4, b + 256, kIdescO, 1u);
-      mma_ss(d, a + 6, b + 384, kIdescO, 1u);
-      mma_commit(smem_u32(&s.empty[stage]));
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+      const uint64_t bh = b + 1024u * h;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        mma_ss_f8(d, a + 2 * kk, bh + 256u * kk, kIdescOHi,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+        mma_ss_f8(d, a + 4 + 2 * kk, bh + 256u * kk, kIdescOLo, 1u);
       }
     }
-    if (!ok) break;
+    mma_commit(smem_u32(&s.empty[stage]));
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
     mma_commit_multicast(smem_u32(&s.pempty[k]), (uint16_t)1u);  // S-CTA
   }
   if (!ok) signal_abort(s, p, rank);
@@ -882,6 +1040,7 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
 // ------------------------------------------------------------- kernel ----
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_fp8_kernel(const __grid_constant__ CUtensorMap kv_map,
+                              const __grid_constant__ CUtensorMap rope_map,
                               const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -894,26 +1053,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     s.ctl_slot = 0;
     s.ctl_final = 0;
-    const uint32_t nconv = 4;  // converter warps
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&s.full[i]), nconv);
+      mbar_init(smem_u32(&s.full[i]), 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
-    for (int i = 0; i < kStages8; ++i) {
-      mbar_init(smem_u32(&s.full8[i]), 1);
-      mbar_init(smem_u32(&s.empty8[i]), nconv);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&s.scfull[i]), 1);
+      mbar_init(smem_u32(&s.scempty[i]), 8);  // the 8 softmax warps
+      mbar_init(smem_u32(&s.tsready[i]), 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s.tsready[i]), nconv);
     mbar_init(smem_u32(&s.sfull), 1);
-    mbar_init(smem_u32(&s.sempty), 8);   // the 8 softmax warps
+    mbar_init(smem_u32(&s.sempty), 8);
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
+      mbar_init(smem_u32(&s.packed[i]), 4);  // the 4 packer warps
       mbar_init(smem_u32(&s.pempty[i]), 1);
     }
     mbar_init(smem_u32(&s.drain), 2);
     mbar_init(smem_u32(&s.corr_done), 4);
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.qready), 8);
+    mbar_init(smem_u32(&s.tail_go), 1);
+    mbar_init(smem_u32(&s.tail_ready), 1);
     if (rank == 1 && w.npages > 0) {
       mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
       for (int k = 0; k < kNP && k < w.npages; ++k)
@@ -921,6 +1082,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
+    prefetch_tmap(&rope_map);
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -949,13 +1111,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp < 4 || warp >= 12) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
       if (warp == 0) {
-        producer_s(s, &kv_map, p, w, rank, lane);
+        producer_s(s, &kv_map, &rope_map, p, w, rank, lane);
       } else if (warp == 1) {
         if (lane == 0) mma_s(s, p, w, tmem, rank);
         __syncwarp();
-      } else if (warp < 4 || warp < 14) {
-        const int cw = warp < 4 ? warp - 2 : warp - 10;  // 0..3
-        converter<128>(s, p, w, rank, cw * 32 + lane, lane);
+      } else if (warp == 2) {
+        scale_warp(s, p, w, rank, lane);
       }
       teardown();
       return;
@@ -966,16 +1127,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
   if (w.npages > 0) {
-    if (warp == 0)
+    if (warp == 0) {
       producer_o(s, &kv_map, p, w, rank, lane);
-    else if (warp == 1) {
+    } else if (warp == 1) {
       if (lane == 0) mma_o(s, p, w, tmem, rank);
       __syncwarp();
-    } else if (warp < 4 || warp == 8 || warp == 9) {
-      const int cw = warp < 4 ? warp - 2 : warp - 6;  // 0..3
-      converter<128>(s, p, w, rank, cw * 32 + lane, lane);
-    } else if (warp < 8) {
+    } else if (warp == 2) {
+      tail_warp(s, p, w, rank, lane);
+    } else if (warp >= 4 && warp < 8) {
       correct_and_store(s, p, w, tmem, rank, warp, lane);
+    } else if (warp >= 8 && warp < 12) {
+      packer(s, p, w, rank, warp, lane);
     }
   } else if (warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0, LSE = -inf.
@@ -1022,15 +1184,17 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.status = a.status;
   const int64_t pairs = (int64_t)p.V * p.num_splits * p.G;
   if (pairs * 2 > 0x7fffffff) return fail(MLA_ERR_INVALID_ARG, "grid too large");
-  CUtensorMap map;
-  int rc = make_kv_tensor_map_fp8_plain(&map, a.kv, a.num_slots);
+  CUtensorMap map, rope_map;
+  int rc = make_kv_tensor_map(&map, a.kv, MLA_KV_FP8_E4M3, a.num_slots);
+  if (rc != MLA_OK) return rc;
+  rc = make_kv_tensor_map_fp8_rope(&rope_map, a.kv, a.num_slots);
   if (rc != MLA_OK) return rc;
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc fp8)");
   mla_partial_tc_fp8_kernel<<<(unsigned)(pairs * 2), kThreads, kSmemBytes,
-                              a.stream>>>(map, p);
+                              a.stream>>>(map, rope_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_fp8_kernel");
   return MLA_OK;

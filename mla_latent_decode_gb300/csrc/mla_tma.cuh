@@ -31,9 +31,10 @@ __host__ __device__ constexpr uint32_t box_chunk_offset(uint32_t r, uint32_t j) 
 int make_kv_tensor_map(CUtensorMap* map, const void* kv, mla_kv_dtype dtype,
                        int64_t num_slots);
 
-// Tensor map of an E4M3 pool in unswizzled boxes of 64 rows x 64 bytes (one
-// 64-dim chunk of a page, 4 KB), the staging format of the FP8 decode kernel.
-int make_kv_tensor_map_fp8_plain(CUtensorMap* map, const void* kv,
-                                 int64_t num_slots);
+// Tensor map of an E4M3 pool in boxes of 64 rows x 64 bytes with the 64-byte
+// swizzle (4 KB): the RoPE key columns 512..575 of one page, the K-major
+// operand layout the FP8 decode kernel's tensor cores read for those dims.
+int make_kv_tensor_map_fp8_rope(CUtensorMap* map, const void* kv,
+                                int64_t num_slots);
 
 }  // namespace mla

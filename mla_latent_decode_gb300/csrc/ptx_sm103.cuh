@@ -234,6 +234,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
+// The same descriptor for the 64-byte swizzle (layout type 4): K-major rows
+// of 64 bytes, 8-row groups `sbo` = 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo,
+                                               uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with BF16 A/B and an FP32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N,
                                                       bool a_mn_major,
@@ -259,6 +271,26 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b,
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// kind::f8f6f4 forms (8-bit A and B, fp32 accumulator; the formats of A and
+// B are fields of the instruction descriptor).  A from TMEM holds four
+// 8-bit elements per 32-bit column, K = 32 per instruction.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d, uint32_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }

@@ -219,6 +219,71 @@ def test_tc_fp8_decode_matches_oracle(name, wl, S):
     print(name, m)
 
 
+def _rescale_tokens(batch, fn):
+    """kv_scale[slot of token t of request b] *= fn(b, t) (in place, B x L)."""
+    for b, L in enumerate(batch.wl.seq_lens):
+        t = torch.arange(L, device="cuda")
+        slots = batch.req_to_token[b, :L].long()
+        batch.kv_scale[slots] *= fn(b, t).to(torch.float32)
+
+
+FP8_SCALE_CASES = [
+    # (name, kv scale factor per token, query factor, output factor).
+    # Scales growing along the context: the running max |scale| crosses
+    # powers of two inside a split (O and l change units mid-stream).
+    ("growing", lambda b, t: torch.pow(2.0, (t // 300).float() - 9.0), 1.0, 1.0),
+    # neighbouring pages 2^18 apart: most of a tile's P' sits far below its max
+    ("alternating", lambda b, t: torch.pow(2.0, -18.0 * ((t // 64) % 2).float()),
+     1.0, 1.0),
+    # scales far from 1 with the query scaled the other way: the scores (and
+    # the LSE) are unchanged and O scales exactly by the factor
+    ("tiny", lambda b, t: torch.full_like(t, 2.0 ** -40, dtype=torch.float32),
+     2.0 ** 40, 2.0 ** -40),
+    ("large", lambda b, t: torch.full_like(t, 2.0 ** 12, dtype=torch.float32),
+     2.0 ** -12, 2.0 ** 12),
+]
+
+
+@pytest.mark.parametrize("name,fn,qf,of", FP8_SCALE_CASES,
+                         ids=[c[0] for c in FP8_SCALE_CASES])
+def test_tc_fp8_scale_magnitudes_match_oracle(name, fn, qf, of):
+    wl = synth.Workload("sc8", 2, 5, 96, [2500, 700], kv_dtype="fp8_e4m3", q_scale=2.0)
+    batch = synth.make_batch(wl, seed=31, device="cuda")
+    _rescale_tokens(batch, fn)
+    batch.q_nope.mul_(qf)
+    batch.q_rope.mul_(qf)
+    hb = synth.host_bits(batch)
+    st = _status()
+    out, lse, _ = mla.decode(batch, num_splits=2, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O_ref, l_ref = oracle_rows(batch, hb, None)
+    m = check_close(f64(out).reshape(-1, 512) / of, f64(lse).reshape(-1), O_ref / of,
+                    l_ref, "fp8_e4m3", f"fp8 scales {name}")
+    print(name, m)
+
+
+def test_tc_fp8_query_dynamic_range_matches_oracle():
+    """Query rows with one element 64 times the rest, and rows scaled by
+    2^-60: the row scale 2^e of the FP8 path keeps every element at least
+    2^-9 of the row's largest exact."""
+    wl = synth.Workload("qd8", 2, 5, 96, [900, 300], kv_dtype="fp8_e4m3")
+    batch = synth.make_batch(wl, seed=32, device="cuda")
+    batch.q_nope[:, :, ::3, 7] *= 64.0
+    batch.q_rope[:, :, 1::3, 5] *= 64.0
+    batch.q_nope[:, :, 2::7, :] *= 2.0 ** -60
+    batch.q_rope[:, :, 2::7, :] *= 2.0 ** -60
+    hb = synth.host_bits(batch)
+    st = _status()
+    out, lse, _ = mla.decode(batch, num_splits=1, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O_ref, l_ref = oracle_rows(batch, hb, None)
+    m = check_close(f64(out).reshape(-1, 512), f64(lse).reshape(-1), O_ref, l_ref,
+                    "fp8_e4m3", "fp8 q dynamic range")
+    print(m)
+
+
 def test_tc_fp8_shards_match_unsharded_oracle():
     sh = synth.Workload("dcp8", 3, 5, 96, [517, 64, 9], num_shards=8,
                         kv_dtype="fp8_e4m3")
