@@ -48,7 +48,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 512;        // 16 warps = 4 warpgroups
+constexpr int kThreads = 640;        // 20 warps = 5 warpgroups
 constexpr int kStages = 4;           // operand ring slots
 constexpr int kStageBytes = 32768;   // S: 4 pages x 128 dims; O: one page of V
 constexpr int kBlocksPerTile = 5;    // S tile: 4 blocks of 128 dims + RoPE
@@ -67,14 +67,15 @@ constexpr uint32_t kQLoCol = 128;   // Qlo columns (Qhi at 0)
 constexpr uint32_t kSCol0 = 256;    // S buffer columns
 constexpr float kTau = 8.f;         // lazy-rescale threshold (log2 units)
 constexpr uint32_t kFull = 0xffffffffu;
-// Register split of the S-CTA (setmaxnreg): 512 threads launch with 128
-// registers each (65,536); the producer/MMA/scale warpgroups (warps 0-3 and
-// 12-15) give registers away so the two softmax warpgroups can hold a
-// 128 x 256 fp32 score tile.  The split is one-way.
-constexpr int kRegsLaunch = 128;
+constexpr int kPartials = 8;         // 32-token groups of an S tile
+// Register split of the S-CTA (setmaxnreg): 640 threads launch with 96
+// registers each (61,440 of 65,536); the producer/MMA/scale warpgroup (warps
+// 0-3) gives registers away so the four softmax warpgroups can hold their
+// scores.  The split is one-way.
+constexpr int kRegsLaunch = 96;
 constexpr int kRegsControl = 40;
-constexpr int kRegsSoftmax = 216;
-static_assert(256 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+constexpr int kRegsSoftmax = 104;
+static_assert(128 * kRegsControl + 512 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 
 // kind::f8f6f4 instruction descriptor: fp32 accumulator, A format a_fmt
@@ -98,7 +99,7 @@ struct __align__(1024) Smem {
   uint32_t tsg[4][kTilePages * kPage / 2];  // S-CTA: f16 pairs scale * 2^g
   int tg[4];                // S-CTA: scale exponent g of tile j % 4
   float fin[kRows];
-  float xch[2][kRows];      // S-CTA: per-warpgroup row values
+  float xch[kPartials][kRows];  // S-CTA: row values per 32-token group
   uint64_t full[kStages];   // TMA -> MMA (bytes)
   uint64_t empty[kStages];  // MMA -> producer
   uint64_t scfull[4];       // S-CTA: scale bulk copies landed
@@ -531,57 +532,76 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
 }
 
 // ------------------------------------------------------ S-CTA: softmax ----
-// Warps 4..11: warpgroup g = 0 (warps 4-7) owns pages 0,1 of each S tile,
-// g = 1 (warps 8-11) pages 2,3.  Thread = query row r (TMEM lane).
+// Warps 4..19: four warpgroups; warpgroup g (warps 4g + 4 .. 4g + 7) owns
+// page g of each S tile, warp quad (warp % 4) owns TMEM lanes (query rows)
+// 32 quad .. 32 quad + 31.  In the tile loop each thread owns rows
+// A = 32 quad + (lane % 16) and B = A + 16 over half the page (lane / 16:
+// tokens 0..31 or 32..63), read with 16x32bx2 loads, so each token scale it
+// loads serves two rows.  Q is prepared with thread = row r: warpgroups 0
+// and 1 split the c_kv dims, warpgroup 2 takes the RoPE dims.
+__device__ __forceinline__ int64_t visible_count(const TcParams& p,
+                                                 const Work& w, int r) {
+  // tokens query row r (of the pair's rows) may see; 0 for padding rows
+  if (r >= w.nrows) return 0;
+  const int i = (w.r_base + r) / p.H;
+  int64_t n = p.kv_limit ? (int64_t)p.kv_limit[(int64_t)w.v * p.q_len + i]
+                         : w.L - p.q_len + 1 + i;
+  return n > w.L ? w.L : (n < 0 ? 0 : n);
+}
+
+// Row scale exponent e: the row's largest |q| times 2^-e lies in [128, 256).
+__device__ __forceinline__ int row_exponent(float amax) {
+  return amax > 0.f ? min(126, max(-126, exponent_of(amax) - 8)) : 0;
+}
+
 __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
                                         const Work& w, uint32_t tmem,
                                         uint32_t rank, int warp, int lane) {
-  const int g = (warp - 4) >> 2;
+  const int g = (warp - 4) >> 2;        // warpgroup = page of the S tile
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   const bool row_ok = r < w.nrows;
-  const int rr = w.r_base + r;
-  const int i = row_ok ? rr / p.H : 0;
-  int64_t n = 0;
-  if (row_ok) {
-    n = p.kv_limit ? (int64_t)p.kv_limit[(int64_t)w.v * p.q_len + i]
-                   : w.L - p.q_len + 1 + i;
-    n = n > w.L ? w.L : (n < 0 ? 0 : n);
-  }
-  const int64_t qrow = (int64_t)w.b * p.q_len * p.H + rr;
+  const int64_t qrow = (int64_t)w.b * p.q_len * p.H + w.r_base + r;
+  const int hp = lane >> 4;             // half of the page: tokens 32 hp ..
+  const int part = 2 * g + hp;          // 32-token group of the S tile
+  const int rA = quad * 32 + (lane & 15), rB = rA + 16;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
 
-  // Row scale 2^e: the row's largest |q| (both warpgroups' parts) lands in
-  // [128, 256) after multiplying by 2^-e.
+  // Row scale 2^e from the warpgroups' partial |q| maxima.
   float amax = 0.f;
-  if (g == 0) {
+  if (g < 2) {
 #pragma unroll 8
-    for (int k = 0; k < 64; ++k)
-      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_nope[qrow * 64 + k] : zero4));
-  } else {
+    for (int k = 0; k < 32; ++k)
+      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_nope[qrow * 64 + 32 * g + k] : zero4));
+  } else if (g == 2) {
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_rope[qrow * 8 + k] : zero4));
   }
   s.xch[g][r] = amax;
-  named_bar_sync(1, 256);
-  amax = fmaxf(s.xch[0][r], s.xch[1][r]);
-  named_bar_sync(1, 256);
-  const int e = amax > 0.f ? min(126, max(-126, exponent_of(amax) - 8)) : 0;
-  const float inv = exp2i(-e);
-  const float crow = p.scale_log2 * exp2i(e);
+  named_bar_sync(1, 512);
+  auto qmax = [&](int row) {
+    return fmaxf(max3(s.xch[0][row], s.xch[1][row], s.xch[2][row]), s.xch[3][row]);
+  };
+  const float inv = exp2i(-row_exponent(qmax(r)));
+  // score factor sm_scale * log2(e) * 2^e of rows A and B
+  const float crowA = p.scale_log2 * exp2i(row_exponent(qmax(rA)));
+  const float crowB = p.scale_log2 * exp2i(row_exponent(qmax(rB)));
+  named_bar_sync(1, 512);
+  const int64_t nA = visible_count(p, w, rA), nB = visible_count(p, w, rB);
 
   // Qhi / Qlo: c_kv dims -> TMEM columns [0, 128) and [128, 256) (column c
-  // holds elements 4c..4c+3), RoPE dims -> shared memory, K-major rows of 64
-  // bytes with the 64-byte swizzle.
-  if (g == 0) {
+  // holds elements 4c..4c+3; warpgroup g < 2 writes dims 256g .. 256g + 255,
+  // 64 dims = 16 columns per step), RoPE dims -> shared memory, K-major rows
+  // of 64 bytes with the 64-byte swizzle.
+  if (g < 2) {
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {  // 128 dims = 32 columns per step
-      uint32_t vh[32], vl[32];
-      const uint4* src = p.q_nope + qrow * 64 + c * 16;
+    for (int c = 0; c < 4; ++c) {
+      uint32_t vh[16], vl[16];
+      const uint4* src = p.q_nope + qrow * 64 + 32 * g + 8 * c;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < 8; ++k) {
         uint2 h, l;
         split_q8(row_ok ? src[k] : zero4, inv, h, l);
         vh[2 * k] = h.x;
@@ -589,11 +609,11 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
         vl[2 * k] = l.x;
         vl[2 * k + 1] = l.y;
       }
-      tmem_st32(tmem + lane_base + 32u * c, vh);
-      tmem_st32(tmem + lane_base + kQLoCol + 32u * c, vl);
+      tmem_st16(tmem + lane_base + 64u * g + 16u * c, vh);
+      tmem_st16(tmem + lane_base + kQLoCol + 64u * g + 16u * c, vl);
     }
     tmem_wait_st();
-  } else {
+  } else if (g == 2) {
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk cc = elements 16cc..16cc+15
       uint2 h0, l0, h1, l1;
@@ -610,204 +630,206 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&s.qready));
 
-  // Running state: m_ref (log2 units, lazy), l in units of 2^m_ref, and the
-  // split's scale exponent g_cur: O accumulates p * scale * 2^g_cur, so it
-  // is kept in units of 2^(m_ref - g_cur).
-  float m_ref = -INFINITY, l = 0.f;
+  // Running state per row (A, B): m_ref (log2 units, lazy), l in units of
+  // 2^m_ref over this thread's tokens; g_cur is the split's scale exponent:
+  // O accumulates p * scale * 2^g_cur, so it is kept in units of
+  // 2^(m_ref - g_cur).
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
   int g_cur = 0;
   bool ok = true;
   const uint32_t peer_pfull0 = mapa(smem_u32(&s.pfull[0]), 1);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   const uint32_t bar_wg = 2 + g;  // named barrier of this warpgroup
+  const uint32_t tA = tmem + lane_base + kSCol0 + 64u * g;
+  const uint32_t tB = tA + (16u << 16);
+  auto all_parts_max = [&](int row) {
+    return fmaxf(fmaxf(max3(s.xch[0][row], s.xch[1][row], s.xch[2][row]),
+                       max3(s.xch[3][row], s.xch[4][row], s.xch[5][row])),
+                 fmaxf(s.xch[6][row], s.xch[7][row]));
+  };
   for (int j = 0; j < ntiles; ++j) {
-    const int np = tile_pages(w, j);
-    const int myp = min(2, max(0, np - 2 * g));  // pages this warpgroup owns
-    uint32_t s0[32], s1[32], s2[32], s3[32];
+    const bool has = g < tile_pages(w, j);  // this warpgroup's page exists
+    uint32_t a[32], b[32];  // rows A and B, tokens 32 hp .. 32 hp + 31
     if (ok && !mbar_wait(smem_u32(&s.sfull), j & 1, &s.abort_flag)) ok = false;
     tc_fence_after();
-    if (__all_sync(kFull, ok) && myp > 0) {
-      const uint32_t col = tmem + lane_base + kSCol0 + 128u * g;
-      tmem_ld32(col, s0);
-      tmem_ld32(col + 32, s1);
-      if (myp > 1) {
-        tmem_ld32(col + 64, s2);
-        tmem_ld32(col + 96, s3);
-      }
+    if (__all_sync(kFull, ok) && has) {
+      tmem_ld16x2_32<32>(tA, a);
+      tmem_ld16x2_32<32>(tB, b);
       tmem_wait_ld();
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.sempty));
 
-    // Token scales of this warpgroup's 128 columns: raw -> raw * scale_t.
+    // Token scales: raw -> raw * scale_t for both rows (one broadcast load
+    // of four scales serves eight scores).
     if (ok && !mbar_wait(smem_u32(&s.tsready[j & 3]), (j >> 2) & 1,
                          &s.abort_flag))
       ok = false;
-    const float* tsc = &s.tscale[j & 3][128 * g];
-    auto apply_scale = [&](uint32_t (&a)[32], int c0) {
+    const float* tsc = &s.tscale[j & 3][kPage * g + 32 * hp];
+    if (has) {
 #pragma unroll
       for (int c = 0; c < 32; c += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(tsc + c0 + c);
-        float x0, x1, x2, x3;
-        f2unpack(fmul2(f2pack(__uint_as_float(a[c]), __uint_as_float(a[c + 1])),
-                       f2pack(f.x, f.y)), x0, x1);
-        f2unpack(fmul2(f2pack(__uint_as_float(a[c + 2]), __uint_as_float(a[c + 3])),
-                       f2pack(f.z, f.w)), x2, x3);
-        a[c] = __float_as_uint(x0);
-        a[c + 1] = __float_as_uint(x1);
-        a[c + 2] = __float_as_uint(x2);
-        a[c + 3] = __float_as_uint(x3);
+        const float4 f = *reinterpret_cast<const float4*>(tsc + c);
+        const uint64_t f01 = f2pack(f.x, f.y), f23 = f2pack(f.z, f.w);
+        float v0, v1, v2, v3;
+        f2unpack(fmul2(f2pack(__uint_as_float(a[c]), __uint_as_float(a[c + 1])), f01), v0, v1);
+        f2unpack(fmul2(f2pack(__uint_as_float(a[c + 2]), __uint_as_float(a[c + 3])), f23), v2, v3);
+        a[c] = __float_as_uint(v0);
+        a[c + 1] = __float_as_uint(v1);
+        a[c + 2] = __float_as_uint(v2);
+        a[c + 3] = __float_as_uint(v3);
+        f2unpack(fmul2(f2pack(__uint_as_float(b[c]), __uint_as_float(b[c + 1])), f01), v0, v1);
+        f2unpack(fmul2(f2pack(__uint_as_float(b[c + 2]), __uint_as_float(b[c + 3])), f23), v2, v3);
+        b[c] = __float_as_uint(v0);
+        b[c + 1] = __float_as_uint(v1);
+        b[c + 2] = __float_as_uint(v2);
+        b[c + 3] = __float_as_uint(v3);
       }
-    };
-    if (myp > 0) {
-      apply_scale(s0, 0);
-      apply_scale(s1, 32);
-    }
-    if (myp > 1) {
-      apply_scale(s2, 64);
-      apply_scale(s3, 96);
     }
 
-    // Visible columns of this row among this warpgroup's 128 columns.
-    const int64_t t0 = (w.p0 + (int64_t)j * kTilePages + 2 * g) * kPage;
-    const int64_t nv = n - t0;
-    const int nvis = nv <= 0 ? 0 : (nv >= 64 * myp ? 64 * myp : (int)nv);
-    // Columns this row may not see become -inf (a select: garbage or NaN in
-    // a masked column never propagates).
-    if (!__all_sync(kFull, nvis == 128)) {
-      auto mask = [&](uint32_t (&a)[32], int c0) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          a[c] = c0 + c < nvis ? a[c] : __float_as_uint(-INFINITY);
-      };
-      mask(s0, 0);
-      mask(s1, 32);
-      mask(s2, 64);
-      mask(s3, 96);
-    }
-    auto xs = [&](int c) -> float {
-      return __uint_as_float(c < 32 ? s0[c] : c < 64 ? s1[c - 32]
-                                    : c < 96 ? s2[c - 64] : s3[c - 96]);
+    // Visible tokens of rows A, B among this thread's 32 (0 for a page the
+    // tile lacks); the others become -inf (a select: garbage or NaN in a
+    // masked column never propagates).  Only tiles at the end of the split
+    // need it.
+    const int64_t t0 = (w.p0 + (int64_t)j * kTilePages + g) * kPage + 32 * hp;
+    auto clampv = [&](int64_t nrow) -> int {
+      const int64_t nv = nrow - t0;
+      return !has || nv <= 0 ? 0 : (nv >= 32 ? 32 : (int)nv);
     };
-    // Row maximum of raw * scale; the row factor crow is positive, so the
-    // maximum of the scores is crow times it (rounding is monotone).
-    float mx[16];
+    const int nvA = clampv(nA), nvB = clampv(nB);
+    if (!__all_sync(kFull, nvA == 32 && nvB == 32)) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      mx[c] = fmaxf(max3(xs(c), xs(c + 16), xs(c + 32)),
-                    max3(max3(xs(c + 48), xs(c + 64), xs(c + 80)), xs(c + 96),
-                         xs(c + 112)));
-    const float m5a = max3(mx[0], mx[1], mx[2]), m5b = max3(mx[3], mx[4], mx[5]);
-    const float m5c = max3(mx[6], mx[7], mx[8]), m5d = max3(mx[9], mx[10], mx[11]);
-    const float m5e = max3(mx[12], mx[13], mx[14]);
-    const float mt_own =
-        max3(max3(m5a, m5b, m5c), max3(m5d, m5e, mx[15]), -INFINITY) * crow;
-    s.xch[g][r] = mt_own;
-    named_bar_sync(1, 256);
-    const float mt = fmaxf(mt_own, s.xch[g ^ 1][r]);
-    named_bar_sync(1, 256);  // both read before the next tile overwrites
+      for (int c = 0; c < 32; ++c) {
+        a[c] = c < nvA ? a[c] : __float_as_uint(-INFINITY);
+        b[c] = c < nvB ? b[c] : __float_as_uint(-INFINITY);
+      }
+    }
+    // Row maxima of raw * scale over this thread's tokens, then over the
+    // tile's eight 32-token groups through shared memory.  The row factor is
+    // positive, so the maximum score is its multiple.
+    auto max32 = [&](const uint32_t (&x)[32]) -> float {
+      float m4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        m4[k] = max3(max3(__uint_as_float(x[8 * k]), __uint_as_float(x[8 * k + 1]),
+                          __uint_as_float(x[8 * k + 2])),
+                     max3(__uint_as_float(x[8 * k + 3]), __uint_as_float(x[8 * k + 4]),
+                          __uint_as_float(x[8 * k + 5])),
+                     fmaxf(__uint_as_float(x[8 * k + 6]), __uint_as_float(x[8 * k + 7])));
+      return fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+    };
+    s.xch[part][rA] = max32(a) * crowA;
+    s.xch[part][rB] = max32(b) * crowB;
+    named_bar_sync(1, 512);
+    const float mtA = all_parts_max(rA), mtB = all_parts_max(rB);
+    named_bar_sync(1, 512);  // all read before the next tile overwrites
 
     // g of this tile (from the scale warp: max |scale| so far times 2^g in
-    // [0.5, 1)).  alpha is O's factor, 2^((m_ref - m_new) + (g_new - g)).
+    // [0.5, 1)).  O's factor is 2^((m_ref - m_new) + (g_new - g)); l's is
+    // 2^(m_ref - m_new).
     const int g_new = s.tg[j & 3];
-    float m_new = m_ref;
-    if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kTau)) m_new = mt;
-    float alpha = 1.f;
-    if (m_ref > -INFINITY && (m_new != m_ref || g_new != g_cur)) {
-      if (m_new != m_ref) l *= ex2(m_ref - m_new);
-      alpha = ex2((m_ref - m_new) + (float)(g_new - g_cur));
-    }
-    m_ref = m_new;
+    auto update = [&](float mt, float& m, float& lsum) -> float {
+      float m_new = m;
+      if (mt > -INFINITY && (m == -INFINITY || mt > m + kTau)) m_new = mt;
+      float alpha = 1.f;
+      if (m > -INFINITY && (m_new != m || g_new != g_cur)) {
+        if (m_new != m) lsum *= ex2(m - m_new);
+        alpha = ex2((m - m_new) + (float)(g_new - g_cur));
+      }
+      m = m_new;
+      return alpha;
+    };
+    const float alphaA = update(mtA, mA, lA), alphaB = update(mtB, mB, lB);
     g_cur = g_new;
-    // A row with nothing visible yet keeps m_ref = -inf: shift by 0 instead
-    // so every p is ex2(-inf) = 0, not NaN.
-    const float shift = m_ref == -INFINITY ? 0.f : m_ref;
 
-    // p = 2^(raw*scale*crow - m_ref) <= 2^tau, l += p, p as packed f16 pairs
-    // (32 words per page); the packers multiply by scale * 2^g.
-    uint32_t pk0[32], pk1[32];
-    const uint64_t c2 = f2pack(crow, crow), nshift2 = f2pack(-shift, -shift);
-    auto make_page = [&](const uint32_t (&lo)[32], const uint32_t (&hi)[32],
-                         uint32_t (&pk)[32]) {
+    // Ship page g in message slot g (four slots, four pages per tile), use
+    // j.  p = 2^(raw*scale*crow - m_ref) <= 2^tau (a row with nothing visible
+    // yet shifts by 0: p = ex2(-inf) = 0), l += p; rows A and B of p go to
+    // the slot as f16 pairs, 16 bytes at a time (the packers multiply by
+    // scale * 2^g), with the tile's rescale (page 0 only), the warp's flag
+    // and, from warp quad 1, the page's factors.
+    const bool any = __any_sync(kFull, alphaA != 1.f || alphaB != 1.f);
+    uint8_t* stg = s.pslot[g];
+    auto make_row = [&](const uint32_t (&x)[32], float crow, float m,
+                        float& lsum, int row) {
+      const float shift = m == -INFINITY ? 0.f : m;
+      const uint64_t c2 = f2pack(crow, crow), nshift2 = f2pack(-shift, -shift);
       uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+      uint8_t* dst = stg + (row >> 3) * 1024;
+      uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {  // columns 4c..4c+3 of the page
-        const int cc = 4 * c;
-        const float x0 = __uint_as_float(cc < 32 ? lo[cc] : hi[cc - 32]);
-        const float x1 = __uint_as_float(cc < 32 ? lo[cc + 1] : hi[cc - 31]);
-        const float x2 = __uint_as_float(cc < 32 ? lo[cc + 2] : hi[cc - 30]);
-        const float x3 = __uint_as_float(cc < 32 ? lo[cc + 3] : hi[cc - 29]);
+      for (int c = 0; c < 8; ++c) {  // tokens 32 hp + 4c .. + 3
         float y0, y1, y2, y3;
-        f2unpack(ffma2(f2pack(x0, x1), c2, nshift2), y0, y1);
-        f2unpack(ffma2(f2pack(x2, x3), c2, nshift2), y2, y3);
+        f2unpack(ffma2(f2pack(__uint_as_float(x[4 * c]), __uint_as_float(x[4 * c + 1])),
+                       c2, nshift2), y0, y1);
+        f2unpack(ffma2(f2pack(__uint_as_float(x[4 * c + 2]), __uint_as_float(x[4 * c + 3])),
+                       c2, nshift2), y2, y3);
         const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
         acc0 = fadd2(acc0, f2pack(p0, p1));
         acc1 = fadd2(acc1, f2pack(p2, p3));
-        pk[2 * c] = pack_f16(p0, p1);
-        pk[2 * c + 1] = pack_f16(p2, p3);
+        if (c & 1) {
+          // 16-B chunk 4 hp + c / 2 = tokens 32 hp + 8 (c / 2) .. + 7, at
+          // position chunk ^ (row % 8) of the row's 128 bytes
+          *reinterpret_cast<uint4*>(dst + box_chunk_offset(row & 7, 4 * hp + (c >> 1))) =
+              make_uint4(w0, w1, pack_f16(p0, p1), pack_f16(p2, p3));
+        } else {
+          w0 = pack_f16(p0, p1);
+          w1 = pack_f16(p2, p3);
+        }
       }
-      float a0, a1, b0, b1;
-      f2unpack(acc0, a0, a1);
-      f2unpack(acc1, b0, b1);
-      l += (a0 + a1) + (b0 + b1);
+      float u0, u1, v0, v1;
+      f2unpack(acc0, u0, u1);
+      f2unpack(acc1, v0, v1);
+      lsum += (u0 + u1) + (v0 + v1);
     };
-    if (myp > 0) make_page(s0, s1, pk0);
-    if (myp > 1) make_page(s2, s3, pk1);
-
-    // Ship one page: wait for its slot, store, hand it to the peer.  Slot
-    // k = (2g + q) belongs to this warpgroup and page position alone (four
-    // slots, four pages per tile), so its uses are sequential here.
-    auto emit_page = [&](const uint32_t (&pk)[32], int q) {
-      const int msg = j * kTilePages + 2 * g + q;  // page index in the split
-      const int k = msg % kNP;
-      const int u = msg / kNP;  // use index of slot k
-      if (u > 0 && ok &&
-          !mbar_wait(smem_u32(&s.pempty[k]), (u - 1) & 1, &s.abort_flag))
+    if (has) {
+      if (j > 0 && ok &&
+          !mbar_wait(smem_u32(&s.pempty[g]), (j - 1) & 1, &s.abort_flag))
         ok = false;
-      uint8_t* stg = s.pslot[k];
-      // Row r's 128 bytes (8-row groups 1024 B apart): 16-B chunk cc =
-      // f16 p of tokens 8cc..8cc+7 at position cc ^ (r % 8).
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(stg + (r >> 3) * 1024 +
-                                  box_chunk_offset(r & 7, cc)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      // The tile's rescale travels with its first page only.
-      const bool first = (g == 0 && q == 0);
-      reinterpret_cast<float*>(stg + kAlphaOff)[r] = first ? alpha : 1.f;
-      const bool any = __any_sync(kFull, first && alpha != 1.f);
+      make_row(a, crowA, mA, lA, rA);
+      make_row(b, crowB, mB, lB, rB);
+      if (hp == 0) {
+        reinterpret_cast<float*>(stg + kAlphaOff)[rA] = g == 0 ? alphaA : 1.f;
+        reinterpret_cast<float*>(stg + kAlphaOff)[rB] = g == 0 ? alphaB : 1.f;
+      }
       if (lane == 0)
-        reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = any ? 1u : 0u;
+        reinterpret_cast<uint32_t*>(stg + kFlagOff)[quad] = g == 0 && any ? 1u : 0u;
       if (quad == 1)  // the page's 64 factors scale * 2^g (f16 pairs)
-        reinterpret_cast<uint32_t*>(stg + kSGOff)[lane] =
-            s.tsg[j & 3][(2 * g + q) * 32 + lane];
+        reinterpret_cast<uint32_t*>(stg + kSGOff)[lane] = s.tsg[j & 3][g * 32 + lane];
       fence_proxy_async_smem();
-      named_bar_sync(bar_wg, 128);
-      if ((warp & 3) == 0 && lane == 0 && ok && !s.abort_flag)
-        // The peer armed pfull[k] with the byte count itself.
-        bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
-                          peer_pfull0 + 8u * k);
-    };
-    if (myp > 0) emit_page(pk0, 0);
-    if (myp > 1) emit_page(pk1, 1);
+    }
+    named_bar_sync(bar_wg, 128);
+    if (quad == 0 && lane == 0 && has && ok && !s.abort_flag)
+      // The peer armed pfull[g] with the byte count itself.
+      bulk_copy_to_peer(mapa(smem_u32(stg), 1), smem_u32(stg), kPMsgBytes,
+                        peer_pfull0 + 8u * g);
     // Done with tscale, tsg and tg of tile j % 4.
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.scempty[j & 3]));
   }
 
-  // Final statistics: l = sum of both warpgroups' partial sums.
-  s.xch[g][r] = l;
-  named_bar_sync(1, 256);
+  // Final statistics: l of a row = the sum over the eight token groups.
+  s.xch[part][rA] = lA;
+  s.xch[part][rB] = lB;
+  named_bar_sync(1, 512);
   if (g == 0) {
-    const float lt = l + s.xch[1][r];
-    if (row_ok) {
+    if (hp == 0) {
       const int64_t rows = (int64_t)p.B * p.q_len * p.H;
-      const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-      p.LSE_part[part * rows + qrow] =
-          lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      const int64_t prt = (int64_t)w.split * (p.V / p.B) + w.shard;
+      auto finish = [&](int row, float m) {
+        float lt = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPartials; ++k) lt += s.xch[k][row];
+        if (row < w.nrows)
+          p.LSE_part[prt * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + row] =
+              lt > 0.f ? (m + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        // O (units 2^(m_ref - g)) / l (units 2^m_ref) = O 2^-g / l
+        s.fin[row] = lt > 0.f ? exp2i(-g_cur) / lt : 0.f;
+      };
+      finish(rA, mA);
+      finish(rB, mB);
     }
-    // O (units 2^(m_ref - g)) / l (units 2^m_ref) = O 2^-g / l
-    s.fin[r] = lt > 0.f ? exp2i(-g_cur) / lt : 0.f;
     fence_proxy_async_smem();
     named_bar_sync(2, 128);
     if (warp == 4 && lane == 0 && !s.abort_flag)
@@ -1059,11 +1081,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s.scfull[i]), 1);
-      mbar_init(smem_u32(&s.scempty[i]), 8);  // the 8 softmax warps
+      mbar_init(smem_u32(&s.scempty[i]), 16);  // the 16 softmax warps
       mbar_init(smem_u32(&s.tsready[i]), 1);
     }
     mbar_init(smem_u32(&s.sfull), 1);
-    mbar_init(smem_u32(&s.sempty), 8);
+    mbar_init(smem_u32(&s.sempty), 16);
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&s.pfull[i]), 1);
       mbar_init(smem_u32(&s.packed[i]), 4);  // the 4 packer warps
@@ -1072,7 +1094,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.drain), 2);
     mbar_init(smem_u32(&s.corr_done), 4);
     mbar_init(smem_u32(&s.fin_full), 1);
-    mbar_init(smem_u32(&s.qready), 8);
+    mbar_init(smem_u32(&s.qready), 16);
     mbar_init(smem_u32(&s.tail_go), 1);
     mbar_init(smem_u32(&s.tail_ready), 1);
     if (rank == 1 && w.npages > 0) {
@@ -1108,7 +1130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   if (w.npages > 0 && rank == 0) {
-    if (warp < 4 || warp >= 12) {
+    if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
       if (warp == 0) {
         producer_s(s, &kv_map, &rope_map, p, w, rank, lane);
