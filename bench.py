@@ -60,6 +60,9 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time mla_decode (partial + combine in one launch) "
+                         "instead of mla_decode_partial + mla_lse_combine")
     ap.add_argument("--sweep", action="store_true",
                     help="wave-quantisation sweep: B in 1..24 x context "
                          "{100k, 400k}, the pages' split rule vs the planner "
@@ -396,8 +399,20 @@ def main():
     out = torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((wl.B, wl.q_len, wl.H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    counters = mla.fused_counters(wl.B, wl.q_len, wl.H, dev)
 
     def step(ev=None):
+        if args.fused:
+            if ev is not None:
+                ev[0].record(stream)
+            mla.decode_fused(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+                             batch.req_to_token, batch.seq_lens, batch.kv_limit,
+                             S, wl.sm_scale, wl.num_shards, O_part, LSE_part,
+                             counters, out, lse, status, split_pages=split_pages)
+            if ev is not None:
+                ev[1].record(stream)
+                ev[2].record(stream)
+            return
         if ev is not None:
             ev[0].record(stream)
         mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
@@ -489,10 +504,16 @@ def main():
             dr.copy_(hr, non_blocking=True)
             dt_.copy_(ht, non_blocking=True)
             ds.copy_(hs, non_blocking=True)
-            mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
-                               batch.kv_limit, S, wl.sm_scale, wl.num_shards,
-                               O_part, LSE_part, status, split_pages=split_pages)
-            mla.lse_combine(O_part, LSE_part, out, lse)
+            if args.fused:
+                mla.decode_fused(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
+                                 batch.kv_limit, S, wl.sm_scale, wl.num_shards,
+                                 O_part, LSE_part, counters, out, lse, status,
+                                 split_pages=split_pages)
+            else:
+                mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
+                                   batch.kv_limit, S, wl.sm_scale, wl.num_shards,
+                                   O_part, LSE_part, status, split_pages=split_pages)
+                mla.lse_combine(O_part, LSE_part, out, lse)
             ho.copy_(out, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -538,6 +559,9 @@ def main():
                 "l2": (f"KV {kv_bytes / 1e6:.1f} MB < 2 x L2: 256-MB L2 flush between timed steps, value from per-step event spans"
                        if flush else f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB KV), no flush"),
                 "parallelism": f"dp{world} (independent requests per rank)",
+                "step": ("mla_decode: partial decode and LSE combine fused in one launch"
+                         if args.fused else
+                         "mla_decode_partial + mla_lse_combine (two launches)"),
             },
             "us_per_layer": ms_per_step * 1e3,
             "partial_us": part_mean * 1e3,
@@ -562,7 +586,7 @@ def main():
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (1 if args.fused else 2) * args.steps,
         }
         print(json.dumps(line))
     if dist:

@@ -3,8 +3,9 @@
  *
  * The library computes weight-absorbed multi-head latent attention (MLA)
  * decode with MTP verification over a paged latent KV cache, as split-KV
- * flash-decoding: one launch writes a partial (O, LSE) per KV split (and per
- * context shard), a second launch merges the partials by LSE.
+ * flash-decoding: a partial (O, LSE) per KV split (and per context shard),
+ * merged by LSE, either as two launches (mla_decode_partial, mla_lse_combine)
+ * or fused into one (mla_decode).
  *
  * Pages that define the operations (cited by title and section):
  *   [VRAM-KV]  "Resident VRAM: weights and KV cache" (zdszero.github.io),
@@ -259,6 +260,34 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        float sm_scale, int num_splits,
                        const int32_t* split_pages, float* O_part,
                        float* LSE_part, int* status, mla_stream_t stream);
+
+/*
+ * Whole decode in one launch ([K3-MLA]: the partial (O, LSE) per split and
+ * shard, then dcp_lse_combine): mla_decode_partial followed by the
+ * mla_lse_combine over its num_splits * num_shards parts, fused.  Each
+ * cluster counts its arrival for its (request, row unit) once its part is
+ * written; the cluster that completes the count merges that unit's rows and
+ * resets the count, so no cluster ever waits for another.
+ *   inputs as mla_decode_partial; O_part and LSE_part are the caller's
+ *                    workspace for the parts (same sizes)
+ *   counters   device int32 [B * ceil(q_len * H / 128)], 4-B aligned:
+ *              all zero before the call; every call leaves them zero (also
+ *              when a bounded wait timed out).  Two calls that may run at
+ *              the same time must not share counters or workspace.
+ *   out        bf16 [B, q_len, H, 512] (round to nearest even), 16-B aligned
+ *   lse_out    fp32 [B, q_len, H] (natural log) or NULL
+ * Same errors as mla_decode_partial; MLA_ERR_INVALID_ARG if counters or out
+ * is NULL.  The tensor-core kernels only (page_size 64).
+ */
+int mla_decode(const void* q_nope_absorbed, const void* q_rope,
+               const void* kv_pages, const float* kv_scale,
+               mla_kv_dtype kv_dtype, int64_t num_slots,
+               const int32_t* req_to_token, int64_t r2t_stride,
+               const int32_t* seq_lens, const int32_t* kv_limit, int B,
+               int q_len, int H, int num_shards, int page_size, float sm_scale,
+               int num_splits, const int32_t* split_pages, float* O_part,
+               float* LSE_part, int32_t* counters, void* out, float* lse_out,
+               int* status, mla_stream_t stream);
 
 /*
  * The same computation on plain CUDA cores (no tensor cores, no TMA): a

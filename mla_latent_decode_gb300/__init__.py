@@ -69,6 +69,9 @@ def library() -> ctypes.CDLL:
             "mla_decode_partial_simt": (i32, [p, p, p, p, i32, i64, p, i64, p, p,
                                               i32, i32, i32, i32, i32, f32, i32, p,
                                               p, p, p, p]),
+            "mla_decode": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32, i32,
+                                 i32, i32, i32, f32, i32, p, p, p, p, p, p, p,
+                                 p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
         }
@@ -226,6 +229,45 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
     return O_part, LSE_part
 
 
+def fused_counters(B: int, q_len: int, H: int, device) -> torch.Tensor:
+    """Zeroed arrival counters for decode_fused (int32 [B * ceil(q_len*H/128)]);
+    every call leaves them zero again, so one tensor serves every call."""
+    return torch.zeros((B * ((q_len * H + 127) // 128),), dtype=torch.int32,
+                       device=device)
+
+
+def decode_fused(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
+                 kv_limit, num_splits: int, sm_scale: float,
+                 num_shards: int = 1, O_part=None, LSE_part=None,
+                 counters=None, out=None, lse_out=None, status=None,
+                 stream=None, split_pages=None):
+    """Partial decode and LSE combine in one launch; see mla_decode.
+
+    Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H]); workspace and
+    outputs are allocated with torch unless given."""
+    B, q_len, H, _ = q_nope.shape
+    dev = q_nope.device
+    if O_part is None:
+        O_part = torch.empty((num_splits, num_shards, B, q_len, H, VALUE_DIM),
+                             dtype=torch.float32, device=dev)
+    if LSE_part is None:
+        LSE_part = torch.empty((num_splits, num_shards, B, q_len, H),
+                               dtype=torch.float32, device=dev)
+    if counters is None:
+        counters = fused_counters(B, q_len, H, dev)
+    if out is None:
+        out = torch.empty((B, q_len, H, VALUE_DIM), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    _check(library().mla_decode(
+        _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
+        kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
+        _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
+        num_splits, _ptr(split_pages), _ptr(O_part), _ptr(LSE_part),
+        _ptr(counters), _ptr(out), _ptr(lse_out), _ptr(status), _stream(stream)))
+    return out, lse_out
+
+
 def lse_combine(O_part, LSE_part, out=None, lse_out=None, stream=None):
     """LSE merge over the leading part dims -> (bf16 [rows, 512], fp32 [rows])."""
     value_shape = LSE_part.shape
@@ -259,8 +301,9 @@ def debug_gather(kv, req_to_token, seq_lens, row_offset, total_rows: int,
 
 
 def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
-           status=None, stream=None, split_pages=None):
-    """One decode step of a synth.Batch-like object: partial + combine.
+           status=None, stream=None, split_pages=None, fused: bool = False):
+    """One decode step of a synth.Batch-like object: partial + combine (two
+    launches, or one with fused=True).
 
     Without num_splits the per-request split planner chooses the parts
     (mla_plan_parts); with num_splits and no split_pages the pages are dealt
@@ -275,6 +318,13 @@ def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
             wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards,
             kv_dtype=wl.kv_dtype)
         split_pages = torch.from_numpy(bnd).to(batch.q_nope.device)
+    if fused:
+        out, lse = decode_fused(
+            batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+            batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,
+            wl.sm_scale, num_shards=wl.num_shards, status=status, stream=stream,
+            split_pages=split_pages)
+        return out, lse, num_splits
     O_part, LSE_part = decode_partial(
         batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
         batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,

@@ -4,10 +4,11 @@
 // exchanged per-shard (O, LSE) pairs by their LSE; the same merge joins the
 // KV splits of one launch.  This is pure streaming work (one read of every
 // partial, one bf16 write), so the kernel is shaped for HBM bandwidth: one
-// warp per output row, each lane owning four float4 columns (coalesced 512-B
-// loads), parts read in order, no shared memory.
+// warp per output row (mla_combine.cuh), parts read in order, no shared
+// memory.
 #include <cuda_bf16.h>
 
+#include "mla_combine.cuh"
 #include "mla_internal.h"
 
 namespace {
@@ -22,42 +23,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int lane = threadIdx.x % 32;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
   if (row >= rows) return;
-
-  float M = -INFINITY;
-  for (int j = 0; j < P; ++j) M = fmaxf(M, __ldg(LSE_part + (int64_t)j * rows + row));
-
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float W = 0.f;
-  if (M != -INFINITY) {
-    for (int j = 0; j < P; ++j) {
-      const float lj = __ldg(LSE_part + (int64_t)j * rows + row);
-      if (lj == -INFINITY) continue;  // empty part: weight 0, never read
-      const float w = expf(lj - M);
-      W += w;
-      const float4* src = reinterpret_cast<const float4*>(
-          O_part + ((int64_t)j * rows + row) * MLA_VALUE_DIM);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 x = __ldg(src + lane + 32 * k);
-        acc[k].x = fmaf(w, x.x, acc[k].x);
-        acc[k].y = fmaf(w, x.y, acc[k].y);
-        acc[k].z = fmaf(w, x.z, acc[k].z);
-        acc[k].w = fmaf(w, x.w, acc[k].w);
-      }
-    }
-  }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  __nv_bfloat162* dst =
-      reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int c = 2 * (lane + 32 * k);  // bf16x2 index of column 4*(lane+32k)
-    dst[c] = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
-    dst[c + 1] = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
-  }
-  if (lse_out && lane == 0) lse_out[row] = W > 0.f ? M + logf(W) : -INFINITY;
+  mla::combine_row<false>(O_part, LSE_part, P, rows, row, out, lse_out, lane);
 }
 
 }  // namespace

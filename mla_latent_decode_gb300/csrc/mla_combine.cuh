@@ -1,0 +1,114 @@
+// mla_combine.cuh -- the LSE-weighted merge of one output row ([K3-MLA],
+// dcp_lse_combine), shared by the standalone combine kernel and the fused
+// epilogue of the partial-decode kernels.
+//
+// Row `row` of `rows` over P parts (part j at O_part + j*rows*512,
+// LSE_part + j*rows): M = max_j LSE_j; w_j = exp(LSE_j - M) (parts with
+// LSE = -inf have weight 0 and are never read); out = sum_j w_j O_j / sum_j
+// w_j in bf16 (round to nearest even); lse = M + ln sum_j w_j.  One warp per
+// row: lane j reads LSE_j (all weights in one round trip, reduced with
+// shuffles), then each lane owns four float4 columns of every part
+// (coalesced 512-byte loads), two parts' loads in flight at a time, parts
+// accumulated in order.
+// kCoherent: the parts were written by other CTAs of the running kernel, so
+// they are read through L2 only (no read-only or L1 copy that could be
+// stale); otherwise the read-only path.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+template <bool kCoherent>
+__device__ __forceinline__ float load_part(const float* p) {
+  return kCoherent ? __ldcg(p) : __ldg(p);
+}
+
+template <bool kCoherent>
+__device__ __forceinline__ float4 load_part4(const float4* p) {
+  return kCoherent ? __ldcg(p) : __ldg(p);
+}
+
+template <bool kCoherent>
+__device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
+                                            const float* __restrict__ LSE_part,
+                                            int P, int64_t rows, int64_t row,
+                                            __nv_bfloat16* __restrict__ out,
+                                            float* __restrict__ lse_out,
+                                            int lane) {
+  constexpr uint32_t kAll = 0xffffffffu;
+  // M = max_j LSE_j: lane j % 32 reads LSE_j (one round trip per 32 parts)
+  float M = -INFINITY;
+  for (int j0 = 0; j0 < P; j0 += 32)
+    if (j0 + lane < P)
+      M = fmaxf(M, load_part<kCoherent>(LSE_part + (int64_t)(j0 + lane) * rows + row));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float W = 0.f;  // lane-partial sum of the weights, reduced below
+  if (M != -INFINITY) {
+    for (int j0 = 0; j0 < P; j0 += 32) {
+      const int n = min(32, P - j0);
+      float wl = 0.f;  // weight of part j0 + lane (0 for an empty part)
+      if (lane < n) {
+        const float lj = load_part<kCoherent>(LSE_part + (int64_t)(j0 + lane) * rows + row);
+        wl = lj == -INFINITY ? 0.f : expf(lj - M);
+      }
+      W += wl;
+      // parts in order, two at a time so both parts' loads are in flight;
+      // an empty part (weight 0) is never read
+      for (int t = 0; t < n; t += 2) {
+        const float w0 = __shfl_sync(kAll, wl, t);
+        const float w1 = t + 1 < n ? __shfl_sync(kAll, wl, t + 1) : 0.f;
+        const float4* s0 = reinterpret_cast<const float4*>(
+            O_part + ((int64_t)(j0 + t) * rows + row) * MLA_VALUE_DIM);
+        const float4* s1 = reinterpret_cast<const float4*>(
+            O_part + ((int64_t)(j0 + t + 1) * rows + row) * MLA_VALUE_DIM);
+        float4 x0[4], x1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x0[k] = w0 != 0.f ? load_part4<kCoherent>(s0 + lane + 32 * k)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          x1[k] = w1 != 0.f ? load_part4<kCoherent>(s1 + lane + 32 * k)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (w0 != 0.f) {
+            acc[k].x = fmaf(w0, x0[k].x, acc[k].x);
+            acc[k].y = fmaf(w0, x0[k].y, acc[k].y);
+            acc[k].z = fmaf(w0, x0[k].z, acc[k].z);
+            acc[k].w = fmaf(w0, x0[k].w, acc[k].w);
+          }
+          if (w1 != 0.f) {
+            acc[k].x = fmaf(w1, x1[k].x, acc[k].x);
+            acc[k].y = fmaf(w1, x1[k].y, acc[k].y);
+            acc[k].z = fmaf(w1, x1[k].z, acc[k].z);
+            acc[k].w = fmaf(w1, x1[k].w, acc[k].w);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kAll, W, o);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  __nv_bfloat162* dst =
+      reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = 2 * (lane + 32 * k);  // bf16x2 index of column 4*(lane+32k)
+    dst[c] = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+    dst[c + 1] = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
+  }
+  if (lse_out && lane == 0) lse_out[row] = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+}  // namespace mla

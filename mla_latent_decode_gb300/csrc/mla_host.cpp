@@ -369,6 +369,32 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
   return launch_tc(a);
 }
 
+int mla_decode(const void* q_nope_absorbed, const void* q_rope,
+               const void* kv_pages, const float* kv_scale,
+               mla_kv_dtype kv_dtype, int64_t num_slots,
+               const int32_t* req_to_token, int64_t r2t_stride,
+               const int32_t* seq_lens, const int32_t* kv_limit, int B,
+               int q_len, int H, int num_shards, int page_size, float sm_scale,
+               int num_splits, const int32_t* split_pages, float* O_part,
+               float* LSE_part, int32_t* counters, void* out, float* lse_out,
+               int* status, mla_stream_t stream) {
+  DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
+               num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
+               B,               q_len,     H,        num_shards, page_size,
+               sm_scale,        num_splits, split_pages, O_part,  LSE_part,  status,
+               (cudaStream_t)stream};
+  int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  if (!counters || !out)
+    return fail(MLA_ERR_INVALID_ARG, "counters and out are required");
+  if (!aligned(counters, 4) || !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)))
+    return fail(MLA_ERR_MISALIGNED, "out needs 16-B alignment, counters and lse_out 4-B");
+  a.out = out;
+  a.lse_out = lse_out;
+  a.counters = counters;
+  return launch_tc(a);
+}
+
 int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
                             const void* kv_pages, const float* kv_scale,
                             mla_kv_dtype kv_dtype, int64_t num_slots,

@@ -47,6 +47,14 @@ struct DecodeArgs {
   float* LSE_part;
   int* status;
   cudaStream_t stream;
+  // Fused combine (mla_decode): the cluster that writes the last part of a
+  // (request, row unit) merges the unit's rows into out (bf16 [B*q_len*H,
+  // 512]) and lse_out (fp32 or NULL), counting arrivals in counters (int32
+  // [B * ceil(q_len*H / 128)], zero on entry and on exit).  NULL counters:
+  // partial results only.
+  void* out = nullptr;
+  float* lse_out = nullptr;
+  int32_t* counters = nullptr;
 };
 
 // Pages [p0, p1) of split s of a request with P pages.  With a split table

@@ -35,6 +35,7 @@
 //   cluster finishes early.
 #include <cuda_bf16.h>
 
+#include "mla_combine.cuh"
 #include "mla_tma.cuh"
 #include "ptx_sm103.cuh"
 
@@ -100,6 +101,7 @@ struct __align__(1024) Smem {
   int abort_flag;
   int ctl_slot;
   int ctl_final;
+  int ctl_last;  // fused combine: this cluster wrote the unit's last part
 };
 constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -120,6 +122,9 @@ struct TcParams {
   float* O_part;
   float* LSE_part;
   int* status;
+  __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
+  float* lse_out;
+  int* counters;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -840,6 +845,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     s.ctl_slot = 0;
     s.ctl_final = 0;
+    s.ctl_last = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
@@ -880,17 +886,50 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
   cluster_sync();  // every CTA's barriers exist before any remote operation
 
+  // Fused combine ([K3-MLA], dcp_lse_combine, in the same launch): rank 0
+  // counts this cluster's arrival for its (request, row unit) once all four
+  // CTAs have written their part; the cluster whose arrival completes the
+  // count (shards x splits) resets it and merges the unit's rows, every part
+  // being in memory by then.  No cluster waits for another.
+  const int unit_u = (int)(blockIdx.x / kCtas) % p.U;
+  auto fused_arrival = [&]() {
+    if (rank == 0 && threadIdx.x == 0) {
+      int* c = p.counters + (int64_t)w.b * p.U + unit_u;
+      const int total = p.num_splits * (p.V / p.B);
+      const bool last = atom_add_acq_rel_gpu(c, 1) == total - 1;
+      if (last) *c = 0;
+      for (uint32_t k = 0; k < kCtas; ++k)
+        st_cluster_u32(mapa(smem_u32(&s.ctl_last), k), last ? 1u : 0u);
+    }
+  };
+  auto fused_combine = [&]() {
+    if (!*reinterpret_cast<volatile int*>(&s.ctl_last)) return;
+    __threadfence();
+    const int R = p.q_len * p.H;
+    const int r0 = unit_u * MLA_ROWS_PER_UNIT;
+    const int n = min(MLA_ROWS_PER_UNIT, R - r0);
+    const int64_t rows = (int64_t)p.B * R;
+    const int P = p.num_splits * (p.V / p.B);
+    constexpr int kWarps = kThreads / 32;
+    for (int r = (int)rank * kWarps + warp; r < n; r += kCtas * kWarps)
+      combine_row<true>(p.O_part, p.LSE_part, P, rows,
+                        (int64_t)w.b * R + r0 + r, p.out, p.lse_out, lane);
+  };
+
   // Teardown, repeated at the end of every role: roles never rejoin, so no
   // warp ever asks setmaxnreg for registers back (a warpgroup that did could
   // take them before the softmax warpgroups got theirs and stall both).
   // The pair's TMEM is released only after all four CTAs are done with it.
   auto teardown = [&]() {
+    if (p.counters) __threadfence();  // this CTA's part before the arrival
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     cluster_sync();
     if (warp == 1) tmem_dealloc_pair(tmem, 512);
+    if (p.counters) fused_arrival();
     cluster_sync();
+    if (p.counters) fused_combine();
   };
 
   if (w.npages > 0 && rank < 2) {
@@ -967,6 +1006,9 @@ int launch_tc(const DecodeArgs& a) {
   p.O_part = a.O_part;
   p.LSE_part = a.LSE_part;
   p.status = a.status;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse_out = a.lse_out;
+  p.counters = a.counters;
   const int64_t units = (int64_t)p.V * p.num_splits * p.U;
   if (units * kCtas > 0x7fffffff)
     return fail(MLA_ERR_INVALID_ARG, "grid too large");

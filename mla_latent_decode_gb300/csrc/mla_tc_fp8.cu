@@ -40,6 +40,7 @@
 //   (ptx_sm103.cuh).
 #include <cuda_bf16.h>
 
+#include "mla_combine.cuh"
 #include "mla_tma.cuh"
 #include "ptx_sm103.cuh"
 
@@ -114,6 +115,7 @@ struct __align__(1024) Smem {
   int abort_flag;
   int ctl_slot;
   int ctl_final;
+  int ctl_last;  // fused combine: this cluster wrote the unit's last part
 };
 constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -136,6 +138,9 @@ struct TcParams {
   float* O_part;
   float* LSE_part;
   int* status;
+  __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
+  float* lse_out;
+  int* counters;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -1075,6 +1080,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     s.ctl_slot = 0;
     s.ctl_final = 0;
+    s.ctl_last = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
@@ -1119,14 +1125,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
   cluster_sync();  // the peer's barriers exist before any remote operation
 
+  // Fused combine ([K3-MLA], dcp_lse_combine, in the same launch): rank 0
+  // counts this pair's arrival for its (request, 128-row group) once both
+  // CTAs have written their part; the pair whose arrival completes the count
+  // (shards x splits) resets it and merges the group's rows, every part being
+  // in memory by then.  No pair waits for another.
+  const int group = (int)(blockIdx.x >> 1) % p.G;
+  auto fused_arrival = [&]() {
+    if (rank == 0 && threadIdx.x == 0) {
+      int* c = p.counters + (int64_t)w.b * p.G + group;
+      const int total = p.num_splits * (p.V / p.B);
+      const bool last = atom_add_acq_rel_gpu(c, 1) == total - 1;
+      if (last) *c = 0;
+      for (uint32_t k = 0; k < 2; ++k)
+        st_cluster_u32(mapa(smem_u32(&s.ctl_last), k), last ? 1u : 0u);
+    }
+  };
+  auto fused_combine = [&]() {
+    if (!*reinterpret_cast<volatile int*>(&s.ctl_last)) return;
+    __threadfence();
+    const int R = p.q_len * p.H;
+    const int r0 = group * kRows;
+    const int n = min(kRows, R - r0);
+    const int64_t rows = (int64_t)p.B * R;
+    const int P = p.num_splits * (p.V / p.B);
+    constexpr int kWarps = kThreads / 32;
+    for (int r = (int)rank * kWarps + warp; r < n; r += 2 * kWarps)
+      combine_row<true>(p.O_part, p.LSE_part, P, rows,
+                        (int64_t)w.b * R + r0 + r, p.out, p.lse_out, lane);
+  };
+
   // Teardown, repeated at the end of every role (roles never rejoin, so no
   // warp asks setmaxnreg for registers back).
   auto teardown = [&]() {
+    if (p.counters) __threadfence();  // this CTA's part before the arrival
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if (p.counters) {
+      cluster_sync();  // both CTAs' parts written
+      fused_arrival();
+    }
     cluster_sync();
+    if (p.counters) fused_combine();
   };
 
   if (w.npages > 0 && rank == 0) {
@@ -1204,6 +1246,9 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.O_part = a.O_part;
   p.LSE_part = a.LSE_part;
   p.status = a.status;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse_out = a.lse_out;
+  p.counters = a.counters;
   const int64_t pairs = (int64_t)p.V * p.num_splits * p.G;
   if (pairs * 2 > 0x7fffffff) return fail(MLA_ERR_INVALID_ARG, "grid too large");
   CUtensorMap map, rope_map;

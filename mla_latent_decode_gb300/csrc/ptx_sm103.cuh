@@ -457,6 +457,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr,
       : "memory");
 }
 
+// Fetch-and-add on a global int at GPU scope with acquire-release order: the
+// writes this thread has made visible before it (fences, barriers) precede
+// the add, and the adds of earlier arrivals precede what follows.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // 32 lanes x 16 consecutive 32-bit columns written from registers.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr,
                                           const uint32_t (&r)[16]) {
