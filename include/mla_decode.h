@@ -31,8 +31,9 @@
  *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device memory owned by the caller; host
- *     pointers are marked "host".  The library allocates nothing, keeps no
- *     per-call state and never frees caller memory.
+ *     pointers are marked "host".  The library allocates nothing and never
+ *     frees caller memory.  It keeps no state between calls, except the
+ *     static scratch of mla_decode_scratch (zero again after every call).
  *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
  *     checked on the host before anything is launched; on error nothing is
  *     launched and mla_last_error_string() (thread-local) says why.
@@ -60,7 +61,9 @@ enum {
   MLA_ERR_UNSUPPORTED = -2, /* valid but not built (e.g. page_size != 64) */
   MLA_ERR_MISALIGNED = -3,  /* a pointer breaks the stated alignment */
   MLA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
-  MLA_ERR_PAGE_TABLE = -5   /* mla_check_page_table found a bad entry */
+  MLA_ERR_PAGE_TABLE = -5,  /* mla_check_page_table found a bad entry */
+  MLA_ERR_SCRATCH = -6      /* mla_decode_scratch: the call needs more than
+                               the library's static scratch */
 };
 
 /* Bits OR-ed into the device status word by the kernels. */
@@ -81,6 +84,7 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 #define MLA_ROPE_DIM 64   /* qk_rope_head_dim */
 #define MLA_VALUE_DIM 512
 #define MLA_PAGE_SIZE 64  /* the only page size the kernels are built for */
+#define MLA_SCRATCH_BYTES (256u << 20) /* static scratch of mla_decode_scratch */
 #define MLA_ROWS_PER_UNIT 256 /* query rows one BF16 work unit (a 4-CTA cluster) owns;
                                  an FP8 unit (a 2-CTA cluster) owns half */
 
@@ -288,6 +292,42 @@ int mla_decode(const void* q_nope_absorbed, const void* q_rope,
                int num_splits, const int32_t* split_pages, float* O_part,
                float* LSE_part, int32_t* counters, void* out, float* lse_out,
                int* status, mla_stream_t stream);
+
+/*
+ * mla_decode with no workspace argument and no allocation: the arrival
+ * counters and the per-part (O, LSE) results live in one static device array
+ * of the library (MLA_SCRATCH_BYTES, 256-byte aligned, one per device,
+ * zero-initialised when the library's device code loads), whose address is
+ * looked up once per device with cudaGetSymbolAddress.  The call makes no
+ * cudaMalloc or cudaFree.  The pages have no counterpart: their kernels
+ * take their workspace from the serving framework; this entry point is the
+ * library's own, for callers that hold no workspace.
+ *   arguments     as mla_decode, without O_part, LSE_part and counters
+ * Size limit: the call needs mla_scratch_bytes(B, q_len, H, num_shards,
+ * num_splits) bytes; above MLA_SCRATCH_BYTES it returns MLA_ERR_SCRATCH
+ * (checked before every other argument, nothing launched) and
+ * mla_last_error_string() gives both sizes.
+ * Races: every call on a device uses the same array.  Calls that may run at
+ * the same time on one device (two streams not ordered by events, two host
+ * threads) race on it: the counters may then complete a unit early and the
+ * merged outputs and the counters' zero state are lost.  Order such calls
+ * (one stream, or events) or use mla_decode with separate workspace.
+ */
+int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
+                       const void* kv_pages, const float* kv_scale,
+                       mla_kv_dtype kv_dtype, int64_t num_slots,
+                       const int32_t* req_to_token, int64_t r2t_stride,
+                       const int32_t* seq_lens, const int32_t* kv_limit, int B,
+                       int q_len, int H, int num_shards, int page_size,
+                       float sm_scale, int num_splits,
+                       const int32_t* split_pages, void* out, float* lse_out,
+                       int* status, mla_stream_t stream);
+
+/* Scratch bytes mla_decode_scratch needs for this shape (each of the
+ * counters, LSE parts and O parts rounded up to 256 bytes), or a negative
+ * MLA_ERR_INVALID_ARG for a count below 1. */
+int64_t mla_scratch_bytes(int B, int q_len, int H, int num_shards,
+                          int num_splits);
 
 /*
  * The same computation on plain CUDA cores (no tensor cores, no TMA): a

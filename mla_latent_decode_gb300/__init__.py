@@ -72,6 +72,10 @@ def library() -> ctypes.CDLL:
             "mla_decode": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32, i32,
                                  i32, i32, i32, f32, i32, p, p, p, p, p, p, p,
                                  p]),
+            "mla_decode_scratch": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
+                                         i32, i32, i32, i32, f32, i32, p, p, p,
+                                         p, p]),
+            "mla_scratch_bytes": (i64, [i32, i32, i32, i32, i32]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
         }
@@ -265,6 +269,33 @@ def decode_fused(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
         num_splits, _ptr(split_pages), _ptr(O_part), _ptr(LSE_part),
         _ptr(counters), _ptr(out), _ptr(lse_out), _ptr(status), _stream(stream)))
+    return out, lse_out
+
+
+def scratch_bytes(B: int, q_len: int, H: int, num_shards: int,
+                  num_splits: int) -> int:
+    """Static scratch bytes decode_scratch needs (see mla_scratch_bytes)."""
+    return _check(library().mla_scratch_bytes(B, q_len, H, num_shards, num_splits))
+
+
+def decode_scratch(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
+                   kv_limit, num_splits: int, sm_scale: float,
+                   num_shards: int = 1, out=None, lse_out=None, status=None,
+                   stream=None, split_pages=None):
+    """decode_fused with its workspace in the library's static scratch; see
+    mla_decode_scratch (calls that may overlap on a device race on it)."""
+    B, q_len, H, _ = q_nope.shape
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((B, q_len, H, VALUE_DIM), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    _check(library().mla_decode_scratch(
+        _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
+        kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
+        _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
+        num_splits, _ptr(split_pages), _ptr(out), _ptr(lse_out), _ptr(status),
+        _stream(stream)))
     return out, lse_out
 
 
