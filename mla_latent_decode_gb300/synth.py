@@ -81,6 +81,7 @@ def config(name: str, seed: int = 0, **over) -> Workload:
     ragged_fp8  24 requests x q_len 5 x 96 heads, context log-uniform in
                 [1k, 200k], FP8 E4M3 KV with a per-token fp32 scale
     sweep_B<b>_L<l>  b requests x q_len 5 x 96 heads x l context, BF16
+    sweep8_B<b>_L<l> the same with FP8 E4M3 KV and a per-token fp32 scale
     """
     if name == "tiny":
         wl = Workload("tiny", 1, 1, 16, [256], num_splits=1)
@@ -94,6 +95,9 @@ def config(name: str, seed: int = 0, **over) -> Workload:
     elif name.startswith("sweep_B"):
         b, l = name[len("sweep_B"):].split("_L")
         wl = Workload(name, int(b), 5, 96, [int(l)] * int(b))
+    elif name.startswith("sweep8_B"):
+        b, l = name[len("sweep8_B"):].split("_L")
+        wl = Workload(name, int(b), 5, 96, [int(l)] * int(b), "fp8_e4m3")
     else:
         raise KeyError(name)
     for k, v in over.items():
