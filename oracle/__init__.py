@@ -65,6 +65,10 @@ def _load():
             lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
             lib.oracle_e4m3_to_f64.restype = dbl
             lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_kv_quantize.restype = None
+            lib.oracle_kv_quantize.argtypes = [p, i64, p, p]
             lib.oracle_num_threads.restype = i32
             lib.oracle_num_threads.argtypes = []
             _lib = lib
@@ -89,6 +93,23 @@ def bf16_to_f64(bits: int) -> float:
 
 def e4m3_to_f64(byte: int) -> float:
     return float(_load().oracle_e4m3_to_f64(int(byte) & 0xFF))
+
+
+def f32_to_e4m3(v: float) -> int:
+    """Nearest E4M3 code of a binary32 value (ties to even, saturated)."""
+    return int(_load().oracle_f32_to_e4m3(float(v)))
+
+
+def kv_quantize(rows):
+    """FP8 cache write of binary32 rows [n, 576]: (codes uint8 [n, 576],
+    scales fp32 [n]) with scale = fl32(amax / 448), code = E4M3(fl32(x /
+    scale)); see oracle_kv_quantize."""
+    x = _c(rows, np.float32).reshape(-1, ROW_DIM)
+    n = x.shape[0]
+    codes = np.zeros((n, ROW_DIM), np.uint8)
+    scales = np.zeros((n,), np.float32)
+    _load().oracle_kv_quantize(_ptr(x), n, _ptr(codes), _ptr(scales))
+    return codes, scales
 
 
 def mla_decode_rows(q_nope_bits, q_rope_bits, kv, kv_is_fp8, kv_scale,

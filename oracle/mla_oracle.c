@@ -262,6 +262,54 @@ void oracle_gather(const uint8_t* kv, int elem_bytes,
   }
 }
 
+/* Nearest E4M3 code to a binary32 value v (round to nearest, ties to the
+ * code with an even mantissa field, i.e. an even code), saturated to the
+ * largest finite magnitude 448; the sign bit is v's (so -0.0 gives 0x80).
+ * The definition written out: every finite non-negative code 0x00..0x7E is
+ * tried.  v must not be NaN. */
+uint8_t oracle_f32_to_e4m3(float v) {
+  const double a = fabs((double)v);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double d = fabs(oracle_e4m3_to_f64((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best_d = d;
+      best = c;
+    }
+  }
+  if (a > 448.0) best = 0x7E;
+  return (uint8_t)(best | (signbit(v) ? 0x80 : 0));
+}
+
+/* The FP8 cache write: quantise n latent rows (binary32 values, here the
+ * bf16 rows widened exactly) to E4M3 codes with one fp32 scale per row
+ * (the per-token scale of the FP8 KV format; the reading taken for its
+ * quantiser is scale = amax / 448 with round-to-nearest codes):
+ *   scale_r   = fl32(max_d |x_rd| / 448)     (one binary32 division)
+ *   code_rd   = E4M3(fl32(x_rd / scale_r))  (one binary32 division, then the
+ *               rounding above); an all-zero row gets scale 0 and codes 0.
+ * Rows must be finite. */
+void oracle_kv_quantize(const float* rows, int64_t n, uint8_t* codes,
+                        float* scales) {
+  for (int64_t r = 0; r < n; ++r) {
+    const float* x = rows + r * ROW_DIM;
+    float amax = 0.f;
+    for (int d = 0; d < ROW_DIM; ++d)
+      if (fabsf(x[d]) > amax) amax = fabsf(x[d]);
+    const float scale = amax / 448.0f;
+    scales[r] = scale;
+    for (int d = 0; d < ROW_DIM; ++d) {
+      if (scale == 0.f) {
+        codes[r * ROW_DIM + d] = 0;
+      } else {
+        const float q = x[d] / scale;
+        codes[r * ROW_DIM + d] = oracle_f32_to_e4m3(q);
+      }
+    }
+  }
+}
+
 /* Threads the OpenMP loops above will use (reported by the CPU baseline). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
