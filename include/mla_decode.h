@@ -330,6 +330,26 @@ int64_t mla_scratch_bytes(int B, int q_len, int H, int num_shards,
                           int num_splits);
 
 /*
+ * Cache write ([VRAM-KV], [VRAM-POOL]): store n new tokens' latent rows in
+ * the paged pool, row r at slot slots[r] (the token's req_to_token entry).
+ *   rows       bf16 [n, 576] (c_kv 512 then RoPE key 64), 16-B aligned
+ *   slots      int32 [n], device; a slot outside [0, num_slots) is skipped
+ *              and MLA_STATUS_BAD_SLOT is OR-ed into status
+ *   kv_pages   [num_slots, 576] bf16 or E4M3 bytes, 16-B aligned
+ *   kv_scale   fp32 [num_slots] for FP8 (NULL for BF16)
+ * BF16: the rows are copied.  FP8 E4M3 (the per-token scale format; the
+ * pages fix neither the scale rule nor the rounding, the reading taken is):
+ *   scale = fl32(max_d |x_d| / 448); code_d = E4M3(fl32(x_d / scale)), both
+ *   IEEE round-to-nearest divisions, E4M3 rounded to nearest even and
+ *   saturated to +-448; an all-zero row gets scale 0 and codes 0.
+ * Rows must be finite.  n = 0 is a no-op.  Slots written by two rows of one
+ * call get either row.
+ */
+int mla_kv_write(const void* rows, int64_t n, const int32_t* slots,
+                 void* kv_pages, mla_kv_dtype kv_dtype, float* kv_scale,
+                 int64_t num_slots, int* status, mla_stream_t stream);
+
+/*
  * The same computation on plain CUDA cores (no tensor cores, no TMA): a
  * slow, simple GPU kernel kept to cross-check the tensor-core path and to
  * cover shapes it does not take.  Same arguments and outputs.

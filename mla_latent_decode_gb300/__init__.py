@@ -76,6 +76,7 @@ def library() -> ctypes.CDLL:
                                          i32, i32, i32, i32, f32, i32, p, p, p,
                                          p, p]),
             "mla_scratch_bytes": (i64, [i32, i32, i32, i32, i32]),
+            "mla_kv_write": (i32, [p, i64, p, p, i32, p, i64, p, p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
         }
@@ -297,6 +298,15 @@ def decode_scratch(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         num_splits, _ptr(split_pages), _ptr(out), _ptr(lse_out), _ptr(status),
         _stream(stream)))
     return out, lse_out
+
+
+def kv_write(rows, slots, kv, kv_scale=None, status=None, stream=None):
+    """Store bf16 latent rows [n, 576] at `slots` of the pool `kv` (bf16, or
+    uint8 E4M3 bytes with `kv_scale`); see mla_kv_write."""
+    n = rows.shape[0]
+    _check(library().mla_kv_write(_ptr(rows), n, _ptr(slots), _ptr(kv),
+                                  _kv_dtype(kv), _ptr(kv_scale), kv.shape[0],
+                                  _ptr(status), _stream(stream)))
 
 
 def lse_combine(O_part, LSE_part, out=None, lse_out=None, stream=None):
