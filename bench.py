@@ -60,6 +60,9 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv-write-rows", type=int, default=0,
+                    help="time mla_kv_write of this many rows to random slots "
+                         "instead of the decode step (with --config's KV dtype)")
     ap.add_argument("--fused", action="store_true",
                     help="time mla_decode (partial + combine in one launch) "
                          "instead of mla_decode_partial + mla_lse_combine")
@@ -344,8 +347,72 @@ def run_sweep(args):
     return 0
 
 
+def run_kv_write(args):
+    """Cache write: N bf16 latent rows stored at random slots of a pool of 2N
+    slots (BF16 copy or FP8 quantise), inputs resident in HBM and larger
+    than L2.  HBM-bound: algorithmic bytes per row = the bf16 row and its
+    slot read, the stored row (and scale) written."""
+    import torch
+
+    import mla_latent_decode_gb300 as mla
+    from mla_latent_decode_gb300 import synth
+    mla.library()
+    wl = synth.config(args.config)
+    fp8 = wl.kv_dtype != "bf16"
+    n = args.kv_write_rows
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(0)
+    rows = torch.randn((n, 576), generator=gen, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(2 * n, device=dev)[:n].to(torch.int32)
+    kv = torch.zeros((2 * n, 576), dtype=torch.uint8 if fp8 else torch.bfloat16,
+                     device=dev)
+    scale = torch.zeros((2 * n,), dtype=torch.float32, device=dev) if fp8 else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        mla.kv_write(rows, slots, kv, scale, status)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.1)
+    t0.record(stream)
+    for _ in range(args.steps):
+        mla.kv_write(rows, slots, kv, scale, status)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = t0.elapsed_time(t1) / args.steps
+    per_row = 1152 + 4 + (576 + 4 if fp8 else 1152)
+    gbs = n * per_row / (ms * 1e-3) / 1e9
+    peaks, kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    print(json.dumps({
+        "metric": "MLA KV cache write GB/s (mla_kv_write)", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (quantise)" if fp8 else "bf16 (copy)",
+        "data": "synthetic",
+        "config": {"workload": f"{n} bf16 latent rows (576-d) to random slots of "
+                               f"a {2 * n}-slot {'E4M3' if fp8 else 'BF16'} pool",
+                   "l2": f"inputs larger than L2 ({n * 1152 / 1e9:.2f} GB of rows), no flush"},
+        "rows_per_s": n / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": None,
+                     "kernel": "mla_kv_write_kernel",
+                     "peak_kind": f"{kind} copy bandwidth",
+                     "bytes_per_row": per_row},
+        "clocks": clk, "gpu_launches": args.steps}))
+    return 0
+
+
 def main():
     args = parse()
+    if args.kv_write_rows > 0:
+        return run_kv_write(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
