@@ -112,6 +112,22 @@ def kv_quantize(rows):
     return codes, scales
 
 
+def _bf16_bits_to_f64(bits):
+    """bf16 bit patterns (uint16 array) -> float64, exactly (the upper half
+    of a binary32)."""
+    b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def head_projection(x_bits, w_bits):
+    """Per-head projection y[m, h, :] = x[m, h, :] . w[h] in fp64 over bf16
+    inputs ([K3-MEM]: the query absorption q_nope . w_kc, and the output
+    projection o_latent . w_vc): x [M, H, K], w [H, K, N] -> y [M, H, N]."""
+    x = _bf16_bits_to_f64(x_bits)
+    w = _bf16_bits_to_f64(w_bits)
+    return np.einsum("mhk,hkn->mhn", x, w)
+
+
 def mla_decode_rows(q_nope_bits, q_rope_bits, kv, kv_is_fp8, kv_scale,
                     req_to_token, seq_lens, kv_limit, B, q_len, H, sm_scale,
                     rows=None, row_lo=None, row_hi=None):
