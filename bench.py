@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--kv-write-rows", type=int, default=0,
                     help="time mla_kv_write of this many rows to random slots "
                          "instead of the decode step (with --config's KV dtype)")
+    ap.add_argument("--projections", action="store_true",
+                    help="time mla_absorb_q and mla_project_out at --config's "
+                         "rows (B * q_len) and heads instead of the decode step")
     ap.add_argument("--fused", action="store_true",
                     help="time mla_decode (partial + combine in one launch) "
                          "instead of mla_decode_partial + mla_lse_combine")
@@ -409,8 +412,96 @@ def run_kv_write(args):
     return 0
 
 
+def run_projections(args):
+    """The per-head projections around the decode (query absorption, output
+    projection) at the workload's B * q_len rows and H heads with synthetic
+    weights.  Weight-bound: R copies of each weight (R x 12.6 MB, more than
+    L2) are used in turn, R launches are captured in one CUDA graph and the
+    graph is replayed, so each launch reads its weights from DRAM and host
+    overhead stays out of the device time; HBM roofline on the algorithmic
+    bytes."""
+    import torch
+
+    import mla_latent_decode_gb300 as mla
+    from mla_latent_decode_gb300 import synth
+    mla.library()
+    wl = synth.config(args.config)
+    B, q, H = wl.B, wl.q_len, wl.H
+    R = 16
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    q_nope = torch.randn((B, q, H, 128), generator=g, device=dev).to(torch.bfloat16)
+    o_lat = torch.randn((B, q, H, 512), generator=g, device=dev).to(torch.bfloat16)
+    w_kc = [(torch.randn((H, 128, 512), generator=g, device=dev) / 11.3).to(torch.bfloat16)
+            for _ in range(R)]
+    w_vc = [(torch.randn((H, 512, 128), generator=g, device=dev) / 22.6).to(torch.bfloat16)
+            for _ in range(R)]
+    q_abs = torch.empty((B, q, H, 512), dtype=torch.bfloat16, device=dev)
+    o_v = torch.empty((B, q, H, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    peaks, kind = measured_peaks()
+    M = B * q
+    ops = {
+        "mla_absorb_q": (lambda r: mla.absorb_q(q_nope, w_kc[r], q_abs, status),
+                         M * H * 128 * 2 + H * 128 * 512 * 2 + M * H * 512 * 2),
+        "mla_project_out": (lambda r: mla.project_out(o_lat, w_vc[r], o_v, status),
+                            M * H * 512 * 2 + H * 512 * 128 * 2 + M * H * 128 * 2),
+    }
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.1)
+    res = {}
+    for name, (fn, nbytes) in ops.items():
+        for r in range(R):
+            fn(r)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for r in range(R):
+                fn(r)
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / (args.steps * R)
+        res[name] = (us, nbytes / (us * 1e-6) / 1e9, nbytes)
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    total_us = sum(v[0] for v in res.values())
+    total_bytes = sum(v[2] for v in res.values())
+    gbs = total_bytes / (total_us * 1e-6) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    print(json.dumps({
+        "metric": "MLA per-head projections us/layer (mla_absorb_q + mla_project_out)",
+        "value": total_us, "unit": "us", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (random weights)",
+        "config": {"workload": f"{M} rows (B {B} x q_len {q}) x {H} heads: "
+                               "q_nope 128 -> 512 (w_kc), o_latent 512 -> 128 (w_vc)",
+                   "l2": f"{R} weight copies used in turn ({R * H * 128 * 512 * 2 / 1e6:.0f} MB "
+                         "per projection, more than L2); launches replayed from a CUDA graph"},
+        "ops": {k: {"us": v[0], "gbs": v[1], "bytes": v[2]} for k, v in res.items()},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": None,
+                     "kernel": "mla_head_gemm_kernel",
+                     "peak_kind": f"{kind} copy bandwidth"},
+        "clocks": clk, "gpu_launches": 2 * R * args.steps}))
+    return 0
+
+
 def main():
     args = parse()
+    if args.projections:
+        return run_projections(args)
     if args.kv_write_rows > 0:
         return run_kv_write(args)
     if args.impl == "reference":

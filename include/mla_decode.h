@@ -83,6 +83,8 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 #define MLA_NOPE_DIM 512  /* kv_lora_rank: c_kv, also the value */
 #define MLA_ROPE_DIM 64   /* qk_rope_head_dim */
 #define MLA_VALUE_DIM 512
+#define MLA_QK_NOPE_DIM 128 /* per-head query/key dims before absorption */
+#define MLA_V_HEAD_DIM 128  /* per-head value dims after the output projection */
 #define MLA_PAGE_SIZE 64  /* the only page size the kernels are built for */
 #define MLA_SCRATCH_BYTES (256u << 20) /* static scratch of mla_decode_scratch */
 #define MLA_ROWS_PER_UNIT 256 /* query rows one BF16 work unit (a 4-CTA cluster) owns;
@@ -348,6 +350,27 @@ int64_t mla_scratch_bytes(int B, int q_len, int H, int num_shards,
 int mla_kv_write(const void* rows, int64_t n, const int32_t* slots,
                  void* kv_pages, mla_kv_dtype kv_dtype, float* kv_scale,
                  int64_t num_slots, int* status, mla_stream_t stream);
+
+/*
+ * The per-head projections around the absorbed decode ([K3-MEM]: w_kc is
+ * 96 x 128 x 512 bf16 and the absorbed query 512-d; the pages' kv_b_proj is
+ * absorbed into w_kc and w_vc, mla_prepare is the step before the decode).
+ * Rows m = b * q_len + i, M = B * q_len; fp32 accumulation, bf16 results
+ * rounded to nearest even.
+ *   mla_absorb_q:    q_absorbed[m, h, :512] = q_nope[m, h, :128] . w_kc[h]
+ *     q_nope bf16 [M, H, 128]; w_kc bf16 [H, 128, 512]; q_absorbed bf16
+ *     [M, H, 512] (the q_nope_absorbed input of the decode)
+ *   mla_project_out: o_v[m, h, :128] = o_latent[m, h, :512] . w_vc[h]
+ *     o_latent bf16 [M, H, 512] (the decode's out); w_vc bf16 [H, 512, 128]
+ *     (reading: v_head_dim 128, the pages give w_vc's name only); o_v bf16
+ *     [M, H, 128]
+ * All arrays device, contiguous, 16-B aligned; 1 <= H <= 65535, M >= 1.
+ * A bounded wait that gives up sets MLA_STATUS_WAIT_TIMEOUT in status.
+ */
+int mla_absorb_q(const void* q_nope, const void* w_kc, void* q_absorbed, int M,
+                 int H, int* status, mla_stream_t stream);
+int mla_project_out(const void* o_latent, const void* w_vc, void* o_v, int M,
+                    int H, int* status, mla_stream_t stream);
 
 /*
  * The same computation on plain CUDA cores (no tensor cores, no TMA): a

@@ -77,6 +77,8 @@ def library() -> ctypes.CDLL:
                                          p, p]),
             "mla_scratch_bytes": (i64, [i32, i32, i32, i32, i32]),
             "mla_kv_write": (i32, [p, i64, p, p, i32, p, i64, p, p]),
+            "mla_absorb_q": (i32, [p, p, p, i32, i32, p, p]),
+            "mla_project_out": (i32, [p, p, p, i32, i32, p, p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
         }
@@ -307,6 +309,28 @@ def kv_write(rows, slots, kv, kv_scale=None, status=None, stream=None):
     _check(library().mla_kv_write(_ptr(rows), n, _ptr(slots), _ptr(kv),
                                   _kv_dtype(kv), _ptr(kv_scale), kv.shape[0],
                                   _ptr(status), _stream(stream)))
+
+
+def absorb_q(q_nope, w_kc, out=None, status=None, stream=None):
+    """q_nope bf16 [B, q, H, 128] . w_kc bf16 [H, 128, 512] -> bf16 [B, q, H,
+    512] (the absorbed query); see mla_absorb_q."""
+    B, q, H, _ = q_nope.shape
+    if out is None:
+        out = torch.empty((B, q, H, NOPE_DIM), dtype=torch.bfloat16, device=q_nope.device)
+    _check(library().mla_absorb_q(_ptr(q_nope), _ptr(w_kc), _ptr(out), B * q, H,
+                                  _ptr(status), _stream(stream)))
+    return out
+
+
+def project_out(o_latent, w_vc, out=None, status=None, stream=None):
+    """o_latent bf16 [B, q, H, 512] . w_vc bf16 [H, 512, 128] -> bf16 [B, q, H,
+    128]; see mla_project_out."""
+    B, q, H, _ = o_latent.shape
+    if out is None:
+        out = torch.empty((B, q, H, 128), dtype=torch.bfloat16, device=o_latent.device)
+    _check(library().mla_project_out(_ptr(o_latent), _ptr(w_vc), _ptr(out), B * q,
+                                     H, _ptr(status), _stream(stream)))
+    return out
 
 
 def lse_combine(O_part, LSE_part, out=None, lse_out=None, stream=None):

@@ -31,6 +31,14 @@ __host__ __device__ constexpr uint32_t box_chunk_offset(uint32_t r, uint32_t j) 
 int make_kv_tensor_map(CUtensorMap* map, const void* kv, mla_kv_dtype dtype,
                        int64_t num_slots);
 
+// Tensor map of a bf16 3-D array (dims innermost first, in elements; strides
+// of dims 1 and 2 in bytes, multiples of 16) in boxes `box` with the
+// 128-byte swizzle (box[0] * 2 bytes <= 128); out-of-range elements read as
+// zeros.
+int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
+                            const uint64_t dims[3], const uint64_t strides[2],
+                            const uint32_t box[3]);
+
 // Tensor map of an E4M3 pool in boxes of 64 rows x 64 bytes with the 64-byte
 // swizzle (4 KB): the RoPE key columns 512..575 of one page, the K-major
 // operand layout the FP8 decode kernel's tensor cores read for those dims.

@@ -167,6 +167,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
+                                            uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // peer CTA's shared memory (cluster address), completing on the peer's
 // barrier (cluster address).
