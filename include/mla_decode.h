@@ -163,12 +163,15 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
  *   1. the uniform deal for S = 1 .. s_max;
  *   2. for S = 2 .. max_parts and 32 caps b = ceil(Pmax * k / 32): part 0 of
  *      request v = min(P_v, b) pages, the other P_v - part0 pages dealt
- *      over parts 1 .. S-1 (boundary m = part0 + floor((m-1) rest / (S-1))).
+ *      over parts 1 .. S-1 (boundary m = part0 + floor((m-1) rest / (S-1)));
+ *   3. for S = 2 .. max_parts, equal chunks of u = ceil(Pmax / S) pages:
+ *      boundary m of request v = min(P_v, m u), so a ragged batch gets units
+ *      of equal work (long requests more parts, short ones fewer).
  * Writes S = *num_parts_out and the boundaries as [V][S + 1] int32 at the
  * start of split_pages_out (a HOST buffer of at least V * (s_max + 1)
  * entries), for mla_decode_partial's split_pages.
  *   rows_per_unit, seq_lens_host, slots, s_max, c0, lam: as mla_plan_ex
- *   max_parts      largest part count of the capped family (1..s_max)
+ *   max_parts      largest part count of families 2 and 3 (1..s_max)
  *   wave_eff_out   sum(unit cost) / (slots * makespan), may be NULL
  *   makespan_out   makespan in pages, may be NULL
  */

@@ -277,6 +277,19 @@ int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
       consider(S);
     }
   }
+  // Equal chunks: parts of u = ceil(Pmax / S) pages in token order, so the
+  // longest request has S full parts and a shorter one fewer (the rest
+  // empty): every non-empty unit but a request's last carries u pages.
+  for (int S = 2; S <= max_parts; ++S) {
+    const int64_t u = (Pmax + S - 1) / S;
+    if (u < 1) continue;
+    bnd.assign((size_t)V * (S + 1), 0);
+    for (int v = 0; v < V; ++v) {
+      int64_t* row = &bnd[(size_t)v * (S + 1)];
+      for (int m = 0; m <= S; ++m) row[m] = std::min(P[v], (int64_t)m * u);
+    }
+    consider(S);
+  }
   for (size_t i = 0; i < best.size(); ++i)
     split_pages_out[i] = (int32_t)best[i];
   *num_parts_out = bestS;

@@ -122,10 +122,11 @@ def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
                s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
                lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT,
                page: int = 64):
-    """Brute force over the two candidate families (uniform deals for
+    """Brute force over three candidate families (uniform deals for
     S = 1..s_max; first part capped at b, the rest dealt over S - 1 parts for
-    S = 2..max_parts), scored by makespan + lam * S * rows / 1024, first of
-    equal scores kept.  Returns (S, boundaries [V][S+1], wave_eff, makespan)."""
+    S = 2..max_parts; equal chunks of ceil(Pmax / S) pages for S =
+    2..max_parts), scored by makespan + lam * S * rows / 1024, first of equal
+    scores kept.  Returns (S, boundaries [V][S+1], wave_eff, makespan)."""
     U = -(-H * q_len // rows_per_unit)
     rows = len(seq_lens) * q_len * H
     P = [-(-max(L, 0) // page) for L in seq_lens]
@@ -155,4 +156,9 @@ def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
                 bnd.append([0] + [first + (m - 1) * rest // (S - 1)
                                   for m in range(1, S + 1)])
             consider(S, bnd)
+    for S in range(2, max_parts + 1):
+        u = -(-pmax // S)
+        if u < 1:
+            continue
+        consider(S, [[min(p, m * u) for m in range(S + 1)] for p in P])
     return best[1], best[2], best[3], best[4]
