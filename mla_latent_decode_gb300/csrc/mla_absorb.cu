@@ -7,7 +7,9 @@
 // (B * q_len) and a weight slice per head, so the weights' HBM bytes bound
 // them; the products run on tcgen05 tensor cores.
 //
-// One CTA per (head h, tile of 128 rows), 4 warps.  Warp 0 lane 0 loads K
+// One CTA per (head h, tile of 128 rows, chunk of NC output columns), 4
+// warps: splitting N gives each head two CTAs at these sizes, so the weight
+// slices stream through twice as many SMs.  Warp 0 lane 0 loads K
 // in chunks of 128 by TMA -- the activation rows of head h through a 3-D
 // tensor map (64 K x 1 head x 128 rows boxes, K-major, 128-byte swizzle,
 // rows past M read as zeros) and the weight slice in 64 x 64 boxes (rows =
@@ -30,26 +32,27 @@ constexpr int kChunkK = 128;       // K per ring stage
 constexpr int kBoxA = 128 * 128;   // 64 K x 128 rows bf16 = 16 KB
 constexpr int kBoxB = 64 * 128;    // 64 K rows x 64 N bf16 = 8 KB
 
-template <int K, int N>
+template <int K, int N, int NC>
 struct HeadGemm {
-  static constexpr int kStages = N == 512 ? 1 : 2;
-  static constexpr int kABytes = (kChunkK / 64) * kBoxA;            // 32 KB
-  static constexpr int kBBytes = (kChunkK / 64) * (N / 64) * kBoxB;  // 128|32 KB
+  static constexpr int kABytes = (kChunkK / 64) * kBoxA;             // 32 KB
+  static constexpr int kBBytes = (kChunkK / 64) * (NC / 64) * kBoxB;  // 64|16 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kChunks = K / kChunkK;
-  static constexpr int kMmaN = N < 256 ? N : 256;
+  static constexpr int kStages = kChunks < 2 ? 1 : 2;
+  static constexpr int kMmaN = NC < 256 ? NC : 256;
+  static constexpr int kTmemCols = NC < 32 ? 32 : NC;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
-  static_assert(K % kChunkK == 0 && N % 64 == 0, "shape");
+  static_assert(K % kChunkK == 0 && N % NC == 0 && NC % 64 == 0, "shape");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int K, int N>
+template <int K, int N, int NC>
 __global__ void __launch_bounds__(128, 1)
     mla_head_gemm_kernel(const __grid_constant__ CUtensorMap a_map,
                          const __grid_constant__ CUtensorMap w_map,
                          __nv_bfloat16* __restrict__ out, int M, int H,
                          int* status) {
-  using G = HeadGemm<K, N>;
+  using G = HeadGemm<K, N, NC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -62,6 +65,7 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int h = blockIdx.y;
   const int m0 = blockIdx.x * kRowsPerCta;
+  const int n_base = blockIdx.z * NC;
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int i = 0; i < G::kStages; ++i) {
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(128, 1)
     prefetch_tmap(&w_map);
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), N < 32 ? 32 : N);
+    tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -99,9 +103,9 @@ __global__ void __launch_bounds__(128, 1)
       for (int kb = 0; kb < kChunkK / 64; ++kb) {
         const int k0 = c * kChunkK + kb * 64;
         tma_load_3d(smem_u32(sa + kb * kBoxA), &a_map, bar, k0, h, m0);
-        for (int nb = 0; nb < N / 64; ++nb)
-          tma_load_3d(smem_u32(sb + (kb * (N / 64) + nb) * kBoxB), &w_map, bar,
-                      nb * 64, k0, h);
+        for (int nb = 0; nb < NC / 64; ++nb)
+          tma_load_3d(smem_u32(sb + (kb * (NC / 64) + nb) * kBoxB), &w_map, bar,
+                      n_base + nb * 64, k0, h);
       }
       if (!mbar_wait(bar, use & 1, abort_flag)) {
         ok = false;
@@ -116,9 +120,9 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-          for (int n0 = 0; n0 < N; n0 += G::kMmaN) {
+          for (int n0 = 0; n0 < NC; n0 += G::kMmaN) {
             const uint64_t b = sdesc_sw128(
-                smem_u32(sb + (kb * (N / 64) + n0 / 64) * kBoxB), kBoxB, 1024);
+                smem_u32(sb + (kb * (NC / 64) + n0 / 64) * kBoxB), kBoxB, 1024);
             mma_ss(tmem + n0, a + 2 * ks, b + 128 * ks, idesc,
                    (c | kb | ks) ? 1u : 0u);
           }
@@ -142,12 +146,13 @@ __global__ void __launch_bounds__(128, 1)
     const int m = m0 + warp * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
-    for (int c0 = 0; c0 < N; c0 += 32) {
+    for (int c0 = 0; c0 < NC; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(taddr + c0, v);
       tmem_wait_ld();
       if (m < M) {
-        uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)m * H + h) * N + c0);
+        uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)m * H + h) * N +
+                                              n_base + c0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t w[4];
@@ -164,13 +169,13 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, N < 32 ? 32 : N);
+  if (warp == 0) tmem_dealloc(tmem, G::kTmemCols);
 }
 
-template <int K, int N>
+template <int K, int N, int NC>
 int launch_head_gemm(const void* in, const void* w, void* out, int M, int H,
                      int* status, cudaStream_t stream, const char* name) {
-  using G = HeadGemm<K, N>;
+  using G = HeadGemm<K, N, NC>;
   if (!in || !w || !out)
     return fail(MLA_ERR_INVALID_ARG, "%s: input, weights and output are required", name);
   if (M < 1 || H < 1 || H > 65535)
@@ -193,11 +198,12 @@ int launch_head_gemm(const void* in, const void* w, void* out, int M, int H,
     int rc = make_tensor_map_bf16_3d(&w_map, w, dims, strides, box);
     if (rc != MLA_OK) return rc;
   }
-  auto kernel = mla_head_gemm_kernel<K, N>;
+  auto kernel = mla_head_gemm_kernel<K, N, NC>;
   cudaError_t e = cudaFuncSetAttribute(
       kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(head gemm)");
-  const dim3 grid((unsigned)((M + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H);
+  const dim3 grid((unsigned)((M + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H,
+                  (unsigned)(N / NC));
   kernel<<<grid, 128, G::kSmemBytes, stream>>>(
       a_map, w_map, static_cast<__nv_bfloat16*>(out), M, H, status);
   e = cudaGetLastError();
@@ -213,7 +219,7 @@ using namespace mla;
 extern "C" int mla_absorb_q(const void* q_nope, const void* w_kc,
                             void* q_absorbed, int M, int H, int* status,
                             mla_stream_t stream) {
-  return launch_head_gemm<MLA_QK_NOPE_DIM, MLA_NOPE_DIM>(
+  return launch_head_gemm<MLA_QK_NOPE_DIM, MLA_NOPE_DIM, 256>(
       q_nope, w_kc, q_absorbed, M, H, status, (cudaStream_t)stream,
       "mla_absorb_q");
 }
@@ -221,7 +227,7 @@ extern "C" int mla_absorb_q(const void* q_nope, const void* w_kc,
 extern "C" int mla_project_out(const void* o_latent, const void* w_vc,
                                void* o_v, int M, int H, int* status,
                                mla_stream_t stream) {
-  return launch_head_gemm<MLA_VALUE_DIM, MLA_V_HEAD_DIM>(
+  return launch_head_gemm<MLA_VALUE_DIM, MLA_V_HEAD_DIM, 64>(
       o_latent, w_vc, o_v, M, H, status, (cudaStream_t)stream,
       "mla_project_out");
 }
