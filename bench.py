@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--config", default="dp16")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--splits", type=int, default=0, help="0: planner")
+    ap.add_argument("--planner", choices=("sched", "parts"), default="sched",
+                    help="sched: parts and longest-first launch order "
+                         "(mla_plan_sched); parts: parts in part-major order "
+                         "(mla_plan_parts)")
     ap.add_argument("--parts-cut", type=int, default=0,
                     help="two parts per request, the first of this many pages "
                          "(reproduces a larger workload's per-request plan on "
@@ -264,7 +268,7 @@ def run_reference(args):
     return 0
 
 
-def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None):
+def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
     """Median device time (ms) of one partial-decode + combine pair at S
     splits, CUDA events on the launching stream."""
     import torch
@@ -282,7 +286,7 @@ def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None):
         mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
                            batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
                            wl.sm_scale, wl.num_shards, O_part, LSE_part, status,
-                           split_pages=split_pages)
+                           split_pages=split_pages, work=work)
         mla.lse_combine(O_part, LSE_part, out, lse)
 
     for _ in range(warmup):
@@ -336,12 +340,22 @@ def run_sweep(args):
             parts = {"splits": S_parts, "wave_eff": eff_parts,
                      "first_part_pages": int(bnd[0][1]), "us": ms * 1e3,
                      "tflops": fl / (ms * 1e-3) / 1e12}
+            S_s, bnd_s, wk, eff_s = mla.plan_sched(
+                wl.B, wl.q_len, wl.H, lens, wl.num_shards, kv_dtype=wl.kv_dtype)
+            dev = batch.q_nope.device
+            ms = time_pair(mla, batch, wl, S_s, iters,
+                           split_pages=torch.from_numpy(bnd_s).to(dev),
+                           work=torch.from_numpy(wk).to(dev))
+            sched = {"splits": S_s, "wave_eff": eff_s,
+                     "first_part_pages": int(bnd_s[0][1]), "us": ms * 1e3,
+                     "tflops": fl / (ms * 1e-3) / 1e12}
             print(json.dumps({
                 "impl": "sweep", "B": B, "context": L, "q_len": wl.q_len,
                 "H": wl.H, "cluster_slots": slots,
                 "pages_rule": {"splits": S_rule, **res[S_rule]},
                 "planner": {"splits": S_plan, "wave_eff": eff, **res[S_plan]},
                 "parts_planner": parts,
+                "scheduler": sched,
                 "scan": {str(k): v for k, v in sorted(res.items())},
                 "unit": "us per layer (partial + combine), attention TFLOP/s",
             }), flush=True)
@@ -526,7 +540,7 @@ def main():
     lens = mla.batch_lengths(batch)
     slots = mla.cluster_slots()
     dev = torch.device("cuda", local)
-    split_pages, plan_desc = None, "uniform deal"
+    split_pages, work, plan_desc = None, None, "uniform deal"
     if args.parts_cut > 0:
         import numpy as np
         P = [-(-L // 64) for L in lens]
@@ -538,15 +552,25 @@ def main():
         S, eff = args.splits, None
     elif wl.num_splits:
         S, eff = wl.num_splits, None
-    else:
-        # the library's per-request split planner (part of the per-batch plan,
-        # computed before timing like the split count)
+    elif args.planner == "parts":
+        # the per-request split planner, part-major launch order (the plan is
+        # computed per batch before timing, like the split count)
         S, bnd, eff = mla.plan_parts(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
                                      kv_dtype=wl.kv_dtype)
         split_pages = torch.from_numpy(bnd).to(dev)
-        plan_desc = (f"per-request parts, first-part boundaries "
-                     f"{sorted({r[1] for r in bnd.tolist()})[:4]}"
+        plan_desc = (f"per-request parts (part-major order), first-part "
+                     f"boundaries {sorted({r[1] for r in bnd.tolist()})[:4]}"
                      if S > 1 else "one part")
+    else:
+        # the work-balanced scheduler: per-request parts and the longest-first
+        # launch order of the work units (computed per batch before timing)
+        S, bnd, wk, eff = mla.plan_sched(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
+                                         kv_dtype=wl.kv_dtype)
+        split_pages = torch.from_numpy(bnd).to(dev)
+        work = torch.from_numpy(wk).to(dev)
+        plan_desc = (f"scheduler: {S} parts per request at most, first-part "
+                     f"boundaries {sorted({r[1] for r in bnd.tolist()})[:4]}, "
+                     f"{len(wk)} work units longest first")
     S_pages = mla.plan_heuristic(wl.B, wl.q_len)
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -566,7 +590,8 @@ def main():
             mla.decode_fused(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
                              batch.req_to_token, batch.seq_lens, batch.kv_limit,
                              S, wl.sm_scale, wl.num_shards, O_part, LSE_part,
-                             counters, out, lse, status, split_pages=split_pages)
+                             counters, out, lse, status, split_pages=split_pages,
+                             work=work)
             if ev is not None:
                 ev[1].record(stream)
                 ev[2].record(stream)
@@ -576,7 +601,7 @@ def main():
         mla.decode_partial(batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
                            batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
                            wl.sm_scale, wl.num_shards, O_part, LSE_part, status,
-                           split_pages=split_pages)
+                           split_pages=split_pages, work=work)
         if ev is not None:
             ev[1].record(stream)
         mla.lse_combine(O_part, LSE_part, out, lse)
@@ -666,11 +691,12 @@ def main():
                 mla.decode_fused(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
                                  batch.kv_limit, S, wl.sm_scale, wl.num_shards,
                                  O_part, LSE_part, counters, out, lse, status,
-                                 split_pages=split_pages)
+                                 split_pages=split_pages, work=work)
             else:
                 mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
                                    batch.kv_limit, S, wl.sm_scale, wl.num_shards,
-                                   O_part, LSE_part, status, split_pages=split_pages)
+                                   O_part, LSE_part, status, split_pages=split_pages,
+                                   work=work)
                 mla.lse_combine(O_part, LSE_part, out, lse)
             ho.copy_(out, non_blocking=True)
             hl.copy_(lse, non_blocking=True)

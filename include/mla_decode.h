@@ -72,8 +72,10 @@ enum {
                                   that CTA are incomplete */
   MLA_STATUS_BAD_LENGTH = 2,   /* a sequence length exceeded the page table
                                   stride and was clamped */
-  MLA_STATUS_BAD_SLOT = 4      /* a page's slot run lay outside the pool; its
+  MLA_STATUS_BAD_SLOT = 4,     /* a page's slot run lay outside the pool; its
                                   rows were read as zeros */
+  MLA_STATUS_BAD_WORK = 8      /* a work-list entry named no work unit; that
+                                  cluster did nothing (see mla_plan_sched) */
 };
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
@@ -192,6 +194,51 @@ int mla_plan_parts(int B, int q_len, int H, int num_shards,
                    int* num_parts_out, float* wave_eff_out);
 
 /*
+ * Work-balanced scheduler: the parts of mla_plan_parts_ex plus the order in
+ * which the kernel takes its work units.  A work unit is one part s of one
+ * virtual request v for one group u of rows_per_unit query rows, identified
+ * by id = (s * V + v) * U + u, U = ceil(q_len * H / rows_per_unit); without
+ * a work list the kernel launches the ids in increasing order.  Here the
+ * units are ordered longest first (cost = pages + c0, an empty unit 1; equal
+ * costs in increasing id), so the cluster slots, which the hardware fills in
+ * launch order as they free up, run a longest-processing-time list schedule:
+ * on a ragged batch the long parts start first and the short ones fill the
+ * gaps at the end ([K3-MLA]'s wave-aware rounding, taken to unequal work).
+ * Candidates are the three families of mla_plan_parts_ex, each scored by the
+ * makespan of that schedule plus lam * S * rows / 1024; the first of equal
+ * scores is kept.
+ *   V .. lam, split_pages_out, num_parts_out: as mla_plan_parts_ex
+ *   work_out       HOST int32 buffer of work_capacity entries; receives the
+ *                  V * S * U unit ids in launch order (a permutation of
+ *                  0 .. V*S*U - 1), for the decode entry points' `work`
+ *   num_work_out   V * S * U
+ *   wave_eff_out   sum(unit cost) / (slots * makespan), may be NULL
+ *   makespan_out   makespan in pages, may be NULL
+ * MLA_ERR_INVALID_ARG (nothing written) if work_capacity < V * S * U.
+ */
+int mla_plan_sched_ex(int V, int q_len, int H, int rows_per_unit,
+                      const int32_t* seq_lens_host, int slots, int s_max,
+                      int max_parts, double c0, double lam,
+                      int32_t* split_pages_out, int* num_parts_out,
+                      int32_t* work_out, int64_t work_capacity,
+                      int64_t* num_work_out, float* wave_eff_out,
+                      double* makespan_out);
+
+/*
+ * mla_plan_sched_ex with mla_plan's defaults (rows per unit and slots of the
+ * kernel that serves kv_dtype, s_max = 64, c0 = 32, lam = 1).
+ * split_pages_out: HOST int32 [num_shards * B * 65]; work_out: HOST int32
+ * [work_capacity], at most num_shards * B * 64 * ceil(q_len * H / 128)
+ * entries are written.
+ */
+int mla_plan_sched(int B, int q_len, int H, int num_shards,
+                   mla_kv_dtype kv_dtype, const int32_t* seq_lens_host,
+                   int num_sms, int max_parts, int32_t* split_pages_out,
+                   int* num_parts_out, int32_t* work_out,
+                   int64_t work_capacity, int64_t* num_work_out,
+                   float* wave_eff_out);
+
+/*
  * Host-side check of a page table (optional validation mode).  All
  * pointers are HOST copies.  Checks, for every virtual request v < V:
  * 1 <= q_len; 0 <= seq_lens[v] <= stride; without kv_limit seq_lens[v] >=
@@ -245,8 +292,17 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *                    partition each request's pages (non-decreasing from 0
  *                    to ceil(L_v / 64)) for the combine to be the full
  *                    result; NULL deals the pages uniformly.
- *                    Work is launched split by split (all first parts, then
- *                    all second parts, ...).
+ *                    Without a work list, work is launched split by split
+ *                    (all first parts, then all second parts, ...).
+ *   work             device int32 [num_work] or NULL: the work-unit ids
+ *                    (see mla_plan_sched) in launch order.  It must hold
+ *                    every id 0 .. num_work - 1 once, num_work = num_splits *
+ *                    num_shards * B * ceil(q_len * H / R), R = 256 rows for
+ *                    BF16 KV and 128 for FP8 (else MLA_ERR_INVALID_ARG); an
+ *                    entry outside that range sets MLA_STATUS_BAD_WORK and
+ *                    its cluster does nothing.  The results do not depend on
+ *                    the order.
+ *   num_work         entries of work (0 when work is NULL)
  *   O_part           fp32 [num_splits, num_shards, B, q_len, H, 512], 16-B al.
  *   LSE_part         fp32 [num_splits, num_shards, B, q_len, H]
  *   status           device int or NULL (MLA_STATUS_* bits are OR-ed in)
@@ -267,8 +323,9 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* seq_lens, const int32_t* kv_limit,
                        int B, int q_len, int H, int num_shards, int page_size,
                        float sm_scale, int num_splits,
-                       const int32_t* split_pages, float* O_part,
-                       float* LSE_part, int* status, mla_stream_t stream);
+                       const int32_t* split_pages, const int32_t* work,
+                       int num_work, float* O_part, float* LSE_part,
+                       int* status, mla_stream_t stream);
 
 /*
  * Whole decode in one launch ([K3-MLA]: the partial (O, LSE) per split and
@@ -294,7 +351,8 @@ int mla_decode(const void* q_nope_absorbed, const void* q_rope,
                const int32_t* req_to_token, int64_t r2t_stride,
                const int32_t* seq_lens, const int32_t* kv_limit, int B,
                int q_len, int H, int num_shards, int page_size, float sm_scale,
-               int num_splits, const int32_t* split_pages, float* O_part,
+               int num_splits, const int32_t* split_pages,
+               const int32_t* work, int num_work, float* O_part,
                float* LSE_part, int32_t* counters, void* out, float* lse_out,
                int* status, mla_stream_t stream);
 
@@ -325,8 +383,9 @@ int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* seq_lens, const int32_t* kv_limit, int B,
                        int q_len, int H, int num_shards, int page_size,
                        float sm_scale, int num_splits,
-                       const int32_t* split_pages, void* out, float* lse_out,
-                       int* status, mla_stream_t stream);
+                       const int32_t* split_pages, const int32_t* work,
+                       int num_work, void* out, float* lse_out, int* status,
+                       mla_stream_t stream);
 
 /* Scratch bytes mla_decode_scratch needs for this shape (each of the
  * counters, LSE parts and O parts rounded up to 256 bytes), or a negative

@@ -62,19 +62,23 @@ def library() -> ctypes.CDLL:
                                         f64, p, p, p, p]),
             "mla_plan_parts": (i32, [i32, i32, i32, i32, i32, p, i32, i32, p, p,
                                      p]),
+            "mla_plan_sched_ex": (i32, [i32, i32, i32, i32, p, i32, i32, i32, f64,
+                                        f64, p, p, p, i64, p, p, p]),
+            "mla_plan_sched": (i32, [i32, i32, i32, i32, i32, p, i32, i32, p, p,
+                                     p, i64, p, p]),
             "mla_check_page_table": (i32, [p, i64, p, p, i32, i32, i32, i64]),
             "mla_decode_partial": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
-                                         i32, i32, i32, i32, f32, i32, p, p, p, p,
-                                         p]),
+                                         i32, i32, i32, i32, f32, i32, p, p, i32,
+                                         p, p, p, p]),
             "mla_decode_partial_simt": (i32, [p, p, p, p, i32, i64, p, i64, p, p,
                                               i32, i32, i32, i32, i32, f32, i32, p,
                                               p, p, p, p]),
             "mla_decode": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32, i32,
-                                 i32, i32, i32, f32, i32, p, p, p, p, p, p, p,
-                                 p]),
+                                 i32, i32, i32, f32, i32, p, p, i32, p, p, p, p,
+                                 p, p, p]),
             "mla_decode_scratch": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
-                                         i32, i32, i32, i32, f32, i32, p, p, p,
-                                         p, p]),
+                                         i32, i32, i32, i32, f32, i32, p, p, i32,
+                                         p, p, p, p]),
             "mla_scratch_bytes": (i64, [i32, i32, i32, i32, i32]),
             "mla_kv_write": (i32, [p, i64, p, p, i32, p, i64, p, p]),
             "mla_absorb_q": (i32, [p, p, p, i32, i32, p, p]),
@@ -187,6 +191,52 @@ def plan_parts(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
     return S.value, bnd.reshape(V, S.value + 1).copy(), eff.value
 
 
+def plan_sched_ex(seq_lens: Sequence[int], q_len: int, H: int, slots: int,
+                  s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
+                  lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT):
+    """Work-balanced scheduler: returns (S, boundaries np.int32 [V, S+1],
+    work np.int32 [V*S*U] (unit ids, longest first), wave_eff, makespan)."""
+    import numpy as np
+    arr = _host_i32(seq_lens)
+    V = len(arr)
+    U = -(-q_len * H // rows_per_unit)
+    cap = V * s_max * U
+    bnd_out = (ctypes.c_int32 * (V * (s_max + 1)))()
+    work_out = (ctypes.c_int32 * cap)()
+    S, n = ctypes.c_int(), ctypes.c_int64()
+    eff, ms = ctypes.c_float(), ctypes.c_double()
+    _check(library().mla_plan_sched_ex(V, q_len, H, rows_per_unit, arr, slots,
+                                       s_max, max_parts, float(c0), float(lam),
+                                       bnd_out, ctypes.byref(S), work_out, cap,
+                                       ctypes.byref(n), ctypes.byref(eff),
+                                       ctypes.byref(ms)))
+    bnd = np.frombuffer(bnd_out, dtype=np.int32)[:V * (S.value + 1)]
+    work = np.frombuffer(work_out, dtype=np.int32)[:n.value].copy()
+    return S.value, bnd.reshape(V, S.value + 1).copy(), work, eff.value, ms.value
+
+
+def plan_sched(B: int, q_len: int, H: int, seq_lens, num_shards: int = 1,
+               num_sms: int = 0, kv_dtype: str = "bf16", max_parts: int = 8):
+    """Work-balanced scheduler with the library defaults for the kernel that
+    serves `kv_dtype`: returns (S, boundaries np.int32 [V, S+1], work
+    np.int32 [V*S*U] in launch order, wave_eff); num_sms=0 asks the device."""
+    import numpy as np
+    arr = _host_i32(seq_lens)
+    V = len(arr)
+    assert V == B * num_shards
+    cap = V * 64 * (-(-q_len * H // 128))
+    bnd_out = (ctypes.c_int32 * (V * 65))()
+    work_out = (ctypes.c_int32 * cap)()
+    S, n, eff = ctypes.c_int(), ctypes.c_int64(), ctypes.c_float()
+    _check(library().mla_plan_sched(B, q_len, H, num_shards, _KV_DTYPE[kv_dtype],
+                                    arr, num_sms, max_parts, bnd_out,
+                                    ctypes.byref(S), work_out, cap,
+                                    ctypes.byref(n), ctypes.byref(eff)))
+    bnd = np.frombuffer(bnd_out, dtype=np.int32)[:V * (S.value + 1)]
+    work = np.frombuffer(work_out, dtype=np.int32)[:n.value].copy()
+    return S.value, bnd.reshape(V, S.value + 1).copy(), work, eff.value
+
+
 def check_page_table(req_to_token, seq_lens, kv_limit, q_len: int,
                      num_slots: int, page_size: int = PAGE_SIZE) -> None:
     """Host validation of a page table (raises MlaError on a bad entry)."""
@@ -211,9 +261,11 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
                    kv_limit, num_splits: int, sm_scale: float,
                    num_shards: int = 1, O_part=None, LSE_part=None,
                    status=None, simt: bool = False, stream=None,
-                   split_pages=None):
+                   split_pages=None, work=None):
     """Partial (O, LSE) per split and shard; see mla_decode_partial.
-    `split_pages`: device int32 [num_shards*B, num_splits+1] or None.
+    `split_pages`: device int32 [num_shards*B, num_splits+1] or None;
+    `work`: device int32 unit ids in launch order (plan_sched) or None
+    (tensor-core path only).
 
     Returns (O_part fp32 [S, shards, B, q, H, 512], LSE_part fp32 [S, shards,
     B, q, H]); outputs are allocated with torch unless given.
@@ -226,13 +278,19 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
     if LSE_part is None:
         LSE_part = torch.empty((num_splits, num_shards, B, q_len, H),
                                dtype=torch.float32, device=dev)
-    fn = library().mla_decode_partial_simt if simt else library().mla_decode_partial
-    _check(fn(_ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale),
-              _kv_dtype(kv), kv.shape[0], _ptr(req_to_token),
-              req_to_token.stride(0), _ptr(seq_lens), _ptr(kv_limit), B, q_len,
-              H, num_shards, PAGE_SIZE, float(sm_scale), num_splits,
-              _ptr(split_pages), _ptr(O_part), _ptr(LSE_part), _ptr(status),
-              _stream(stream)))
+    args = (_ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale),
+            _kv_dtype(kv), kv.shape[0], _ptr(req_to_token),
+            req_to_token.stride(0), _ptr(seq_lens), _ptr(kv_limit), B, q_len,
+            H, num_shards, PAGE_SIZE, float(sm_scale), num_splits,
+            _ptr(split_pages))
+    tail = (_ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream))
+    if simt:
+        if work is not None:
+            raise ValueError("the CUDA-core path takes no work list")
+        _check(library().mla_decode_partial_simt(*args, *tail))
+    else:
+        _check(library().mla_decode_partial(
+            *args, _ptr(work), 0 if work is None else work.numel(), *tail))
     return O_part, LSE_part
 
 
@@ -247,7 +305,7 @@ def decode_fused(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
                  kv_limit, num_splits: int, sm_scale: float,
                  num_shards: int = 1, O_part=None, LSE_part=None,
                  counters=None, out=None, lse_out=None, status=None,
-                 stream=None, split_pages=None):
+                 stream=None, split_pages=None, work=None):
     """Partial decode and LSE combine in one launch; see mla_decode.
 
     Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H]); workspace and
@@ -270,7 +328,8 @@ def decode_fused(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
         kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
         _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
-        num_splits, _ptr(split_pages), _ptr(O_part), _ptr(LSE_part),
+        num_splits, _ptr(split_pages), _ptr(work),
+        0 if work is None else work.numel(), _ptr(O_part), _ptr(LSE_part),
         _ptr(counters), _ptr(out), _ptr(lse_out), _ptr(status), _stream(stream)))
     return out, lse_out
 
@@ -284,7 +343,7 @@ def scratch_bytes(B: int, q_len: int, H: int, num_shards: int,
 def decode_scratch(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
                    kv_limit, num_splits: int, sm_scale: float,
                    num_shards: int = 1, out=None, lse_out=None, status=None,
-                   stream=None, split_pages=None):
+                   stream=None, split_pages=None, work=None):
     """decode_fused with its workspace in the library's static scratch; see
     mla_decode_scratch (calls that may overlap on a device race on it)."""
     B, q_len, H, _ = q_nope.shape
@@ -297,8 +356,9 @@ def decode_scratch(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
         kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
         _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
-        num_splits, _ptr(split_pages), _ptr(out), _ptr(lse_out), _ptr(status),
-        _stream(stream)))
+        num_splits, _ptr(split_pages), _ptr(work),
+        0 if work is None else work.numel(), _ptr(out), _ptr(lse_out),
+        _ptr(status), _stream(stream)))
     return out, lse_out
 
 
@@ -366,35 +426,38 @@ def debug_gather(kv, req_to_token, seq_lens, row_offset, total_rows: int,
 
 
 def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
-           status=None, stream=None, split_pages=None, fused: bool = False):
+           status=None, stream=None, split_pages=None, fused: bool = False,
+           work=None):
     """One decode step of a synth.Batch-like object: partial + combine (two
     launches, or one with fused=True).
 
-    Without num_splits the per-request split planner chooses the parts
-    (mla_plan_parts); with num_splits and no split_pages the pages are dealt
-    uniformly.  Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H],
-    num_splits).
+    Without num_splits the work-balanced scheduler chooses the parts and the
+    launch order (mla_plan_sched; the CUDA-core path takes the parts only);
+    with num_splits and no split_pages the pages are dealt uniformly.
+    Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H], num_splits).
     """
     wl = batch.wl
     if num_splits is None and wl.num_splits:
         num_splits = wl.num_splits
     if num_splits is None:
-        num_splits, bnd, _ = plan_parts(
+        num_splits, bnd, wk, _ = plan_sched(
             wl.B, wl.q_len, wl.H, batch_lengths(batch), wl.num_shards,
             kv_dtype=wl.kv_dtype)
         split_pages = torch.from_numpy(bnd).to(batch.q_nope.device)
+        if not simt:
+            work = torch.from_numpy(wk).to(batch.q_nope.device)
     if fused:
         out, lse = decode_fused(
             batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
             batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,
             wl.sm_scale, num_shards=wl.num_shards, status=status, stream=stream,
-            split_pages=split_pages)
+            split_pages=split_pages, work=work)
         return out, lse, num_splits
     O_part, LSE_part = decode_partial(
         batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
         batch.req_to_token, batch.seq_lens, batch.kv_limit, num_splits,
         wl.sm_scale, num_shards=wl.num_shards, status=status, simt=simt,
-        stream=stream, split_pages=split_pages)
+        stream=stream, split_pages=split_pages, work=work)
     out, lse = lse_combine(O_part, LSE_part, stream=stream)
     return out, lse, num_splits
 

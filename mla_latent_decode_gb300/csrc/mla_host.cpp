@@ -70,6 +70,24 @@ int check_decode_args(const DecodeArgs& a) {
   return MLA_OK;
 }
 
+int check_work(const DecodeArgs& a) {
+  if (!a.work) {
+    if (a.num_work != 0)
+      return fail(MLA_ERR_INVALID_ARG, "num_work %d without a work list", a.num_work);
+    return MLA_OK;
+  }
+  const int R = a.kv_dtype == MLA_KV_FP8_E4M3 ? MLA_ROWS_PER_UNIT / 2
+                                             : MLA_ROWS_PER_UNIT;
+  const int64_t U = ((int64_t)a.q_len * a.H + R - 1) / R;
+  const int64_t n = (int64_t)a.B * a.num_shards * a.num_splits * U;
+  if (a.num_work != n)
+    return fail(MLA_ERR_INVALID_ARG, "num_work %d: the launch has %lld work units",
+                a.num_work, (long long)n);
+  if (!aligned(a.work, 4))
+    return fail(MLA_ERR_MISALIGNED, "work needs 4-B alignment");
+  return MLA_OK;
+}
+
 // Default cost constants of mla_plan, in units of one page of one work unit
 // (about 0.9 us on a GB300): a work unit's fixed cost (launch, Q load,
 // pipeline fill, O_part write, wave hand-over) and the price of one more split
@@ -187,41 +205,64 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
                      num_splits_out, wave_eff_out, nullptr);
 }
 
-// One split schedule (boundaries bnd[v * (S + 1) + k]) in launch order: part
-// s of every request before part s + 1, row units innermost; a unit costs its
-// pages + c0, an empty one c_empty.  Returns the list-scheduling makespan on
-// `slots` and adds the unit costs to *total.
+// One split schedule (boundaries bnd[v * (S + 1) + k]): its work units, each
+// (part s, request v, row unit u) costing its pages + c0 (an empty one
+// c_empty), are list-scheduled on `slots` in launch order, which is by
+// increasing id (s * V + v) * U + u (part-major), or with `lpt` longest first
+// (equal costs by increasing id).  Returns the makespan, adds the unit costs
+// to *total and, when `order` is given, stores the ids in launch order.
 static double schedule_makespan(const std::vector<int64_t>& P, int U, int S,
                                 const std::vector<int64_t>& bnd, int slots,
-                                double c0, double c_empty, double* total) {
-  std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+                                double c0, double c_empty, bool lpt,
+                                double* total, std::vector<int32_t>* order) {
   const size_t V = P.size();
-  const size_t n = std::min<size_t>((size_t)slots, V * (size_t)S * (size_t)U);
-  for (size_t k = 0; k < n; ++k) heap.push(0.0);
-  double end = 0.0, tot = 0.0;
+  // the U units of one (s, v) share its cost and have consecutive ids
+  std::vector<std::pair<double, int64_t>> groups;
+  groups.reserve(V * (size_t)S);
   for (int s = 0; s < S; ++s)
     for (size_t v = 0; v < V; ++v) {
       const int64_t pages = bnd[v * (S + 1) + s + 1] - bnd[v * (S + 1) + s];
-      const double c = pages > 0 ? (double)pages + c0 : c_empty;
-      for (int u = 0; u < U; ++u) {
-        const double t = heap.top() + c;
-        heap.pop();
-        end = std::max(end, t);
-        heap.push(t);
-        tot += c;
-      }
+      groups.emplace_back(pages > 0 ? (double)pages + c0 : c_empty,
+                          (int64_t)s * (int64_t)V + (int64_t)v);
+    }
+  if (lpt)
+    std::stable_sort(groups.begin(), groups.end(),
+                     [](const std::pair<double, int64_t>& a,
+                        const std::pair<double, int64_t>& b) {
+                       return a.first > b.first;
+                     });
+  std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+  const size_t n = std::min<size_t>((size_t)slots, V * (size_t)S * (size_t)U);
+  for (size_t k = 0; k < n; ++k) heap.push(0.0);
+  double end = 0.0, tot = 0.0;
+  if (order) order->clear();
+  for (const auto& g : groups)
+    for (int u = 0; u < U; ++u) {
+      const double t = heap.top() + g.first;
+      heap.pop();
+      end = std::max(end, t);
+      heap.push(t);
+      tot += g.first;
+      if (order) order->push_back((int32_t)(g.second * U + u));
     }
   *total = tot;
   return end;
 }
 
-int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
-                      const int32_t* seq_lens_host, int slots, int s_max,
-                      int max_parts, double c0, double lam,
-                      int32_t* split_pages_out, int* num_parts_out,
-                      float* wave_eff_out, double* makespan_out) {
-  if (V < 1 || q_len < 1 || H < 1 || !seq_lens_host || !split_pages_out ||
-      !num_parts_out)
+// The candidate families of the parts planner (uniform deals, capped first
+// part, equal chunks), scored by the schedule's makespan + lam * S * rows /
+// 1024 in launch order or longest first; the first of equal scores wins.
+struct PartsPlan {
+  int S = 0;
+  std::vector<int64_t> bnd;
+  double makespan = 0, total = 0;
+};
+
+static int plan_parts_impl(int V, int q_len, int H, int rows_per_unit,
+                           const int32_t* seq_lens_host, int slots, int s_max,
+                           int max_parts, double c0, double lam, bool lpt,
+                           PartsPlan* best_out) {
+  if (V < 1 || q_len < 1 || H < 1 || !seq_lens_host)
     return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
   if (rows_per_unit < 1 || slots < 1 || s_max < 1 || s_max > 1024 ||
       max_parts < 1 || max_parts > s_max || !(c0 >= 0) || !(lam >= 0))
@@ -238,19 +279,21 @@ int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
   }
   constexpr int kCaps = 32;
   constexpr double kEmpty = 1.0;
-  double bestJ = 0, bestMs = 0, bestTot = 0;
-  int bestS = 0;
-  std::vector<int64_t> bnd, best;
+  double bestJ = 0;
+  PartsPlan& best = *best_out;
+  best = PartsPlan();
+  std::vector<int64_t> bnd;
   auto consider = [&](int S) {
     double tot = 0;
-    const double ms = schedule_makespan(P, U, S, bnd, slots, c0, kEmpty, &tot);
+    const double ms =
+        schedule_makespan(P, U, S, bnd, slots, c0, kEmpty, lpt, &tot, nullptr);
     const double J = ms + lam * S * rows / 1024.0;
-    if (bestS == 0 || J < bestJ - 1e-9) {
+    if (best.S == 0 || J < bestJ - 1e-9) {
       bestJ = J;
-      bestS = S;
-      bestMs = ms;
-      bestTot = tot;
-      best = bnd;
+      best.S = S;
+      best.makespan = ms;
+      best.total = tot;
+      best.bnd = bnd;
     }
   };
   // Uniform deals.
@@ -290,12 +333,77 @@ int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
     }
     consider(S);
   }
-  for (size_t i = 0; i < best.size(); ++i)
-    split_pages_out[i] = (int32_t)best[i];
-  *num_parts_out = bestS;
+  return MLA_OK;
+}
+
+// Cluster slots of the kernel that serves kv_dtype (num_sms > 0: that many
+// SMs divided by the cluster size instead of asking the device).
+static int decode_slots(mla_kv_dtype kv_dtype, int num_sms) {
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const int ctas = fp8 ? 2 : 4;
+  if (num_sms > 0) return std::max(1, num_sms / ctas);
+  const int slots = fp8 ? pair_slots_fp8() : mla_cluster_slots();
+  if (slots == 0) return fail(MLA_ERR_CUDA, "no decode cluster fits on this device");
+  return slots;
+}
+
+int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
+                      const int32_t* seq_lens_host, int slots, int s_max,
+                      int max_parts, double c0, double lam,
+                      int32_t* split_pages_out, int* num_parts_out,
+                      float* wave_eff_out, double* makespan_out) {
+  if (!split_pages_out || !num_parts_out)
+    return fail(MLA_ERR_INVALID_ARG, "bad planner arguments");
+  PartsPlan best;
+  const int rc = plan_parts_impl(V, q_len, H, rows_per_unit, seq_lens_host,
+                                 slots, s_max, max_parts, c0, lam, false, &best);
+  if (rc != MLA_OK) return rc;
+  for (size_t i = 0; i < best.bnd.size(); ++i)
+    split_pages_out[i] = (int32_t)best.bnd[i];
+  *num_parts_out = best.S;
   if (wave_eff_out)
-    *wave_eff_out = bestMs > 0 ? (float)(bestTot / ((double)slots * bestMs)) : 1.f;
-  if (makespan_out) *makespan_out = bestMs;
+    *wave_eff_out = best.makespan > 0
+                        ? (float)(best.total / ((double)slots * best.makespan))
+                        : 1.f;
+  if (makespan_out) *makespan_out = best.makespan;
+  return MLA_OK;
+}
+
+int mla_plan_sched_ex(int V, int q_len, int H, int rows_per_unit,
+                      const int32_t* seq_lens_host, int slots, int s_max,
+                      int max_parts, double c0, double lam,
+                      int32_t* split_pages_out, int* num_parts_out,
+                      int32_t* work_out, int64_t work_capacity,
+                      int64_t* num_work_out, float* wave_eff_out,
+                      double* makespan_out) {
+  if (!split_pages_out || !num_parts_out || !work_out || !num_work_out)
+    return fail(MLA_ERR_INVALID_ARG, "bad scheduler arguments");
+  PartsPlan best;
+  int rc = plan_parts_impl(V, q_len, H, rows_per_unit, seq_lens_host, slots,
+                           s_max, max_parts, c0, lam, true, &best);
+  if (rc != MLA_OK) return rc;
+  const int U = (H * q_len + rows_per_unit - 1) / rows_per_unit;
+  const int64_t n = (int64_t)V * best.S * U;
+  if (n > work_capacity || n > 0x7fffffff)
+    return fail(MLA_ERR_INVALID_ARG, "work list needs %lld entries, capacity %lld",
+                (long long)n, (long long)work_capacity);
+  std::vector<int64_t> P(V);
+  for (int v = 0; v < V; ++v)
+    P[v] = ((int64_t)std::max<int32_t>(seq_lens_host[v], 0) + MLA_PAGE_SIZE - 1) /
+           MLA_PAGE_SIZE;
+  std::vector<int32_t> order;
+  double tot = 0;
+  schedule_makespan(P, U, best.S, best.bnd, slots, c0, 1.0, true, &tot, &order);
+  for (size_t i = 0; i < best.bnd.size(); ++i)
+    split_pages_out[i] = (int32_t)best.bnd[i];
+  for (int64_t i = 0; i < n; ++i) work_out[i] = order[(size_t)i];
+  *num_parts_out = best.S;
+  *num_work_out = n;
+  if (wave_eff_out)
+    *wave_eff_out = best.makespan > 0
+                        ? (float)(best.total / ((double)slots * best.makespan))
+                        : 1.f;
+  if (makespan_out) *makespan_out = best.makespan;
   return MLA_OK;
 }
 
@@ -307,21 +415,35 @@ int mla_plan_parts(int B, int q_len, int H, int num_shards,
     return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
     return fail(MLA_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
-  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
-  const int ctas = fp8 ? 2 : 4;
-  int slots;
-  if (num_sms > 0) {
-    slots = std::max(1, num_sms / ctas);
-  } else {
-    slots = fp8 ? pair_slots_fp8() : mla_cluster_slots();
-    if (slots < 0) return slots;
-    if (slots == 0) return fail(MLA_ERR_CUDA, "no decode cluster fits on this device");
-  }
+  const int slots = decode_slots(kv_dtype, num_sms);
+  if (slots < 0) return slots;
   return mla_plan_parts_ex(B * num_shards, q_len, H,
-                           fp8 ? MLA_ROWS_PER_UNIT / 2 : MLA_ROWS_PER_UNIT,
+                           kv_dtype == MLA_KV_FP8_E4M3 ? MLA_ROWS_PER_UNIT / 2
+                                                       : MLA_ROWS_PER_UNIT,
                            seq_lens_host, slots, 64, max_parts, kPlanUnitCost,
                            kPlanSplitCost, split_pages_out, num_parts_out,
                            wave_eff_out, nullptr);
+}
+
+int mla_plan_sched(int B, int q_len, int H, int num_shards,
+                   mla_kv_dtype kv_dtype, const int32_t* seq_lens_host,
+                   int num_sms, int max_parts, int32_t* split_pages_out,
+                   int* num_parts_out, int32_t* work_out,
+                   int64_t work_capacity, int64_t* num_work_out,
+                   float* wave_eff_out) {
+  if (B < 1 || num_shards < 1)
+    return fail(MLA_ERR_INVALID_ARG, "B and num_shards must be >= 1");
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  const int slots = decode_slots(kv_dtype, num_sms);
+  if (slots < 0) return slots;
+  return mla_plan_sched_ex(B * num_shards, q_len, H,
+                           kv_dtype == MLA_KV_FP8_E4M3 ? MLA_ROWS_PER_UNIT / 2
+                                                       : MLA_ROWS_PER_UNIT,
+                           seq_lens_host, slots, 64, max_parts, kPlanUnitCost,
+                           kPlanSplitCost, split_pages_out, num_parts_out,
+                           work_out, work_capacity, num_work_out, wave_eff_out,
+                           nullptr);
 }
 
 int mla_check_page_table(const int32_t* r2t, int64_t stride,
@@ -370,14 +492,19 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* seq_lens, const int32_t* kv_limit, int B,
                        int q_len, int H, int num_shards, int page_size,
                        float sm_scale, int num_splits,
-                       const int32_t* split_pages, float* O_part,
-                       float* LSE_part, int* status, mla_stream_t stream) {
+                       const int32_t* split_pages, const int32_t* work,
+                       int num_work, float* O_part, float* LSE_part,
+                       int* status, mla_stream_t stream) {
   DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
                num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
                B,               q_len,     H,        num_shards, page_size,
                sm_scale,        num_splits, split_pages, O_part,  LSE_part,  status,
                (cudaStream_t)stream};
+  a.work = work;
+  a.num_work = num_work;
   int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  rc = check_work(a);
   if (rc != MLA_OK) return rc;
   return launch_tc(a);
 }
@@ -388,7 +515,8 @@ int mla_decode(const void* q_nope_absorbed, const void* q_rope,
                const int32_t* req_to_token, int64_t r2t_stride,
                const int32_t* seq_lens, const int32_t* kv_limit, int B,
                int q_len, int H, int num_shards, int page_size, float sm_scale,
-               int num_splits, const int32_t* split_pages, float* O_part,
+               int num_splits, const int32_t* split_pages,
+               const int32_t* work, int num_work, float* O_part,
                float* LSE_part, int32_t* counters, void* out, float* lse_out,
                int* status, mla_stream_t stream) {
   DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
@@ -396,7 +524,11 @@ int mla_decode(const void* q_nope_absorbed, const void* q_rope,
                B,               q_len,     H,        num_shards, page_size,
                sm_scale,        num_splits, split_pages, O_part,  LSE_part,  status,
                (cudaStream_t)stream};
+  a.work = work;
+  a.num_work = num_work;
   int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  rc = check_work(a);
   if (rc != MLA_OK) return rc;
   if (!counters || !out)
     return fail(MLA_ERR_INVALID_ARG, "counters and out are required");

@@ -55,6 +55,10 @@ struct DecodeArgs {
   void* out = nullptr;
   float* lse_out = nullptr;
   int32_t* counters = nullptr;
+  // Launch order of the work units (ids (s * V + v) * U + u) or NULL for
+  // increasing ids; num_work = V * num_splits * U (checked by check_work).
+  const int32_t* work = nullptr;
+  int num_work = 0;
 };
 
 // Pages [p0, p1) of split s of a request with P pages.  With a split table
@@ -79,6 +83,10 @@ __host__ __device__ inline void split_page_range(const int32_t* row, int S,
 // Host checks common to every partial-decode launch; returns MLA_OK or an
 // error code with the message set.
 int check_decode_args(const DecodeArgs& a);
+
+// Host checks of a work list against the tensor-core kernel that serves
+// a.kv_dtype (rows per unit 256 for BF16, 128 for FP8).
+int check_work(const DecodeArgs& a);
 
 // Launchers (defined next to their kernels).
 int launch_simt(const DecodeArgs& a);

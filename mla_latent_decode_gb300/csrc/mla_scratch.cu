@@ -70,8 +70,9 @@ int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
                        const int32_t* seq_lens, const int32_t* kv_limit, int B,
                        int q_len, int H, int num_shards, int page_size,
                        float sm_scale, int num_splits,
-                       const int32_t* split_pages, void* out, float* lse_out,
-                       int* status, mla_stream_t stream) {
+                       const int32_t* split_pages, const int32_t* work,
+                       int num_work, void* out, float* lse_out, int* status,
+                       mla_stream_t stream) {
   // The size limit is checked before anything else, so an oversized request
   // fails here whatever else is wrong with it.
   const int64_t need = mla_scratch_bytes(B, q_len, H, num_shards, num_splits);
@@ -92,7 +93,11 @@ int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
                B,               q_len,     H,        num_shards, page_size,
                sm_scale,        num_splits, split_pages, placeholder,
                placeholder,     status,    (cudaStream_t)stream};
+  a.work = work;
+  a.num_work = num_work;
   int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  rc = check_work(a);
   if (rc != MLA_OK) return rc;
   if (!out) return fail(MLA_ERR_INVALID_ARG, "out is required");
   void* base = nullptr;
@@ -109,8 +114,8 @@ int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
   return mla_decode(q_nope_absorbed, q_rope, kv_pages, kv_scale, kv_dtype,
                     num_slots, req_to_token, r2t_stride, seq_lens, kv_limit, B,
                     q_len, H, num_shards, page_size, sm_scale, num_splits,
-                    split_pages, O_part, LSE_part, counters, out, lse_out,
-                    status, stream);
+                    split_pages, work, num_work, O_part, LSE_part, counters, out,
+                    lse_out, status, stream);
 }
 
 }  // extern "C"

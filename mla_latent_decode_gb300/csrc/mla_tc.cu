@@ -117,6 +117,7 @@ struct TcParams {
   const int32_t* seq_lens;
   const int32_t* kv_limit;
   const int32_t* split_pages;  // [V, num_splits + 1] page boundaries or NULL
+  const int32_t* work;         // unit ids in launch order or NULL
   int B, q_len, H, V, num_splits, U;  // U = row pairs (256 rows) per request
   float scale_log2;        // sm_scale * log2(e)
   float* O_part;
@@ -202,18 +203,27 @@ __device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
     if (c != rank) st_cluster_u32(mapa(smem_u32(&s.abort_flag), c), 1u);
 }
 
-// Work of one cluster: (split, virtual request v, row pair u), launched in
-// that order (split slowest: the planner's list schedule puts every
-// request's first part before any second part); this CTA's row group is
-// 2u + (rank & 1).
+// Work of one cluster: unit id (split, virtual request v, row pair u) =
+// (split * V + v) * U + u, the cluster's index or, with a work list, the
+// list's entry at that index (an entry that names no unit: skip); this
+// CTA's row group is 2u + (rank & 1).
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
   int64_t L, p0;
 };
 
-__device__ __forceinline__ Work unit_work(const TcParams& p, uint32_t rank) {
+// The cluster's unit id, or -1 for a work-list entry outside [0, units).
+__device__ __forceinline__ int cluster_unit(const TcParams& p) {
+  const int k = blockIdx.x / kCtas;
+  if (!p.work) return k;
+  const int unit = p.work[k];
+  return unit < 0 || (int64_t)unit >= (int64_t)p.V * p.num_splits * p.U ? -1
+                                                                         : unit;
+}
+
+__device__ __forceinline__ Work unit_work(const TcParams& p, int unit,
+                                          uint32_t rank) {
   Work w;
-  int unit = blockIdx.x / kCtas;
   const int u = unit % p.U;
   unit /= p.U;
   w.v = unit % p.V;
@@ -839,7 +849,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
-  const Work w = unit_work(p, rank);
+  if (cluster_unit(p) < 0) {  // every CTA of the cluster read the same entry
+    if (rank == 0 && threadIdx.x == 0 && p.status)
+      atomicOr(p.status, MLA_STATUS_BAD_WORK);
+    return;
+  }
+  const Work w = unit_work(p, cluster_unit(p), rank);
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -891,9 +906,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
   // CTAs have written their part; the cluster whose arrival completes the
   // count (shards x splits) resets it and merges the unit's rows, every part
   // being in memory by then.  No cluster waits for another.
-  const int unit_u = (int)(blockIdx.x / kCtas) % p.U;
   auto fused_arrival = [&]() {
     if (rank == 0 && threadIdx.x == 0) {
+      const int unit_u = w.r_base / MLA_ROWS_PER_UNIT;
       int* c = p.counters + (int64_t)w.b * p.U + unit_u;
       const int total = p.num_splits * (p.V / p.B);
       const bool last = atom_add_acq_rel_gpu(c, 1) == total - 1;
@@ -906,7 +921,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     if (!*reinterpret_cast<volatile int*>(&s.ctl_last)) return;
     __threadfence();
     const int R = p.q_len * p.H;
-    const int r0 = unit_u * MLA_ROWS_PER_UNIT;
+    const int r0 = w.r_base / MLA_ROWS_PER_UNIT * MLA_ROWS_PER_UNIT;
     const int n = min(MLA_ROWS_PER_UNIT, R - r0);
     const int64_t rows = (int64_t)p.B * R;
     const int P = p.num_splits * (p.V / p.B);
@@ -996,6 +1011,7 @@ int launch_tc(const DecodeArgs& a) {
   p.seq_lens = a.seq_lens;
   p.kv_limit = a.kv_limit;
   p.split_pages = a.split_pages;
+  p.work = a.work;
   p.B = a.B;
   p.q_len = a.q_len;
   p.H = a.H;

@@ -133,6 +133,8 @@ struct TcParams {
   const int32_t* seq_lens;
   const int32_t* kv_limit;
   const int32_t* split_pages;  // [V, num_splits + 1] page boundaries or NULL
+  const int32_t* work;         // unit ids in launch order or NULL
+  int units;                   // V * num_splits * G
   int B, q_len, H, V, num_splits, G;
   float scale_log2;        // sm_scale * log2(e)
   float* O_part;
@@ -292,10 +294,18 @@ struct Work {
   bool tail;  // the split's last page is the request's partial last page
 };
 
-__device__ __forceinline__ Work pair_work(const TcParams& p) {
+// The pair's unit id (split, virtual request v, row group g) = (split * V +
+// v) * G + g: the pair's index or, with a work list, the list's entry there;
+// -1 for an entry outside [0, units).
+__device__ __forceinline__ int pair_unit(const TcParams& p) {
+  const int k = blockIdx.x >> 1;
+  if (!p.work) return k;
+  const int unit = p.work[k];
+  return (unsigned)unit < (unsigned)p.units ? unit : -1;
+}
+
+__device__ __forceinline__ Work pair_work(const TcParams& p, int pair) {
   Work w;
-  // launch order (split, virtual request v, row group g), split slowest
-  int pair = blockIdx.x >> 1;
   const int g = pair % p.G;
   pair /= p.G;
   w.v = pair % p.V;
@@ -1074,7 +1084,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
-  const Work w = pair_work(p);
+  const int unit = pair_unit(p);
+  if (unit < 0) {  // both CTAs of the pair read the same entry
+    if (rank == 0 && threadIdx.x == 0 && p.status)
+      atomicOr(p.status, MLA_STATUS_BAD_WORK);
+    return;
+  }
+  const Work w = pair_work(p, unit);
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -1130,9 +1146,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // CTAs have written their part; the pair whose arrival completes the count
   // (shards x splits) resets it and merges the group's rows, every part being
   // in memory by then.  No pair waits for another.
-  const int group = (int)(blockIdx.x >> 1) % p.G;
   auto fused_arrival = [&]() {
     if (rank == 0 && threadIdx.x == 0) {
+      const int group = w.r_base / kRows;
       int* c = p.counters + (int64_t)w.b * p.G + group;
       const int total = p.num_splits * (p.V / p.B);
       const bool last = atom_add_acq_rel_gpu(c, 1) == total - 1;
@@ -1145,7 +1161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!*reinterpret_cast<volatile int*>(&s.ctl_last)) return;
     __threadfence();
     const int R = p.q_len * p.H;
-    const int r0 = group * kRows;
+    const int r0 = w.r_base;
     const int n = min(kRows, R - r0);
     const int64_t rows = (int64_t)p.B * R;
     const int P = p.num_splits * (p.V / p.B);
@@ -1236,6 +1252,7 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.seq_lens = a.seq_lens;
   p.kv_limit = a.kv_limit;
   p.split_pages = a.split_pages;
+  p.work = a.work;
   p.B = a.B;
   p.q_len = a.q_len;
   p.H = a.H;
@@ -1251,6 +1268,7 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.counters = a.counters;
   const int64_t pairs = (int64_t)p.V * p.num_splits * p.G;
   if (pairs * 2 > 0x7fffffff) return fail(MLA_ERR_INVALID_ARG, "grid too large");
+  p.units = (int)pairs;
   CUtensorMap map, rope_map;
   int rc = make_kv_tensor_map(&map, a.kv, MLA_KV_FP8_E4M3, a.num_slots);
   if (rc != MLA_OK) return rc;

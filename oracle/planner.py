@@ -103,30 +103,51 @@ N_CAPS = 32        # cap candidates b = ceil(Pmax * k / 32), k = 1..32
 EMPTY_COST = 1.0   # an empty work unit
 
 
-def parts_makespan(P: Sequence[int], U: int, S: int, bnd: List[List[int]],
-                   slots: int, c0: float):
-    """List-scheduling makespan of a per-request split schedule in launch
-    order (part s of every request before part s + 1, row units innermost);
-    a unit costs its pages + c0, an empty one EMPTY_COST.  Returns
-    (makespan, total cost)."""
-    costs = []
+def parts_units(P: Sequence[int], U: int, S: int, bnd: List[List[int]],
+                c0: float):
+    """Every work unit of a per-request split schedule as (id, cost), id =
+    (s * V + v) * U + u in increasing order (part s of every request before
+    part s + 1, row units innermost); a unit costs its pages + c0, an empty
+    one EMPTY_COST."""
+    V = len(P)
+    units = []
     for s in range(S):
-        for v in range(len(P)):
+        for v in range(V):
             pages = bnd[v][s + 1] - bnd[v][s]
             c = float(pages) + c0 if pages > 0 else EMPTY_COST
-            costs.extend([c] * U)
+            for u in range(U):
+                units.append(((s * V + v) * U + u, c))
+    return units
+
+
+def lpt_order(units):
+    """Longest processing time first: by decreasing cost, equal costs by
+    increasing id."""
+    return sorted(units, key=lambda iu: (-iu[1], iu[0]))
+
+
+def parts_makespan(P: Sequence[int], U: int, S: int, bnd: List[List[int]],
+                   slots: int, c0: float, lpt: bool = False):
+    """List-scheduling makespan of a per-request split schedule, its units
+    taken in launch order (increasing id) or, with lpt, longest first.
+    Returns (makespan, total cost)."""
+    units = parts_units(P, U, S, bnd, c0)
+    if lpt:
+        units = lpt_order(units)
+    costs = [c for _, c in units]
     return makespan(costs, slots), sum(costs)
 
 
 def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
                s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
                lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT,
-               page: int = 64):
+               page: int = 64, lpt: bool = False):
     """Brute force over three candidate families (uniform deals for
     S = 1..s_max; first part capped at b, the rest dealt over S - 1 parts for
     S = 2..max_parts; equal chunks of ceil(Pmax / S) pages for S =
     2..max_parts), scored by makespan + lam * S * rows / 1024, first of equal
-    scores kept.  Returns (S, boundaries [V][S+1], wave_eff, makespan)."""
+    scores kept; the makespan takes the units in launch order, or longest
+    first with lpt.  Returns (S, boundaries [V][S+1], wave_eff, makespan)."""
     U = -(-H * q_len // rows_per_unit)
     rows = len(seq_lens) * q_len * H
     P = [-(-max(L, 0) // page) for L in seq_lens]
@@ -135,7 +156,7 @@ def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
 
     def consider(S, bnd):
         nonlocal best
-        ms, tot = parts_makespan(P, U, S, bnd, slots, c0)
+        ms, tot = parts_makespan(P, U, S, bnd, slots, c0, lpt)
         J = ms + lam * S * rows / 1024.0
         if best is None or J < best[0] - 1e-9:
             best = (J, S, bnd, tot / (slots * ms) if ms > 0 else 1.0, ms)
@@ -162,3 +183,18 @@ def plan_parts(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
             continue
         consider(S, [[min(p, m * u) for m in range(S + 1)] for p in P])
     return best[1], best[2], best[3], best[4]
+
+
+def plan_sched(seq_lens: Sequence[int], H: int, q_len: int, slots: int,
+               s_max: int = 64, max_parts: int = 8, c0: float = 32.0,
+               lam: float = 1.0, rows_per_unit: int = ROWS_PER_UNIT,
+               page: int = 64):
+    """The work-balanced scheduler: plan_parts scored with the units taken
+    longest first, and that order as the work list.  Returns (S, boundaries
+    [V][S+1], work ids in launch order, wave_eff, makespan)."""
+    S, bnd, eff, ms = plan_parts(seq_lens, H, q_len, slots, s_max, max_parts,
+                                 c0, lam, rows_per_unit, page, lpt=True)
+    U = -(-H * q_len // rows_per_unit)
+    P = [-(-max(L, 0) // page) for L in seq_lens]
+    work = [i for i, _ in lpt_order(parts_units(P, U, S, bnd, c0))]
+    return S, bnd, work, eff, ms

@@ -112,14 +112,15 @@ def test_page_table_check(lib):
 def _call_partial(lib, **over):
     a = dict(qn=16, qr=16, kv=16, ks=None, dt=0, ns=4096, r2t=16, st=64, sl=16,
              kl=None, B=1, q=5, H=96, shards=1, ps=64, scale=0.07, S=1, O=16,
-             L=16, status=None)
+             L=16, status=None, work=None, nw=0)
     a.update(over)
     p = lambda x: None if x is None else ctypes.c_void_p(x)
     return lib.mla_decode_partial(p(a["qn"]), p(a["qr"]), p(a["kv"]), p(a["ks"]),
                                   a["dt"], a["ns"], p(a["r2t"]), a["st"], p(a["sl"]),
                                   p(a["kl"]), a["B"], a["q"], a["H"], a["shards"],
-                                  a["ps"], a["scale"], a["S"], None, p(a["O"]),
-                                  p(a["L"]), p(a["status"]), None)
+                                  a["ps"], a["scale"], a["S"], None, p(a["work"]),
+                                  a["nw"], p(a["O"]), p(a["L"]), p(a["status"]),
+                                  None)
 
 
 def test_bad_arguments_are_rejected_on_the_host(lib):
@@ -131,6 +132,11 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert _call_partial(lib, ns=10) == -1         # pool smaller than a page
     assert _call_partial(lib, kv=24) == -3         # misaligned KV
     assert _call_partial(lib, scale=float("nan")) == -1
+    # a work list must name every unit: 1 request x 1 split x 2 row units
+    assert _call_partial(lib, work=16, nw=1) == -1
+    assert _call_partial(lib, work=16, nw=3) == -1
+    assert _call_partial(lib, work=None, nw=2) == -1
+    assert _call_partial(lib, work=18, nw=2) == -3     # misaligned work list
     assert b"page_size" in lib.mla_last_error_string() or True
     assert lib.mla_lse_combine(None, None, 1, 1, None, None, None) == -1
     assert lib.mla_lse_combine(ctypes.c_void_p(16), ctypes.c_void_p(16), 0, 1,
@@ -174,3 +180,43 @@ def test_parts_planner_fills_idle_slots_at_dp16():
     assert S_u == 1 and ms_u == 1563 + 32
     assert S_p >= 2 and ms_p < 0.93 * ms_u
     assert len({tuple(r) for r in bnd}) == 1   # same cut for every request
+
+
+def test_sched_planner_matches_reference(lib):
+    """mla_plan_sched_ex against oracle/planner.plan_sched: the same parts,
+    the same longest-first work list and the same modelled makespan."""
+    rng = random.Random(13)
+    cases = [([100_000] * 16, 96, 5, 36, 256), ([100_000] * 4, 96, 5, 36, 256),
+             ([256], 16, 1, 36, 256),
+             ([1198, 152649, 2686, 60048, 10681, 170646, 4569], 96, 5, 76, 128)]
+    for _ in range(12):
+        V = rng.randint(1, 12)
+        lens = [int(np.exp(rng.uniform(np.log(5), np.log(200_000)))) for _ in range(V)]
+        cases.append((lens, rng.choice([16, 96]), rng.randint(1, 5),
+                      rng.choice([7, 36, 76]), rng.choice([128, 256])))
+    for lens, H, q, slots, rpu in cases:
+        c0, lam = rng.choice([(32.0, 1.0), (4.0, 1.0), (0.0, 0.5)])
+        S, bnd, work, eff, ms = mla.plan_sched_ex(lens, q, H, slots, 16, 4, c0,
+                                                  lam, rows_per_unit=rpu)
+        S2, bnd2, work2, eff2, ms2 = ref.plan_sched(lens, H, q, slots, 16, 4, c0,
+                                                    lam, rows_per_unit=rpu)
+        assert (S, ms) == (S2, ms2), (lens[:4], H, q, slots, rpu)
+        assert bnd.tolist() == bnd2
+        assert work.tolist() == work2
+        assert eff == pytest.approx(eff2, rel=1e-6)
+
+
+def test_sched_planner_defaults_and_capacity(lib):
+    lens = [3000, 90_000, 700]
+    for kv, U in (("bf16", 2), ("fp8_e4m3", 4)):
+        S, bnd, work, eff = mla.plan_sched(3, 5, 96, lens, num_sms=152, kv_dtype=kv)
+        assert sorted(work.tolist()) == list(range(3 * S * U))
+        assert 0 < eff <= 1
+    # too small a work buffer: an error, nothing written
+    arr = (ctypes.c_int32 * 3)(*lens)
+    bnd = (ctypes.c_int32 * (3 * 17))()
+    work = (ctypes.c_int32 * 1)()
+    S, n = ctypes.c_int(), ctypes.c_int64()
+    rc = lib.mla_plan_sched_ex(3, 5, 96, 256, arr, 38, 16, 4, 32.0, 1.0, bnd,
+                               ctypes.byref(S), work, 1, ctypes.byref(n), None, None)
+    assert rc == -1 and b"capacity" in lib.mla_last_error_string()

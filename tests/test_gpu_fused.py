@@ -135,6 +135,6 @@ def test_fused_rejects_missing_outputs():
     rc = lib.mla_decode(p(batch.q_nope), p(batch.q_rope), p(batch.kv), None, 0,
                         batch.kv.shape[0], p(batch.req_to_token),
                         batch.req_to_token.stride(0), p(batch.seq_lens), None, 1,
-                        1, 16, 1, 64, wl.sm_scale, 1, None, p(O_part), p(LSE_part),
-                        None, None, None, None, mla._stream(None))
+                        1, 16, 1, 64, wl.sm_scale, 1, None, None, 0, p(O_part),
+                        p(LSE_part), None, None, None, None, mla._stream(None))
     assert rc == -1

@@ -48,14 +48,14 @@ def test_scratch_limit_is_checked_first(lib):
     assert mla.scratch_bytes(B, q, H, 1, S) > SCRATCH_BYTES
     rc = lib.mla_decode_scratch(None, None, None, None, 0, 1 << 20, None, 64,
                                 None, None, B, q, H, 1, 64, 0.07, S, None, None,
-                                None, None, None)
+                                0, None, None, None, None)
     assert rc == MLA_ERR_SCRATCH
     msg = lib.mla_last_error_string().decode()
     assert str(mla.scratch_bytes(B, q, H, 1, S)) in msg and str(SCRATCH_BYTES) in msg
     # within the limit, the same NULL pointers are an ordinary argument error
     rc = lib.mla_decode_scratch(None, None, None, None, 0, 1 << 20, None, 64,
                                 None, None, 1, 1, 16, 1, 64, 0.07, 1, None, None,
-                                None, None, None)
+                                0, None, None, None, None)
     assert rc == -1
 
 
