@@ -461,19 +461,24 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   // Q row: nope part -> TMEM columns [0, 256) (column c holds elements 2c,
   // 2c+1), rope part -> shared memory in the K-major 128-B swizzled layout.
   if (g == 0) {
+    // Two batches of four 32-column chunks: 512 bytes of the row in flight.
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t v[32];
-      const uint4* src = p.q_nope + qrow * 64 + c * 8;
+    for (int c0 = 0; c0 < 8; c0 += 4) {
+      uint32_t v[4][32];
+      const uint4* src = p.q_nope + qrow * 64 + c0 * 8;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 x = row_ok ? src[k] : make_uint4(0, 0, 0, 0);
-        v[4 * k] = x.x;
-        v[4 * k + 1] = x.y;
-        v[4 * k + 2] = x.z;
-        v[4 * k + 3] = x.w;
-      }
-      tmem_st32(tmem + lane_base + 32u * c, v);
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 x = row_ok ? src[cc * 8 + k] : make_uint4(0, 0, 0, 0);
+          v[cc][4 * k] = x.x;
+          v[cc][4 * k + 1] = x.y;
+          v[cc][4 * k + 2] = x.z;
+          v[cc][4 * k + 3] = x.w;
+        }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        tmem_st32(tmem + lane_base + 32u * (c0 + cc), v[cc]);
     }
     tmem_wait_st();
   } else {
@@ -775,8 +780,11 @@ __device__ __forceinline__ void relay_o(Smem& s, const TcParams& p,
 // Warps 4..7 of each O-CTA, thread = row r of this CTA's row group.  A
 // drain event (every earlier pair MMA complete) either asks for a rescale of
 // the rows whose running max rose (factors in the P slot that triggered it)
-// or, the last one, for the epilogue: O_part = O / l.
+// or, the last one, for the epilogue: O_part = O / l, written by TMA stores
+// (each warp stages its 32 rows x 32 values at a time in the then idle ring,
+// 128-byte swizzled, two buffers per warp).
 __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
+                                                  const CUtensorMap* o_map,
                                                   const Work& w, uint32_t tmem,
                                                   uint32_t rank, int warp,
                                                   int lane) {
@@ -817,32 +825,48 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
   }
   tc_fence_after();
   const float inv = s.fin[r];
-  const bool row_ok = r < w.nrows;
-  const int64_t rows = (int64_t)p.B * p.q_len * p.H;
-  const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-  float* dst = p.O_part +
-               (part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r) *
-                   MLA_VALUE_DIM;
+  // Box (32 values, 32 rows) of the [parts * B, q_len * H, 512] map: this
+  // warp's rows start at y; rows past q_len * H are clipped by the TMA unit
+  // (a box wholly past them is skipped).
+  const int y = w.r_base + quad * 32;
+  const int z = ((int)w.split * (p.V / p.B) + w.shard) * p.B + w.b;
+  const bool store = y < p.q_len * p.H;
+  uint8_t* const stage = s.ring[2 * quad];  // 8 KB: two 4-KB boxes
 #pragma unroll 1
-  for (int c0 = 0; c0 < MLA_VALUE_DIM; c0 += 32) {
+  for (int k = 0; k < MLA_VALUE_DIM / 32; ++k) {
     uint32_t v[32];
-    tmem_ld32(tmem + lane_base + c0, v);
+    tmem_ld32(tmem + lane_base + 32u * k, v);
     tmem_wait_ld();
-    if (row_ok) {
-      float4* d4 = reinterpret_cast<float4*>(dst + c0);
+    uint8_t* buf = stage + (k & 1) * 4096;
+    if (k >= 2) {  // the store issued from this buffer has read it
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+    }
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv,
-                            __uint_as_float(v[4 * e + 1]) * inv,
-                            __uint_as_float(v[4 * e + 2]) * inv,
-                            __uint_as_float(v[4 * e + 3]) * inv);
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<float4*>(buf + box_chunk_offset(lane, e)) =
+          make_float4(__uint_as_float(v[4 * e]) * inv,
+                      __uint_as_float(v[4 * e + 1]) * inv,
+                      __uint_as_float(v[4 * e + 2]) * inv,
+                      __uint_as_float(v[4 * e + 3]) * inv);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && store) {
+      tma_store_3d(o_map, smem_u32(buf), 32 * k, y, z);
+      bulk_commit_group();
     }
   }
+  if (lane == 0) {
+    bulk_wait_group<0>();
+    fence_proxy_async();
+  }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------- kernel ----
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
+                          const __grid_constant__ CUtensorMap o_map,
                           const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -855,6 +879,20 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
   const Work w = unit_work(p, cluster_unit(p), rank);
+  // Start this CTA's query rows on their way to L2 before the set-up (the
+  // softmax warpgroups move them to TMEM and shared memory right after it).
+  if (rank < 2 && warp >= 4 && w.npages > 0) {
+    const int r = (warp & 3) * 32 + lane;
+    if (r < w.nrows) {
+      const int64_t qrow = (int64_t)w.b * p.q_len * p.H + w.r_base + r;
+      if (warp < 8) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) prefetch_l2(p.q_nope + qrow * 64 + c * 8);
+      } else {
+        prefetch_l2(p.q_rope + qrow * 8);
+      }
+    }
+  }
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -887,6 +925,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
+    if (rank >= 2) prefetch_tmap(&o_map);
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -976,7 +1015,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4 && warp < 8) {
-      correct_and_store(s, p, w, tmem, rank, warp, lane);
+      correct_and_store(s, p, &o_map, w, tmem, rank, warp, lane);
     }
   } else if (warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0 (O-CTAs), LSE = -inf (S-CTAs).
@@ -1028,15 +1067,17 @@ int launch_tc(const DecodeArgs& a) {
   const int64_t units = (int64_t)p.V * p.num_splits * p.U;
   if (units * kCtas > 0x7fffffff)
     return fail(MLA_ERR_INVALID_ARG, "grid too large");
-  CUtensorMap map;
+  CUtensorMap map, o_map;
   int rc = make_kv_tensor_map(&map, a.kv, a.kv_dtype, a.num_slots);
+  if (rc != MLA_OK) return rc;
+  rc = make_o_part_map(&o_map, a);
   if (rc != MLA_OK) return rc;
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc)");
   mla_partial_tc_kernel<<<(unsigned)(units * kCtas), kThreads, kSmemBytes,
-                          a.stream>>>(map, p);
+                          a.stream>>>(map, o_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_kernel");
   return MLA_OK;
