@@ -71,36 +71,6 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
   return MLA_OK;
 }
 
-int make_tensor_map_f32_3d(CUtensorMap* map, const void* base,
-                           const uint64_t dims[3], const uint64_t strides[2],
-                           const uint32_t box[3]) {
-  auto fn = encode_fn();
-  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-  cuuint64_t st[2] = {strides[0], strides[1]};
-  cuuint32_t bx[3] = {box[0], box[1], box[2]};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                  const_cast<void*>(base), d, st, bx, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled (3-D f32) failed (%d)",
-                (int)r);
-  return MLA_OK;
-}
-
-int make_o_part_map(CUtensorMap* map, const DecodeArgs& a) {
-  const uint64_t R = (uint64_t)a.q_len * a.H;
-  const uint64_t dims[3] = {(uint64_t)MLA_VALUE_DIM, R,
-                            (uint64_t)a.num_splits * a.num_shards * a.B};
-  const uint64_t strides[2] = {(uint64_t)MLA_VALUE_DIM * 4,
-                               R * MLA_VALUE_DIM * 4};
-  const uint32_t box[3] = {32, (uint32_t)(R < 32 ? R : 32), 1};
-  return make_tensor_map_f32_3d(map, a.O_part, dims, strides, box);
-}
-
 int make_kv_tensor_map_fp8_rope(CUtensorMap* map, const void* kv,
                                 int64_t num_slots) {
   auto fn = encode_fn();

@@ -96,7 +96,9 @@ struct __align__(1024) Smem {
   uint64_t tail_full;       // O-CTAs: the last, partial page landed here
   uint64_t tail_ready;      // rank 2: both halves of that page sanitised
   uint64_t fin_full;        // O-CTAs: 1/l of every row arrived
+  uint64_t epi_go;          // O-CTAs: the epilogue may read O (warps 4-7)
   uint64_t qready;          // rank 0: both S-CTAs' Q rows are in place
+  uint64_t qbar;            // S-CTAs: a pass of query boxes landed
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -123,6 +125,7 @@ struct TcParams {
   float* O_part;
   float* LSE_part;
   int* status;
+  int q_box_rows;          // rows of a query TMA box: min(128, B * q_len * H)
   __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
   float* lse_out;
   int* counters;
@@ -441,6 +444,8 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
 // the pair MMA fills from both CTAs' halves of the tile).  Thread = query
 // row r (TMEM lane) of this CTA's row group.
 __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
+                                        const CUtensorMap* qn_map,
+                                        const CUtensorMap* qr_map,
                                         const Work& w, uint32_t tmem,
                                         uint32_t rank, int warp, int lane) {
   const int g = (warp - 4) >> 2;
@@ -458,37 +463,54 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   }
   const int64_t qrow = (int64_t)w.b * p.q_len * p.H + rr;
 
-  // Q row: nope part -> TMEM columns [0, 256) (column c holds elements 2c,
-  // 2c+1), rope part -> shared memory in the K-major 128-B swizzled layout.
-  if (g == 0) {
-    // Two batches of four 32-column chunks: 512 bytes of the row in flight.
-#pragma unroll 1
-    for (int c0 = 0; c0 < 8; c0 += 4) {
-      uint32_t v[4][32];
-      const uint4* src = p.q_nope + qrow * 64 + c0 * 8;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 x = row_ok ? src[cc * 8 + k] : make_uint4(0, 0, 0, 0);
-          v[cc][4 * k] = x.x;
-          v[cc][4 * k + 1] = x.y;
-          v[cc][4 * k + 2] = x.z;
-          v[cc][4 * k + 3] = x.w;
+  // Q rows by TMA (boxes of 64 values x 128 rows, 128-byte swizzle, rows
+  // from this CTA's first): the rope part straight into its MMA operand
+  // buffer; the nope part in two passes of four boxes through the P slots,
+  // idle until the first S tile, from which warpgroup 0 moves row r to TMEM
+  // lane r (columns [0, 256), column c holding elements 2c, 2c+1).
+  {
+    const int qy = w.b * p.q_len * p.H + w.r_base;
+    const uint32_t box = (uint32_t)p.q_box_rows * 128u;
+    const uint32_t qbar = smem_u32(&s.qbar);
+    if (warp == 4 && lane == 0) {
+      mbar_arrive_expect_tx(qbar, 5 * box);
+      for (int k = 0; k < 4; ++k)
+        tma_load_3d(smem_u32(s.pslot[k]), qn_map, qbar, 64 * k, qy, 0);
+      tma_load_3d(smem_u32(s.qrope), qr_map, qbar, 0, qy, 0);
+    }
+    bool qok = mbar_wait(qbar, 0, &s.abort_flag);
+    if (g == 0) {
+      for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 1) {
+          named_bar_sync(2, 128);  // every row of the first pass read
+          if (warp == 4 && lane == 0) {
+            mbar_arrive_expect_tx(qbar, 4 * box);
+            for (int k = 0; k < 4; ++k)
+              tma_load_3d(smem_u32(s.pslot[k]), qn_map, qbar, 64 * (4 + k), qy,
+                          0);
+          }
+          qok = qok && mbar_wait(qbar, 1, &s.abort_flag);
         }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        tmem_st32(tmem + lane_base + 32u * (c0 + cc), v[cc]);
-    }
-    tmem_wait_st();
-  } else {
+        for (int k = 0; k < 4; ++k) {
+          uint32_t v[32];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 x = row_ok ? p.q_rope[qrow * 8 + k] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(s.qrope + (r >> 3) * 1024 +
-                                box_chunk_offset(r & 7, k)) = x;
+          for (int e = 0; e < 8; ++e) {
+            const uint4 x =
+                row_ok && qok ? *reinterpret_cast<const uint4*>(
+                                    s.pslot[k] + box_chunk_offset(r, e))
+                              : make_uint4(0, 0, 0, 0);
+            v[4 * e] = x.x;
+            v[4 * e + 1] = x.y;
+            v[4 * e + 2] = x.z;
+            v[4 * e + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_base + 32u * (4 * pass + k), v);
+        }
+      }
+      tmem_wait_st();
     }
-    fence_proxy_async_smem();
+    if (!__all_sync(kFull, qok) && lane == 0) signal_abort(s, p, rank);
   }
   tc_fence_before();
   __syncwarp();
@@ -776,15 +798,70 @@ __device__ __forceinline__ void relay_o(Smem& s, const TcParams& p,
   }
 }
 
+// ------------------------------------------------ O-CTA: epilogue stores ----
+// O_part = O / l for this thread's row r (TMEM lane) over value columns
+// [256 half, +256), 32 at a time: the warp stages its 32 rows x 32 values
+// in 4 KB of the then idle ring (row r at 128 r bytes, 16-byte chunk e at
+// position e ^ (r % 8), so neither the writes nor the reads below conflict)
+// and reads them back four rows per instruction, lane l taking chunk l % 8
+// of row 4i + l / 8: every store instruction writes four full 128-byte
+// lines of O_part.
+__device__ __forceinline__ void store_o_rows(Smem& s, const TcParams& p,
+                                             const Work& w, uint32_t tmem,
+                                             int warp, int lane, int half) {
+  const int quad = warp & 3;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  const float inv = s.fin[quad * 32 + lane];
+  const int64_t rows = (int64_t)p.B * p.q_len * p.H;
+  const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
+  float* const dst0 = p.O_part + (part * rows + (int64_t)w.b * p.q_len * p.H +
+                                  w.r_base + quad * 32) * MLA_VALUE_DIM;
+  const int nvalid = w.nrows - quad * 32;  // rows of this warp in range
+  uint8_t* const buf = s.ring[warp - 4];
+#pragma unroll 1
+  for (int k = 0; k < 8; ++k) {
+    const int c0 = 256 * half + 32 * k;
+    uint32_t v[32];
+    tmem_ld32(tmem + lane_base + c0, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<float4*>(buf + box_chunk_offset(lane, e)) =
+          make_float4(__uint_as_float(v[4 * e]) * inv,
+                      __uint_as_float(v[4 * e + 1]) * inv,
+                      __uint_as_float(v[4 * e + 2]) * inv,
+                      __uint_as_float(v[4 * e + 3]) * inv);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), e = lane & 7;
+      const float4 f =
+          *reinterpret_cast<const float4*>(buf + box_chunk_offset(rr, e));
+      if (rr < nvalid)
+        *reinterpret_cast<float4*>(dst0 + (int64_t)rr * MLA_VALUE_DIM + c0 +
+                                   4 * e) = f;
+    }
+    __syncwarp();  // every lane read the box before it is refilled
+  }
+}
+
+// Warps 8..11 of each O-CTA: the second half of the value columns, once
+// warps 4..7 have seen the last drain and 1/l.
+__device__ __forceinline__ void store_o_upper(Smem& s, const TcParams& p,
+                                              const Work& w, uint32_t tmem,
+                                              int warp, int lane) {
+  if (!mbar_wait(smem_u32(&s.epi_go), 0, &s.abort_flag)) return;
+  tc_fence_after();
+  store_o_rows(s, p, w, tmem, warp, lane, 1);
+}
+
 // ---------------------------------------- O-CTA: correction + epilogue ----
 // Warps 4..7 of each O-CTA, thread = row r of this CTA's row group.  A
 // drain event (every earlier pair MMA complete) either asks for a rescale of
 // the rows whose running max rose (factors in the P slot that triggered it)
-// or, the last one, for the epilogue: O_part = O / l, written by TMA stores
-// (each warp stages its 32 rows x 32 values at a time in the then idle ring,
-// 128-byte swizzled, two buffers per warp).
+// or, the last one, for the epilogue: O_part = O / l over the first half of
+// the value columns (warps 8..11 take the second, after epi_go).
 __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
-                                                  const CUtensorMap* o_map,
                                                   const Work& w, uint32_t tmem,
                                                   uint32_t rank, int warp,
                                                   int lane) {
@@ -824,49 +901,16 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
     return;
   }
   tc_fence_after();
-  const float inv = s.fin[r];
-  // Box (32 values, 32 rows) of the [parts * B, q_len * H, 512] map: this
-  // warp's rows start at y; rows past q_len * H are clipped by the TMA unit
-  // (a box wholly past them is skipped).
-  const int y = w.r_base + quad * 32;
-  const int z = ((int)w.split * (p.V / p.B) + w.shard) * p.B + w.b;
-  const bool store = y < p.q_len * p.H;
-  uint8_t* const stage = s.ring[2 * quad];  // 8 KB: two 4-KB boxes
-#pragma unroll 1
-  for (int k = 0; k < MLA_VALUE_DIM / 32; ++k) {
-    uint32_t v[32];
-    tmem_ld32(tmem + lane_base + 32u * k, v);
-    tmem_wait_ld();
-    uint8_t* buf = stage + (k & 1) * 4096;
-    if (k >= 2) {  // the store issued from this buffer has read it
-      if (lane == 0) bulk_wait_group_read<1>();
-      __syncwarp();
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      *reinterpret_cast<float4*>(buf + box_chunk_offset(lane, e)) =
-          make_float4(__uint_as_float(v[4 * e]) * inv,
-                      __uint_as_float(v[4 * e + 1]) * inv,
-                      __uint_as_float(v[4 * e + 2]) * inv,
-                      __uint_as_float(v[4 * e + 3]) * inv);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && store) {
-      tma_store_3d(o_map, smem_u32(buf), 32 * k, y, z);
-      bulk_commit_group();
-    }
-  }
-  if (lane == 0) {
-    bulk_wait_group<0>();
-    fence_proxy_async();
-  }
   __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&s.epi_go));
+  store_o_rows(s, p, w, tmem, warp, lane, 0);
 }
 
 // ------------------------------------------------------------- kernel ----
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
-                          const __grid_constant__ CUtensorMap o_map,
+                          const __grid_constant__ CUtensorMap qn_map,
+                          const __grid_constant__ CUtensorMap qr_map,
                           const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -879,20 +923,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
   const Work w = unit_work(p, cluster_unit(p), rank);
-  // Start this CTA's query rows on their way to L2 before the set-up (the
-  // softmax warpgroups move them to TMEM and shared memory right after it).
-  if (rank < 2 && warp >= 4 && w.npages > 0) {
-    const int r = (warp & 3) * 32 + lane;
-    if (r < w.nrows) {
-      const int64_t qrow = (int64_t)w.b * p.q_len * p.H + w.r_base + r;
-      if (warp < 8) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) prefetch_l2(p.q_nope + qrow * 64 + c * 8);
-      } else {
-        prefetch_l2(p.q_rope + qrow * 8);
-      }
-    }
-  }
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -915,7 +945,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.tail_full), 1);
     mbar_init(smem_u32(&s.tail_ready), 2);
     mbar_init(smem_u32(&s.fin_full), 1);
+    mbar_init(smem_u32(&s.epi_go), 4);
     mbar_init(smem_u32(&s.qready), 16);
+    mbar_init(smem_u32(&s.qbar), 1);
     if (rank >= 2 && w.npages > 0) {
       mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
       // rank 2 also receives rank 1's 16 flag bytes per message
@@ -925,7 +957,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
-    if (rank >= 2) prefetch_tmap(&o_map);
+    if (rank < 2) {
+      prefetch_tmap(&qn_map);
+      prefetch_tmap(&qr_map);
+    }
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -999,7 +1034,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax(s, p, w, tmem, rank, warp, lane);
+    softmax(s, p, &qn_map, &qr_map, w, tmem, rank, warp, lane);
     teardown();
     return;
   }
@@ -1015,7 +1050,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4 && warp < 8) {
-      correct_and_store(s, p, &o_map, w, tmem, rank, warp, lane);
+      correct_and_store(s, p, w, tmem, rank, warp, lane);
+    } else if (warp >= 8) {
+      store_o_upper(s, p, w, tmem, warp, lane);
     }
   } else if (warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0 (O-CTAs), LSE = -inf (S-CTAs).
@@ -1067,17 +1104,30 @@ int launch_tc(const DecodeArgs& a) {
   const int64_t units = (int64_t)p.V * p.num_splits * p.U;
   if (units * kCtas > 0x7fffffff)
     return fail(MLA_ERR_INVALID_ARG, "grid too large");
-  CUtensorMap map, o_map;
+  CUtensorMap map, qn_map, qr_map;
   int rc = make_kv_tensor_map(&map, a.kv, a.kv_dtype, a.num_slots);
   if (rc != MLA_OK) return rc;
-  rc = make_o_part_map(&o_map, a);
-  if (rc != MLA_OK) return rc;
+  {
+    // The query rows as [B * q_len * H, 512] and [.., 64] bf16, boxes of 64
+    // values x min(128, rows) rows.
+    const uint64_t rows = (uint64_t)a.B * a.q_len * a.H;
+    p.q_box_rows = (int)(rows < 128 ? rows : 128);
+    const uint32_t box[3] = {64, (uint32_t)p.q_box_rows, 1};
+    const uint64_t dn[3] = {(uint64_t)MLA_NOPE_DIM, rows, 1};
+    const uint64_t sn[2] = {(uint64_t)MLA_NOPE_DIM * 2, rows * MLA_NOPE_DIM * 2};
+    rc = make_tensor_map_bf16_3d(&qn_map, a.q_nope, dn, sn, box);
+    if (rc != MLA_OK) return rc;
+    const uint64_t dr[3] = {(uint64_t)MLA_ROPE_DIM, rows, 1};
+    const uint64_t sr[2] = {(uint64_t)MLA_ROPE_DIM * 2, rows * MLA_ROPE_DIM * 2};
+    rc = make_tensor_map_bf16_3d(&qr_map, a.q_rope, dr, sr, box);
+    if (rc != MLA_OK) return rc;
+  }
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc)");
   mla_partial_tc_kernel<<<(unsigned)(units * kCtas), kThreads, kSmemBytes,
-                          a.stream>>>(map, o_map, p);
+                          a.stream>>>(map, qn_map, qr_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_kernel");
   return MLA_OK;

@@ -39,17 +39,6 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
                             const uint64_t dims[3], const uint64_t strides[2],
                             const uint32_t box[3]);
 
-// The same for a fp32 3-D array (box[0] * 4 bytes <= 128), used by the
-// decode kernels' TMA stores of O_part.
-int make_tensor_map_f32_3d(CUtensorMap* map, const void* base,
-                           const uint64_t dims[3], const uint64_t strides[2],
-                           const uint32_t box[3]);
-
-// Tensor map of a launch's O_part as [parts * B, q_len * H, 512] fp32 in
-// boxes of 32 values x min(32, q_len * H) rows, the decode kernels' epilogue
-// stores (a request's rows never spill into the next request's).
-int make_o_part_map(CUtensorMap* map, const DecodeArgs& a);
-
 // Tensor map of an E4M3 pool in boxes of 64 rows x 64 bytes with the 64-byte
 // swizzle (4 KB): the RoPE key columns 512..575 of one page, the K-major
 // operand layout the FP8 decode kernel's tensor cores read for those dims.

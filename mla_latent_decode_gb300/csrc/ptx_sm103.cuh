@@ -178,42 +178,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
-// 3-D tiled TMA store of a shared-memory box to global memory, tracked by
-// this thread's bulk async-groups.  Elements outside the tensor are not
-// written; the coordinates must not be negative.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
-                                             int32_t x, int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group "
-      "[%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
-      "r"(src), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-// Close this thread's current bulk async-group.
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until at most N of this thread's bulk async-groups still read their
-// shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until at most N of this thread's bulk async-groups are incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-// Order async-proxy accesses (completed TMA stores) before this thread's
-// later generic-proxy accesses.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async;" ::: "memory");
-}
-// Start the 128-byte line holding `p` on its way to L2.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // peer CTA's shared memory (cluster address), completing on the peer's
 // barrier (cluster address).
