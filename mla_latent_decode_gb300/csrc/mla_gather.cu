@@ -71,6 +71,20 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
   return MLA_OK;
 }
 
+int make_query_maps(CUtensorMap* nope, CUtensorMap* rope, const DecodeArgs& a,
+                    int* box_rows) {
+  const uint64_t rows = (uint64_t)a.B * a.q_len * a.H;
+  *box_rows = (int)(rows < 128 ? rows : 128);
+  const uint32_t box[3] = {64, (uint32_t)*box_rows, 1};
+  const uint64_t dn[3] = {(uint64_t)MLA_NOPE_DIM, rows, 1};
+  const uint64_t sn[2] = {(uint64_t)MLA_NOPE_DIM * 2, rows * MLA_NOPE_DIM * 2};
+  int rc = make_tensor_map_bf16_3d(nope, a.q_nope, dn, sn, box);
+  if (rc != MLA_OK) return rc;
+  const uint64_t dr[3] = {(uint64_t)MLA_ROPE_DIM, rows, 1};
+  const uint64_t sr[2] = {(uint64_t)MLA_ROPE_DIM * 2, rows * MLA_ROPE_DIM * 2};
+  return make_tensor_map_bf16_3d(rope, a.q_rope, dr, sr, box);
+}
+
 int make_kv_tensor_map_fp8_rope(CUtensorMap* map, const void* kv,
                                 int64_t num_slots) {
   auto fn = encode_fn();

@@ -1107,21 +1107,8 @@ int launch_tc(const DecodeArgs& a) {
   CUtensorMap map, qn_map, qr_map;
   int rc = make_kv_tensor_map(&map, a.kv, a.kv_dtype, a.num_slots);
   if (rc != MLA_OK) return rc;
-  {
-    // The query rows as [B * q_len * H, 512] and [.., 64] bf16, boxes of 64
-    // values x min(128, rows) rows.
-    const uint64_t rows = (uint64_t)a.B * a.q_len * a.H;
-    p.q_box_rows = (int)(rows < 128 ? rows : 128);
-    const uint32_t box[3] = {64, (uint32_t)p.q_box_rows, 1};
-    const uint64_t dn[3] = {(uint64_t)MLA_NOPE_DIM, rows, 1};
-    const uint64_t sn[2] = {(uint64_t)MLA_NOPE_DIM * 2, rows * MLA_NOPE_DIM * 2};
-    rc = make_tensor_map_bf16_3d(&qn_map, a.q_nope, dn, sn, box);
-    if (rc != MLA_OK) return rc;
-    const uint64_t dr[3] = {(uint64_t)MLA_ROPE_DIM, rows, 1};
-    const uint64_t sr[2] = {(uint64_t)MLA_ROPE_DIM * 2, rows * MLA_ROPE_DIM * 2};
-    rc = make_tensor_map_bf16_3d(&qr_map, a.q_rope, dr, sr, box);
-    if (rc != MLA_OK) return rc;
-  }
+  rc = make_query_maps(&qn_map, &qr_map, a, &p.q_box_rows);
+  if (rc != MLA_OK) return rc;
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);

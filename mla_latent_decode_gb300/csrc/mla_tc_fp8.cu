@@ -111,6 +111,7 @@ struct __align__(1024) Smem {
   uint64_t packed[kNP];     // O-CTA: P' of slot k split into Phi | Plo
   uint64_t pempty[kNP];
   uint64_t drain, corr_done, fin_full, qready, tail_go, tail_ready;
+  uint64_t qbar;            // S-CTA: the query boxes landed
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -140,6 +141,7 @@ struct TcParams {
   float* O_part;
   float* LSE_part;
   int* status;
+  int q_box_rows;          // rows of a query TMA box: min(128, B * q_len * H)
   __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
   float* lse_out;
   int* counters;
@@ -357,6 +359,9 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   uint32_t stage = 0, phase = 0;
   int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
+  // The ring holds the query rows until every softmax warp has moved them.
+  if (lane == 0 && !mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) ok = false;
+  ok = __shfl_sync(kFull, ok, 0);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles && ok; ++j) {
     const int m0 = j * kTilePages;
@@ -553,7 +558,10 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
 // A = 32 quad + (lane % 16) and B = A + 16 over half the page (lane / 16:
 // tokens 0..31 or 32..63), read with 16x32bx2 loads, so each token scale it
 // loads serves two rows.  Q is prepared with thread = row r: warpgroups 0
-// and 1 split the c_kv dims, warpgroup 2 takes the RoPE dims.
+// and 1 split the c_kv dims, warpgroup 2 takes the RoPE dims.  The query
+// rows arrive by TMA (boxes of 64 values x 128 rows, 128-byte swizzle): the
+// c_kv dims in the ring, idle until the producer starts the KV stream once
+// every softmax warp has passed qready, the RoPE dims in P slot 0.
 __device__ __forceinline__ int64_t visible_count(const TcParams& p,
                                                  const Work& w, int r) {
   // tokens query row r (of the pair's rows) may see; 0 for padding rows
@@ -570,6 +578,8 @@ __device__ __forceinline__ int row_exponent(float amax) {
 }
 
 __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
+                                        const CUtensorMap* qn_map,
+                                        const CUtensorMap* qr_map,
                                         const Work& w, uint32_t tmem,
                                         uint32_t rank, int warp, int lane) {
   const int g = (warp - 4) >> 2;        // warpgroup = page of the S tile
@@ -577,22 +587,43 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   const int r = quad * 32 + lane;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   const bool row_ok = r < w.nrows;
-  const int64_t qrow = (int64_t)w.b * p.q_len * p.H + w.r_base + r;
   const int hp = lane >> 4;             // half of the page: tokens 32 hp ..
   const int part = 2 * g + hp;          // 32-token group of the S tile
   const int rA = quad * 32 + (lane & 15), rB = rA + 16;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
+
+  const uint32_t qbar = smem_u32(&s.qbar);
+  if (warp == 4 && lane == 0) {
+    const uint32_t box = (uint32_t)p.q_box_rows * 128u;
+    const int qy = w.b * p.q_len * p.H + w.r_base;
+    mbar_arrive_expect_tx(qbar, 9 * box);
+    for (int k = 0; k < 8; ++k)
+      tma_load_3d(smem_u32(s.ring[0]) + 16384u * k, qn_map, qbar, 64 * k, qy, 0);
+    tma_load_3d(smem_u32(s.pslot[0]), qr_map, qbar, 0, qy, 0);
+  }
+  const bool qok = mbar_wait(qbar, 0, &s.abort_flag);
+  // 16-byte chunk k of this row's c_kv dims (k < 64) or RoPE dims (k < 8).
+  auto qchunk = [&](int k) -> uint4 {
+    return row_ok && qok ? *reinterpret_cast<const uint4*>(
+                               s.ring[0] + 16384 * (k >> 3) +
+                               box_chunk_offset(r, k & 7))
+                         : zero4;
+  };
+  auto qrope_chunk = [&](int k) -> uint4 {
+    return row_ok && qok ? *reinterpret_cast<const uint4*>(
+                               s.pslot[0] + box_chunk_offset(r, k))
+                         : zero4;
+  };
 
   // Row scale 2^e from the warpgroups' partial |q| maxima.
   float amax = 0.f;
   if (g < 2) {
 #pragma unroll 8
     for (int k = 0; k < 32; ++k)
-      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_nope[qrow * 64 + 32 * g + k] : zero4));
+      amax = fmaxf(amax, absmax_bf16x8(qchunk(32 * g + k)));
   } else if (g == 2) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      amax = fmaxf(amax, absmax_bf16x8(row_ok ? p.q_rope[qrow * 8 + k] : zero4));
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, absmax_bf16x8(qrope_chunk(k)));
   }
   s.xch[g][r] = amax;
   named_bar_sync(1, 512);
@@ -614,11 +645,10 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t vh[16], vl[16];
-      const uint4* src = p.q_nope + qrow * 64 + 32 * g + 8 * c;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         uint2 h, l;
-        split_q8(row_ok ? src[k] : zero4, inv, h, l);
+        split_q8(qchunk(32 * g + 8 * c + k), inv, h, l);
         vh[2 * k] = h.x;
         vh[2 * k + 1] = h.y;
         vl[2 * k] = l.x;
@@ -632,8 +662,8 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk cc = elements 16cc..16cc+15
       uint2 h0, l0, h1, l1;
-      split_q8(row_ok ? p.q_rope[qrow * 8 + 2 * cc] : zero4, inv, h0, l0);
-      split_q8(row_ok ? p.q_rope[qrow * 8 + 2 * cc + 1] : zero4, inv, h1, l1);
+      split_q8(qrope_chunk(2 * cc), inv, h0, l0);
+      split_q8(qrope_chunk(2 * cc + 1), inv, h1, l1);
       const uint32_t off = (r >> 3) * 512 + (r & 7) * 64 +
                            (((cc ^ (r >> 1)) & 3) << 4);
       *reinterpret_cast<uint4*>(s.qrope[0] + off) = make_uint4(h0.x, h0.y, h1.x, h1.y);
@@ -641,6 +671,7 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     }
     fence_proxy_async_smem();
   }
+  if (!__all_sync(kFull, qok) && lane == 0) signal_abort(s, p, rank);
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&s.qready));
@@ -1050,27 +1081,41 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
     return;
   }
   tc_fence_after();
+  // O_part = O / l, 32 values at a time: the warp stages its 32 rows in 4 KB
+  // of the then idle ring (row r at 128 r bytes, 16-byte chunk e at position
+  // e ^ (r % 8): neither the writes nor the reads below conflict) and reads
+  // them back four rows per instruction, lane l taking chunk l % 8 of row
+  // 4i + l / 8, so every store instruction writes four full 128-byte lines.
   const float inv = s.fin[r];
-  const bool row_ok = r < w.nrows;
   const int64_t rows = (int64_t)p.B * p.q_len * p.H;
   const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-  float* dst = p.O_part +
-               (part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r) *
-                   MLA_VALUE_DIM;
+  float* const dst0 = p.O_part + (part * rows + (int64_t)w.b * p.q_len * p.H +
+                                  w.r_base + quad * 32) * MLA_VALUE_DIM;
+  const int nvalid = w.nrows - quad * 32;  // rows of this warp in range
+  uint8_t* const buf = s.ring[0] + 4096 * quad;
 #pragma unroll 1
   for (int c0 = 0; c0 < MLA_VALUE_DIM; c0 += 32) {
     uint32_t v[32];
     tmem_ld32(tmem + lane_base + c0, v);
     tmem_wait_ld();
-    if (row_ok) {
-      float4* d4 = reinterpret_cast<float4*>(dst + c0);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv,
-                            __uint_as_float(v[4 * e + 1]) * inv,
-                            __uint_as_float(v[4 * e + 2]) * inv,
-                            __uint_as_float(v[4 * e + 3]) * inv);
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<float4*>(buf + box_chunk_offset(lane, e)) =
+          make_float4(__uint_as_float(v[4 * e]) * inv,
+                      __uint_as_float(v[4 * e + 1]) * inv,
+                      __uint_as_float(v[4 * e + 2]) * inv,
+                      __uint_as_float(v[4 * e + 3]) * inv);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), e = lane & 7;
+      const float4 f =
+          *reinterpret_cast<const float4*>(buf + box_chunk_offset(rr, e));
+      if (rr < nvalid)
+        *reinterpret_cast<float4*>(dst0 + (int64_t)rr * MLA_VALUE_DIM + c0 +
+                                   4 * e) = f;
     }
+    __syncwarp();  // every lane read the box before it is refilled
   }
 }
 
@@ -1078,6 +1123,8 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_fp8_kernel(const __grid_constant__ CUtensorMap kv_map,
                               const __grid_constant__ CUtensorMap rope_map,
+                              const __grid_constant__ CUtensorMap qn_map,
+                              const __grid_constant__ CUtensorMap qr_map,
                               const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -1117,6 +1164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.corr_done), 4);
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.qready), 16);
+    mbar_init(smem_u32(&s.qbar), 1);
     mbar_init(smem_u32(&s.tail_go), 1);
     mbar_init(smem_u32(&s.tail_ready), 1);
     if (rank == 1 && w.npages > 0) {
@@ -1127,6 +1175,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&kv_map);
     prefetch_tmap(&rope_map);
+    if (rank == 0) {
+      prefetch_tmap(&qn_map);
+      prefetch_tmap(&qr_map);
+    }
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -1202,7 +1254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax(s, p, w, tmem, rank, warp, lane);
+    softmax(s, p, &qn_map, &qr_map, w, tmem, rank, warp, lane);
     teardown();
     return;
   }
@@ -1274,12 +1326,15 @@ int launch_tc_fp8(const DecodeArgs& a) {
   if (rc != MLA_OK) return rc;
   rc = make_kv_tensor_map_fp8_rope(&rope_map, a.kv, a.num_slots);
   if (rc != MLA_OK) return rc;
+  CUtensorMap qn_map, qr_map;
+  rc = make_query_maps(&qn_map, &qr_map, a, &p.q_box_rows);
+  if (rc != MLA_OK) return rc;
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc fp8)");
   mla_partial_tc_fp8_kernel<<<(unsigned)(pairs * 2), kThreads, kSmemBytes,
-                              a.stream>>>(map, rope_map, p);
+                              a.stream>>>(map, rope_map, qn_map, qr_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_fp8_kernel");
   return MLA_OK;

@@ -39,6 +39,12 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
                             const uint64_t dims[3], const uint64_t strides[2],
                             const uint32_t box[3]);
 
+// Tensor maps of a launch's query rows, [B * q_len * H, 512] and [.., 64]
+// bf16 (as 3-D arrays with one plane), in boxes of 64 values x min(128,
+// rows) rows with the 128-byte swizzle; *box_rows receives the box height.
+int make_query_maps(CUtensorMap* nope, CUtensorMap* rope, const DecodeArgs& a,
+                    int* box_rows);
+
 // Tensor map of an E4M3 pool in boxes of 64 rows x 64 bytes with the 64-byte
 // swizzle (4 KB): the RoPE key columns 512..575 of one page, the K-major
 // operand layout the FP8 decode kernel's tensor cores read for those dims.
