@@ -77,6 +77,11 @@ def parse():
                     help="wave-quantisation sweep: B in 1..24 x context "
                          "{100k, 400k}, the pages' split rule vs the planner "
                          "(one JSON line per point)")
+    ap.add_argument("--c0-scan", action="store_true",
+                    help="time the scheduler's plans for unit costs c0 in "
+                         "{4, 8, 12, 16, 24, 32} on the 100k sweep, dp16, DCP, "
+                         "ragged FP8 and FP8 sweep points (refits the planners' "
+                         "unit cost), one JSON line per workload")
     ap.add_argument("--sweep-scan", default="",
                     help="extra comma-separated split counts to time at "
                          "every sweep point")
@@ -306,6 +311,45 @@ def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
     return statistics.median(ts)
 
 
+def run_c0_scan(args):
+    """The scheduler's plans (mla_plan_sched_ex) for a range of unit costs c0,
+    each distinct plan timed as a partial + combine pair: the data the
+    planners' default unit costs are fitted to."""
+    import torch
+
+    import mla_latent_decode_gb300 as mla
+    from mla_latent_decode_gb300 import synth
+    mla.library()
+    c0s = [4.0, 8.0, 12.0, 16.0, 24.0, 32.0]
+    configs = [f"sweep_B{B}_L100000" for B in (1, 2, 4, 8, 12, 16, 20, 24)]
+    configs += ["dp16", "dcp", "ragged_fp8"]
+    configs += [f"sweep8_B{B}_L100000" for B in (4, 8, 16, 24)]
+    for name in configs:
+        wl = synth.config(name)
+        batch = synth.make_batch(wl, seed=0, device="cuda")
+        lens = mla.batch_lengths(batch)
+        fp8 = wl.kv_dtype != "bf16"
+        dev = batch.q_nope.device
+        timed, res = {}, {}
+        for c0 in c0s:
+            S, bnd, work, _, ms = mla.plan_sched_ex(
+                lens, wl.q_len, wl.H, 76 if fp8 else 36, 64, 8, c0, 1.0,
+                rows_per_unit=128 if fp8 else 256)
+            key = (S, bnd.tobytes(), work.tobytes())
+            if key not in timed:
+                iters = 20 if wl.B * max(wl.seq_lens) < 5e6 else 8
+                timed[key] = 1e3 * time_pair(
+                    mla, batch, wl, S, iters, split_pages=torch.from_numpy(bnd).to(dev),
+                    work=torch.from_numpy(work).to(dev))
+            res[str(c0)] = {"splits": S, "us": timed[key], "model_makespan": ms}
+        print(json.dumps({"impl": "c0_scan", "config": name,
+                          "slots": 76 if fp8 else 36, "unit": "us per layer "
+                          "(partial + combine)", "by_c0": res}), flush=True)
+        del batch
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_sweep(args):
     """Wave-quantisation sweep: for every (B, context) point, the pair timed
     with the pages' split rule and with the planner's split (and any extra
@@ -522,6 +566,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.c0_scan:
+        return run_c0_scan(args)
     rank, world, local = dist_env()
     import torch
 

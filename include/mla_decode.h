@@ -144,9 +144,9 @@ int mla_plan_ex(int V, int q_len, int H, int rows_per_unit,
  * kv_dtype: BF16 -> rows_per_unit = 256 and slots = mla_cluster_slots() (or
  * num_sms / 4 when num_sms > 0); FP8 E4M3 -> rows_per_unit = 128 and the
  * resident 2-CTA clusters of the FP8 kernel (or num_sms / 2); s_max = 64;
- * c0 = 32; lam = 1 (fitted to the BF16 kernel's measured times on GB300,
- * B = 1..24 requests x 100k / 400k tokens: a work unit costs about 32 pages
- * beyond its own).
+ * c0 = 16 for BF16 and 32 for FP8 E4M3; lam = 1 (fitted to the kernels'
+ * measured times on GB300, B = 1..24 requests x 100k / 400k tokens: a work
+ * unit costs about that many pages beyond its own).
  *   B, num_shards  requests and context shards (V = B * num_shards);
  *   kv_dtype       MLA_KV_BF16 or MLA_KV_FP8_E4M3 (else MLA_ERR_INVALID_ARG)
  *   seq_lens_host  host int32 [num_shards * B] (shard-local lengths).
@@ -185,7 +185,7 @@ int mla_plan_parts_ex(int V, int q_len, int H, int rows_per_unit,
 
 /*
  * mla_plan_parts_ex with mla_plan's defaults (rows per unit and slots of the
- * kernel that serves kv_dtype, s_max = 64, c0 = 32, lam = 1).
+ * kernel that serves kv_dtype, s_max = 64, c0 and lam as mla_plan).
  * split_pages_out: HOST int32 buffer of at least num_shards * B * 65 entries.
  */
 int mla_plan_parts(int B, int q_len, int H, int num_shards,
@@ -226,7 +226,7 @@ int mla_plan_sched_ex(int V, int q_len, int H, int rows_per_unit,
 
 /*
  * mla_plan_sched_ex with mla_plan's defaults (rows per unit and slots of the
- * kernel that serves kv_dtype, s_max = 64, c0 = 32, lam = 1).
+ * kernel that serves kv_dtype, s_max = 64, c0 and lam as mla_plan).
  * split_pages_out: HOST int32 [num_shards * B * 65]; work_out: HOST int32
  * [work_capacity], at most num_shards * B * 64 * ceil(q_len * H / 128)
  * entries are written.

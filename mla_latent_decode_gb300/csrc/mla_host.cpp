@@ -88,15 +88,23 @@ int check_work(const DecodeArgs& a) {
   return MLA_OK;
 }
 
-// Default cost constants of mla_plan, in units of one page of one work unit
-// (about 0.9 us on a GB300): a work unit's fixed cost (launch, Q load,
-// pipeline fill, O_part write, wave hand-over) and the price of one more split
-// per 1024 query rows (partial outputs written and re-read by the combine).
-// Fitted to the decode kernel's measured times over B = 1..24 requests x
-// {100k, 400k} tokens x {1, 2, 3, 4, 6, 9, 18} splits, where they choose the
-// fastest measured split count at every point.
-constexpr double kPlanUnitCost = 32.0;
+// Default cost constants of the planners, in units of one page of one work
+// unit (about 0.9 us on a GB300): a work unit's fixed cost (launch, Q load,
+// pipeline fill and drain, O_part write, wave hand-over) and the price of one
+// more split per 1024 query rows (partial outputs written and re-read by the
+// combine).  The split price and the FP8 unit cost were fitted to the
+// kernels' measured times over B = 1..24 requests x {100k, 400k} tokens x
+// {1, 2, 3, 4, 6, 9, 18} splits; the BF16 unit cost was refitted once its
+// query load and epilogue shrank (a unit's fixed time fell from about 20 to
+// about 8 us): every value from 8 to 24 then gives the fastest measured plan
+// on the sweep at 100k, dp16 and DCP, and 16 sits in the middle.
+constexpr double kPlanUnitCostBf16 = 16.0;
+constexpr double kPlanUnitCostFp8 = 32.0;
 constexpr double kPlanSplitCost = 1.0;
+
+static double plan_unit_cost(mla_kv_dtype kv_dtype) {
+  return kv_dtype == MLA_KV_FP8_E4M3 ? kPlanUnitCostFp8 : kPlanUnitCostBf16;
+}
 
 // List-scheduling makespan of units in launch order on `slots` slots.
 static double makespan(const std::vector<double>& costs, int slots) {
@@ -201,7 +209,7 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
   }
   return mla_plan_ex(B * num_shards, q_len, H,
                      fp8 ? MLA_ROWS_PER_UNIT / 2 : MLA_ROWS_PER_UNIT,
-                     seq_lens_host, slots, 64, kPlanUnitCost, kPlanSplitCost,
+                     seq_lens_host, slots, 64, plan_unit_cost(kv_dtype), kPlanSplitCost,
                      num_splits_out, wave_eff_out, nullptr);
 }
 
@@ -420,7 +428,7 @@ int mla_plan_parts(int B, int q_len, int H, int num_shards,
   return mla_plan_parts_ex(B * num_shards, q_len, H,
                            kv_dtype == MLA_KV_FP8_E4M3 ? MLA_ROWS_PER_UNIT / 2
                                                        : MLA_ROWS_PER_UNIT,
-                           seq_lens_host, slots, 64, max_parts, kPlanUnitCost,
+                           seq_lens_host, slots, 64, max_parts, plan_unit_cost(kv_dtype),
                            kPlanSplitCost, split_pages_out, num_parts_out,
                            wave_eff_out, nullptr);
 }
@@ -440,7 +448,7 @@ int mla_plan_sched(int B, int q_len, int H, int num_shards,
   return mla_plan_sched_ex(B * num_shards, q_len, H,
                            kv_dtype == MLA_KV_FP8_E4M3 ? MLA_ROWS_PER_UNIT / 2
                                                        : MLA_ROWS_PER_UNIT,
-                           seq_lens_host, slots, 64, max_parts, kPlanUnitCost,
+                           seq_lens_host, slots, 64, max_parts, plan_unit_cost(kv_dtype),
                            kPlanSplitCost, split_pages_out, num_parts_out,
                            work_out, work_capacity, num_work_out, wave_eff_out,
                            nullptr);
