@@ -15,8 +15,12 @@
 // rows past M read as zeros) and the weight slice in 64 x 64 boxes (rows =
 // K, 128-byte rows of N: MN-major) -- and issues M = 128, N <= 256, K = 16
 // bf16 MMAs into TMEM; the four warps then round their 32 rows to bf16.
-// Every wait is bounded (ptx_sm103.cuh); a timeout sets
-// MLA_STATUS_WAIT_TIMEOUT.
+// Launches use programmatic dependent launch: a CTA lets the stream's next
+// kernel start at once and, before it waits for the kernels it depends on,
+// has its whole weight slice prefetched into L2 (a prefetch reads nothing
+// into the CTA, so weights written by those kernels are still read after
+// they finish: L2 holds the current data).  Every wait is bounded
+// (ptx_sm103.cuh); a timeout sets MLA_STATUS_WAIT_TIMEOUT.
 #include <cuda_bf16.h>
 
 #include "mla_tma.cuh"
@@ -86,9 +90,15 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  griddep_launch_dependents();
   bool ok = true;
   if (threadIdx.x == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, G::kMmaN, false, true);
+    // The weight slice into L2 while earlier kernels finish.
+    for (int k0 = 0; k0 < K; k0 += 64)
+      for (int nb = 0; nb < NC / 64; ++nb)
+        tma_prefetch_3d(&w_map, n_base + nb * 64, k0, h);
+    griddep_wait();
     for (int c = 0; c < G::kChunks && ok; ++c) {
       const int st = c % G::kStages;
       const uint32_t use = c / G::kStages;
@@ -102,10 +112,10 @@ __global__ void __launch_bounds__(128, 1)
       mbar_arrive_expect_tx(bar, G::kStageBytes);
       for (int kb = 0; kb < kChunkK / 64; ++kb) {
         const int k0 = c * kChunkK + kb * 64;
-        tma_load_3d(smem_u32(sa + kb * kBoxA), &a_map, bar, k0, h, m0);
         for (int nb = 0; nb < NC / 64; ++nb)
           tma_load_3d(smem_u32(sb + (kb * (NC / 64) + nb) * kBoxB), &w_map, bar,
                       n_base + nb * 64, k0, h);
+        tma_load_3d(smem_u32(sa + kb * kBoxA), &a_map, bar, k0, h, m0);
       }
       if (!mbar_wait(bar, use & 1, abort_flag)) {
         ok = false;
@@ -202,11 +212,20 @@ int launch_head_gemm(const void* in, const void* w, void* out, int M, int H,
   cudaError_t e = cudaFuncSetAttribute(
       kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(head gemm)");
-  const dim3 grid((unsigned)((M + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H,
-                  (unsigned)(N / NC));
-  kernel<<<grid, 128, G::kSmemBytes, stream>>>(
-      a_map, w_map, static_cast<__nv_bfloat16*>(out), M, H, status);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((M + kRowsPerCta - 1) / kRowsPerCta),
+                     (unsigned)H, (unsigned)(N / NC));
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a_map, w_map,
+                         static_cast<__nv_bfloat16*>(out), M, H, status);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_head_gemm_kernel");
   return MLA_OK;
 }

@@ -178,6 +178,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Start the 3-D box at (x, y, z) of a tensor on its way into L2 (no shared
+// memory written, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x,
+                                                int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+          tmap),
+      "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic stream serialization) start its prologue now; and wait
+// until every grid this one depends on has completed with its memory
+// operations visible (a no-op when the launch has no such dependency).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // peer CTA's shared memory (cluster address), completing on the peer's
 // barrier (cluster address).
