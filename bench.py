@@ -44,7 +44,7 @@ METRIC = ("MLA decode µs/layer & attention TFLOP/s at 100k ctx; "
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_partial_traffic.json")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -85,7 +85,7 @@ def parse():
     ap.add_argument("--sweep-scan", default="",
                     help="extra comma-separated split counts to time at "
                          "every sweep point")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -93,6 +93,25 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def slowest_rank(local, dist=None, device="cpu"):
+    """The job's time for a region every rank times on its own clock: the
+    slowest rank's (max over ranks; the local value without a process
+    group)."""
+    if dist is None:
+        return float(local)
+    import torch
+    t = torch.tensor([float(local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, steps, world, seconds):
+    """Whole-job throughput: every rank decodes its own batch (data
+    parallel, no collective on the data path), so the job processes world x
+    the per-rank FLOPs in the slowest rank's time."""
+    return world * flops_per_rank_step * steps / seconds / 1e12
 
 
 def workload_desc(wl):
@@ -691,20 +710,12 @@ def main():
     comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in timed region")
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
     if flush:  # time the steps only, not the flushes between them
         total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
-        if dist:
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
+    total_ms = slowest_rank(total_ms, dist, dev)
     fl = wl.flops()
     ms_per_step = total_ms / args.steps
-    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(fl, args.steps, world, total_ms * 1e-3)
     peaks, peak_kind = measured_peaks()
     part_mean = statistics.mean(part_ms)
     achieved = fl / (part_mean * 1e-3) / 1e12
@@ -755,12 +766,8 @@ def main():
         for _ in range(n_e2e):
             e2e_step()
         torch.cuda.synchronize()
-        e2e_s = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": world * fl * n_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
+        e2e_s = slowest_rank(time.perf_counter() - t0, dist, dev)
+        e2e = {"value": job_tflops(fl, n_e2e, world, e2e_s), "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "steps": n_e2e}
 
