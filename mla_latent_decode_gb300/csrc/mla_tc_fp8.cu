@@ -791,19 +791,20 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 
     // Ship page g in message slot g (four slots, four pages per tile), use
     // j.  p = 2^(raw*scale*crow - m_ref) <= 2^tau (a row with nothing visible
-    // yet shifts by 0: p = ex2(-inf) = 0), l += p; rows A and B of p go to
-    // the slot as f16 pairs, 16 bytes at a time (the packers multiply by
-    // scale * 2^g), with the tile's rescale (page 0 only), the warp's flag
-    // and, from warp quad 1, the page's factors.
+    // yet shifts by 0: p = ex2(-inf) = 0), l += p.  Rows A and B of p are
+    // packed as f16 pairs in place of their scores (word i of a row's 16 is
+    // written after the scores it replaces were read), and only then does the
+    // warpgroup wait for the slot: the O pair consumes pages in order, so
+    // page 3's slot frees last, and the exponentials would otherwise queue
+    // behind it.  Then the rows go to the slot 16 bytes at a time (the
+    // packers multiply by scale * 2^g), with the tile's rescale (page 0
+    // only), the warp's flag and, from warp quad 1, the page's factors.
     const bool any = __any_sync(kFull, alphaA != 1.f || alphaB != 1.f);
     uint8_t* stg = s.pslot[g];
-    auto make_row = [&](const uint32_t (&x)[32], float crow, float m,
-                        float& lsum, int row) {
+    auto make_row = [&](uint32_t (&x)[32], float crow, float m, float& lsum) {
       const float shift = m == -INFINITY ? 0.f : m;
       const uint64_t c2 = f2pack(crow, crow), nshift2 = f2pack(-shift, -shift);
       uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-      uint8_t* dst = stg + (row >> 3) * 1024;
-      uint32_t w0 = 0, w1 = 0;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {  // tokens 32 hp + 4c .. + 3
         float y0, y1, y2, y3;
@@ -814,27 +815,31 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
         const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
         acc0 = fadd2(acc0, f2pack(p0, p1));
         acc1 = fadd2(acc1, f2pack(p2, p3));
-        if (c & 1) {
-          // 16-B chunk 4 hp + c / 2 = tokens 32 hp + 8 (c / 2) .. + 7, at
-          // position chunk ^ (row % 8) of the row's 128 bytes
-          *reinterpret_cast<uint4*>(dst + box_chunk_offset(row & 7, 4 * hp + (c >> 1))) =
-              make_uint4(w0, w1, pack_f16(p0, p1), pack_f16(p2, p3));
-        } else {
-          w0 = pack_f16(p0, p1);
-          w1 = pack_f16(p2, p3);
-        }
+        x[2 * c] = pack_f16(p0, p1);
+        x[2 * c + 1] = pack_f16(p2, p3);
       }
       float u0, u1, v0, v1;
       f2unpack(acc0, u0, u1);
       f2unpack(acc1, v0, v1);
       lsum += (u0 + u1) + (v0 + v1);
     };
+    // 16-B chunk 4 hp + q = tokens 32 hp + 8q .. + 7 of a row (words 4q ..
+    // 4q + 3), at position chunk ^ (row % 8) of the row's 128 bytes.
+    auto store_row = [&](const uint32_t (&x)[32], int row) {
+      uint8_t* dst = stg + (row >> 3) * 1024;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(dst + box_chunk_offset(row & 7, 4 * hp + q)) =
+            make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    };
     if (has) {
+      make_row(a, crowA, mA, lA);
+      make_row(b, crowB, mB, lB);
       if (j > 0 && ok &&
           !mbar_wait(smem_u32(&s.pempty[g]), (j - 1) & 1, &s.abort_flag))
         ok = false;
-      make_row(a, crowA, mA, lA, rA);
-      make_row(b, crowB, mB, lB, rB);
+      store_row(a, rA);
+      store_row(b, rB);
       if (hp == 0) {
         reinterpret_cast<float*>(stg + kAlphaOff)[rA] = g == 0 ? alphaA : 1.f;
         reinterpret_cast<float*>(stg + kAlphaOff)[rB] = g == 0 ? alphaB : 1.f;
