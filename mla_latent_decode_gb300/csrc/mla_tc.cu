@@ -15,11 +15,13 @@
 //   consumes 64 B/clk of K, so the KV tile of one MMA is split over two SMs
 //   with the CTA-pair (cta_group::2) MMA, M = 256 rows = two row groups:
 //     ranks 0,1, the "S pair": rank r owns row group 2u + r: Q_nope (bf16
-//       pairs) in TMEM columns [0, 256), Q_rope in shared memory, one S
-//       buffer of 256 columns (an S tile = 4 pages = 256 tokens).  Rank r
-//       loads pages 2r, 2r+1 of every tile in 16-KB stages (one 64-dim chunk
-//       of its two pages, 128-byte swizzled TMA boxes); each stage feeds 4
-//       pair MMAs of M=256, N=256, K=16 issued by rank 0.  Two softmax
+//       pairs) in TMEM columns [0, 256), Q_rope in shared memory, both
+//       brought by TMA (Q_nope through the P slots, idle until the first S
+//       tile), one S buffer of 256 columns (an S tile = 4 pages = 256
+//       tokens).  Rank r loads pages 2r, 2r+1 of every tile in 16-KB stages
+//       (one 64-dim chunk of its two pages, 128-byte swizzled TMA boxes);
+//       each stage feeds 4 pair MMAs of M=256, N=256, K=16 issued by rank
+//       0.  Two softmax
 //       warpgroups per CTA own two pages each, exchange row maxima once per
 //       tile, keep base-2 running statistics with lazy rescaling, and ship
 //       each page's P (bf16, K-major, 128-byte swizzled) plus rescale
@@ -28,8 +30,10 @@
 //       2u + r in all of its TMEM and loads half of V: dims [256n + 128r,
 //       +128) of each page for the two 256-wide halves n, one 32-KB stage
 //       per page; each page feeds 8 pair MMAs of M=256, N=256, K=16 (A = P,
-//       B = V MN-major) issued by rank 2.  Correction warps rescale O rows when an S-CTA raised a
-//       running max, then write the normalised O_part rows.
+//       B = V MN-major) issued by rank 2.  Correction warps rescale O rows
+//       when an S-CTA raised a running max; then warps 4..11 write the
+//       normalised O_part rows, staged through the idle ring so that every
+//       store instruction writes full 128-byte lines.
 //   Per SM the TMA then lands 16 KB per 512 tensor cycles.  Every wait is
 //   bounded (ptx_sm103.cuh); a timeout sets MLA_STATUS_WAIT_TIMEOUT and the
 //   cluster finishes early.

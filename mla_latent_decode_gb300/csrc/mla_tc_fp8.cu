@@ -31,8 +31,10 @@
 //   Each product thus takes two 8-bit MMAs, as long as one 16-bit MMA, and
 //   the tensor cores read the E4M3 bytes with no conversion pass.
 //   Rank 0 (S-CTA) holds Qhi/Qlo (TMEM columns [0, 256) for the 512 c_kv
-//   dims, shared memory for the 64 RoPE dims) and one 256-column S tile;
-//   rank 1 (O-CTA) holds O (128 rows x 512 fp32 = all 512 TMEM columns).
+//   dims, shared memory for the 64 RoPE dims), split from query rows that
+//   TMA brings into the still idle ring, and one 256-column S tile; rank 1
+//   (O-CTA) holds O (128 rows x 512 fp32 = all 512 TMEM columns) and writes
+//   O_part through the idle ring in full 128-byte lines.
 //   g is the exponent with max|scale| 2^g in [0.5, 1) over the tokens seen
 //   so far (a scale warp tracks it per tile), so P' <= p <= 2^8 stays inside
 //   E4M3's range whatever the scales' magnitude; O is kept in units of
