@@ -82,6 +82,8 @@ def config(name: str, seed: int = 0, **over) -> Workload:
                 [1k, 200k], FP8 E4M3 KV with a per-token fp32 scale
     sweep_B<b>_L<l>  b requests x q_len 5 x 96 heads x l context, BF16
     sweep8_B<b>_L<l> the same with FP8 E4M3 KV and a per-token fp32 scale
+    dcp_B<b>    b requests of dcp's shape (8 shards of 100k tokens): a
+                smaller case of the same kernel launch
     """
     if name == "tiny":
         wl = Workload("tiny", 1, 1, 16, [256], num_splits=1)
@@ -95,6 +97,9 @@ def config(name: str, seed: int = 0, **over) -> Workload:
     elif name.startswith("sweep_B"):
         b, l = name[len("sweep_B"):].split("_L")
         wl = Workload(name, int(b), 5, 96, [int(l)] * int(b))
+    elif name.startswith("dcp_B"):
+        b = int(name[len("dcp_B"):])
+        wl = Workload(name, b, 5, 96, [100_000] * b, num_shards=8)
     elif name.startswith("sweep8_B"):
         b, l = name[len("sweep8_B"):].split("_L")
         wl = Workload(name, int(b), 5, 96, [int(l)] * int(b), "fp8_e4m3")
