@@ -8,8 +8,9 @@
 // them; the products run on tcgen05 tensor cores.
 //
 // One CTA per (head h, tile of 128 rows, chunk of NC output columns), 4
-// warps: splitting N gives each head two CTAs at these sizes, so the weight
-// slices stream through twice as many SMs.  Warp 0 lane 0 loads K
+// warps: splitting N (4 chunks of 128 for the query absorption, 2 of 64 for
+// the output projection) streams each head's weight slice through several
+// SMs at once; these launches are latency-bound, not bandwidth-bound.  Warp 0 lane 0 loads K
 // in chunks of 128 by TMA -- the activation rows of head h through a 3-D
 // tensor map (64 K x 1 head x 128 rows boxes, K-major, 128-byte swizzle,
 // rows past M read as zeros) and the weight slice in 64 x 64 boxes (rows =
@@ -238,7 +239,7 @@ using namespace mla;
 extern "C" int mla_absorb_q(const void* q_nope, const void* w_kc,
                             void* q_absorbed, int M, int H, int* status,
                             mla_stream_t stream) {
-  return launch_head_gemm<MLA_QK_NOPE_DIM, MLA_NOPE_DIM, 256>(
+  return launch_head_gemm<MLA_QK_NOPE_DIM, MLA_NOPE_DIM, 128>(
       q_nope, w_kc, q_absorbed, M, H, status, (cudaStream_t)stream,
       "mla_absorb_q");
 }
