@@ -194,6 +194,27 @@ def test_tc_full_size_dcp_sampled_rows_vs_unsharded_oracle():
     print("dcp", S, m)
 
 
+@pytest.mark.parametrize("name", ["sweep_B1_L400000", "sweep8_B1_L400000"])
+def test_tc_longest_context_sampled_rows(name):
+    """One request of 400k tokens (6250 pages), BF16 or FP8 KV, with the
+    scheduler's parts (18 for BF16): the longest context of the sweep, checked
+    on sampled rows and the row-group edges."""
+    wl = synth.config(name)
+    batch = synth.make_batch(wl, seed=3, device="cuda")
+    st = _status()
+    out, lse, S = mla.decode(batch, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and S > 1
+    hb = synth.host_bits(batch)
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([rng.choice(wl.rows, 30, replace=False),
+                                     [0, 127, 128, 255, 256, 383, 384, 479]]))
+    O_ref, l_ref = oracle_rows(batch, hb, rows)
+    m = check_close(f64(out).reshape(-1, 512)[rows], f64(lse).reshape(-1)[rows],
+                    O_ref, l_ref, wl.kv_dtype, f"{name} S={S}")
+    print(name, S, m)
+
+
 # ----------------------------------------------------------- FP8 E4M3 KV ----
 FP8_CASES = [
     ("fp8_tiny", synth.Workload("t8", 1, 1, 16, [256], kv_dtype="fp8_e4m3"), 1),
