@@ -633,9 +633,11 @@ def main():
                                          kv_dtype=wl.kv_dtype)
         split_pages = torch.from_numpy(bnd).to(dev)
         work = torch.from_numpy(wk).to(dev)
-        plan_desc = (f"scheduler: {S} parts per request at most, first-part "
-                     f"boundaries {sorted({r[1] for r in bnd.tolist()})[:4]}, "
-                     f"{len(wk)} work units longest first")
+        longest = max(bnd.tolist(), key=lambda r: r[-1])
+        sizes = [b1 - b0 for b0, b1 in zip(longest, longest[1:]) if b1 > b0]
+        plan_desc = (f"scheduler: {S} parts per request at most (the longest "
+                     f"request's parts: {sizes} pages), {len(wk)} work units "
+                     f"launched longest first")
     S_pages = mla.plan_heuristic(wl.B, wl.q_len)
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
