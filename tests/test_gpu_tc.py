@@ -73,13 +73,19 @@ def test_tc_partials_match_oracle_per_split():
                     O_ref, l_ref, "bf16", f"split {s}")
 
 
-def test_tc_shards_match_unsharded_oracle():
-    sh = synth.Workload("dcp", 3, 5, 96, [517, 64, 9], num_shards=8)
-    base = synth.Workload("dcp", 3, 5, 96, [517, 64, 9])
+@pytest.mark.parametrize("lens,splits", [([517, 64, 9], 2), ([5, 300, 7], None)],
+                         ids=["short", "empty_shards_scheduled"])
+def test_tc_shards_match_unsharded_oracle(lens, splits):
+    """8 token-interleaved shards vs the unsharded oracle.  With 5- and
+    7-token requests some shards hold no token at all (their parts are
+    empty: O = 0, LSE = -inf) and shard-local lengths fall below q_len; the
+    second case takes the scheduler's parts and launch order."""
+    sh = synth.Workload("dcp", 3, 5, 96, lens, num_shards=8)
+    base = synth.Workload("dcp", 3, 5, 96, lens)
     b_sh = synth.make_batch(sh, seed=5, device="cuda")
     b_un = synth.make_batch(base, seed=5, device="cuda")
     st = _status()
-    out_s, lse_s, _ = mla.decode(b_sh, num_splits=2, status=st)
+    out_s, lse_s, _ = mla.decode(b_sh, num_splits=splits, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     O_ref, l_ref = oracle_rows(b_un, synth.host_bits(b_un), None)
