@@ -311,12 +311,14 @@ def test_tc_fp8_query_dynamic_range_matches_oracle():
     print(m)
 
 
-def test_tc_fp8_shards_match_unsharded_oracle():
-    sh = synth.Workload("dcp8", 3, 5, 96, [517, 64, 9], num_shards=8,
+@pytest.mark.parametrize("lens,splits", [([517, 64, 9], 2), ([5, 300, 7], None)],
+                         ids=["short", "empty_shards_scheduled"])
+def test_tc_fp8_shards_match_unsharded_oracle(lens, splits):
+    sh = synth.Workload("dcp8", 3, 5, 96, lens, num_shards=8,
                         kv_dtype="fp8_e4m3")
     batch = synth.make_batch(sh, seed=5, device="cuda")
     st = _status()
-    out, lse, _ = mla.decode(batch, num_splits=2, status=st)
+    out, lse, _ = mla.decode(batch, num_splits=splits, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     host, Bq = compact_unsharded(batch, [0, 1, 2])
