@@ -15,7 +15,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests are skipped (not failed) when no GPU is visible; `-m gpu` on a
-    # GPU machine runs them.
+    # machine with a GB300 runs them.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
