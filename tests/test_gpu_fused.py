@@ -53,6 +53,9 @@ CASES = [
     ("bf16_empty_splits", synth.Workload("fe", 2, 5, 32, [64, 200]), 9),
     ("fp8_small", synth.Workload("f8", 3, 5, 96, [1000, 257, 5], kv_dtype="fp8_e4m3"), 3),
     ("fp8_empty_splits", synth.Workload("f8e", 2, 5, 32, [64, 200], kv_dtype="fp8_e4m3"), 9),
+    # 700 rows per request: 3 BF16 units, 6 FP8 units, each with its counter
+    ("bf16_rows_700_q7", synth.Workload("f7", 2, 7, 100, [900, 450]), 2),
+    ("fp8_rows_700_q7", synth.Workload("f78", 2, 7, 100, [900, 450], kv_dtype="fp8_e4m3"), 2),
 ]
 
 

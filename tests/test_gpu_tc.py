@@ -37,6 +37,10 @@ CASES = [
     ("peaked", synth.Workload("p", 2, 5, 96, [3000, 333], q_scale=8.0), 4),
     ("long_one_split", synth.Workload("l", 1, 5, 96, [20_000]), 1),
     ("empty_splits", synth.Workload("e", 2, 5, 32, [64, 200]), 9),
+    # more rows per request than the 480 of the pages' shape: 700 rows are 3
+    # units of 256 (the last 188), 1024 rows exactly 4; q_len 7 and 8
+    ("rows_700_q7", synth.Workload("r7", 2, 7, 100, [900, 450]), 2),
+    ("rows_1024_q8", synth.Workload("r1k", 1, 8, 128, [1300]), 2),
 ]
 
 
@@ -229,6 +233,9 @@ FP8_CASES = [
     ("fp8_peaked", synth.Workload("p8", 2, 5, 96, [3000, 333], kv_dtype="fp8_e4m3",
                                   q_scale=8.0), 4),
     ("fp8_empty_splits", synth.Workload("e8", 2, 5, 32, [64, 200], kv_dtype="fp8_e4m3"), 9),
+    # 700 rows: 6 units of 128 (the last 60); 1024 rows: exactly 8
+    ("fp8_rows_700_q7", synth.Workload("r78", 2, 7, 100, [900, 450], kv_dtype="fp8_e4m3"), 2),
+    ("fp8_rows_1024_q8", synth.Workload("r1k8", 1, 8, 128, [1300], kv_dtype="fp8_e4m3"), 2),
 ]
 
 
