@@ -106,8 +106,23 @@ static double plan_unit_cost(mla_kv_dtype kv_dtype) {
   return kv_dtype == MLA_KV_FP8_E4M3 ? kPlanUnitCostFp8 : kPlanUnitCostBf16;
 }
 
-// List-scheduling makespan of units in launch order on `slots` slots.
-static double makespan(const std::vector<double>& costs, int slots) {
+// The planners score each candidate plan by its list-scheduling makespan
+// plus a price per split, and keep the first candidate that beats the best
+// score so far by more than 1e-9.  A candidate whose makespan is known to
+// reach `cutoff` = best score - its split price (+ a relative margin far above
+// rounding) cannot win, so its schedule stops there: the chosen plan is the
+// one the full search gives.  A list schedule on m slots never ends before
+// max(total cost / m, largest unit cost), which prunes most candidates before
+// any scheduling.
+static double prune_cutoff(bool have_best, double best_score, double price) {
+  if (!have_best) return INFINITY;
+  return best_score - price + 1e-7 * std::max(1.0, std::fabs(best_score));
+}
+
+// List-scheduling makespan of units in launch order on `slots` slots, or
+// INFINITY once it is known to reach `cutoff`.
+static double makespan(const std::vector<double>& costs, int slots,
+                       double cutoff) {
   if (costs.empty()) return 0.0;
   std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
   const size_t n = std::min<size_t>((size_t)slots, costs.size());
@@ -117,6 +132,7 @@ static double makespan(const std::vector<double>& costs, int slots) {
     double t = heap.top() + c;
     heap.pop();
     end = std::max(end, t);
+    if (end >= cutoff) return INFINITY;
     heap.push(t);
   }
   return end;
@@ -159,23 +175,40 @@ int mla_plan_ex(int V, int q_len, int H, int rows_per_unit,
   const double rows = (double)V * q_len * H;
   double bestJ = 0, bestEff = 0, bestMs = 0;
   int bestS = 0;
+  int64_t sumP = 0, maxP = 0;
+  for (int v = 0; v < V; ++v) {
+    const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
+    const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+    sumP += P;
+    maxP = std::max(maxP, P);
+  }
   std::vector<double> costs;
   for (int S = 1; S <= s_max; ++S) {
+    const double price = lam * S * rows / 1024.0;
+    const double cutoff = prune_cutoff(bestS != 0, bestJ, price);
+    // Every part costs its pages + c0 and a request's parts hold all its
+    // pages, the largest ceil(P / S): the bound needs no cost list.
+    const double total_lb = (double)G * ((double)sumP + (double)V * S * c0);
+    const double cmax_lb = (double)((maxP + S - 1) / S) + c0;
+    if (std::max(total_lb / slots, cmax_lb) >= cutoff) continue;
     costs.clear();
-    double total = 0;
+    double total = 0, cmax = 0;
     for (int s = 0; s < S; ++s) {
       for (int v = 0; v < V; ++v) {
         const int64_t L = std::max<int32_t>(seq_lens_host[v], 0);
         const int64_t P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
         const double c = (double)((s + 1) * P / S - s * P / S) + c0;
+        cmax = std::max(cmax, c);
         for (int g = 0; g < G; ++g) {
           costs.push_back(c);
           total += c;
         }
       }
     }
-    const double ms = makespan(costs, slots);
-    const double J = ms + lam * S * rows / 1024.0;
+    if (std::max(total / slots, cmax) >= cutoff) continue;
+    const double ms = makespan(costs, slots, cutoff);
+    if (ms == INFINITY) continue;
+    const double J = ms + price;
     if (bestS == 0 || J < bestJ - 1e-9) {
       bestJ = J;
       bestS = S;
@@ -219,20 +252,27 @@ int mla_plan(int B, int q_len, int H, int num_shards, mla_kv_dtype kv_dtype,
 // increasing id (s * V + v) * U + u (part-major), or with `lpt` longest first
 // (equal costs by increasing id).  Returns the makespan, adds the unit costs
 // to *total and, when `order` is given, stores the ids in launch order.
+// Returns INFINITY (and no order) once the makespan is known to reach
+// `cutoff`.
 static double schedule_makespan(const std::vector<int64_t>& P, int U, int S,
                                 const std::vector<int64_t>& bnd, int slots,
                                 double c0, double c_empty, bool lpt,
-                                double* total, std::vector<int32_t>* order) {
+                                double* total, std::vector<int32_t>* order,
+                                double cutoff = INFINITY) {
   const size_t V = P.size();
   // the U units of one (s, v) share its cost and have consecutive ids
   std::vector<std::pair<double, int64_t>> groups;
   groups.reserve(V * (size_t)S);
+  double lower = 0, cmax = 0;
   for (int s = 0; s < S; ++s)
     for (size_t v = 0; v < V; ++v) {
       const int64_t pages = bnd[v * (S + 1) + s + 1] - bnd[v * (S + 1) + s];
-      groups.emplace_back(pages > 0 ? (double)pages + c0 : c_empty,
-                          (int64_t)s * (int64_t)V + (int64_t)v);
+      const double c = pages > 0 ? (double)pages + c0 : c_empty;
+      groups.emplace_back(c, (int64_t)s * (int64_t)V + (int64_t)v);
+      lower += c * U;
+      cmax = std::max(cmax, c);
     }
+  if (std::max(lower / slots, cmax) >= cutoff) return INFINITY;
   if (lpt)
     std::stable_sort(groups.begin(), groups.end(),
                      [](const std::pair<double, int64_t>& a,
@@ -249,6 +289,7 @@ static double schedule_makespan(const std::vector<int64_t>& P, int U, int S,
       const double t = heap.top() + g.first;
       heap.pop();
       end = std::max(end, t);
+      if (end >= cutoff) return INFINITY;
       heap.push(t);
       tot += g.first;
       if (order) order->push_back((int32_t)(g.second * U + u));
@@ -293,9 +334,12 @@ static int plan_parts_impl(int V, int q_len, int H, int rows_per_unit,
   std::vector<int64_t> bnd;
   auto consider = [&](int S) {
     double tot = 0;
+    const double price = lam * S * rows / 1024.0;
     const double ms =
-        schedule_makespan(P, U, S, bnd, slots, c0, kEmpty, lpt, &tot, nullptr);
-    const double J = ms + lam * S * rows / 1024.0;
+        schedule_makespan(P, U, S, bnd, slots, c0, kEmpty, lpt, &tot, nullptr,
+                          prune_cutoff(best.S != 0, bestJ, price));
+    if (ms == INFINITY) return;
+    const double J = ms + price;
     if (best.S == 0 || J < bestJ - 1e-9) {
       bestJ = J;
       best.S = S;
@@ -304,8 +348,23 @@ static int plan_parts_impl(int V, int q_len, int H, int rows_per_unit,
       best.bnd = bnd;
     }
   };
-  // Uniform deals.
+  // Uniform deals.  Request v's S parts hold its P pages, min(P, S) of them
+  // non-empty and none above ceil(P / S): the schedule's lower bound comes
+  // before any boundary is written.
   for (int S = 1; S <= s_max; ++S) {
+    if (best.S != 0) {
+      double lower = 0, cmax = 0;
+      for (int v = 0; v < V; ++v) {
+        const int64_t full = std::min<int64_t>(P[v], S);
+        lower += (double)P[v] + c0 * full + kEmpty * (S - full);
+        if (P[v] > 0) cmax = std::max(cmax, (double)((P[v] + S - 1) / S) + c0);
+        if (full < S) cmax = std::max(cmax, kEmpty);
+      }
+      lower *= U;
+      if (std::max(lower / slots, cmax) >=
+          prune_cutoff(true, bestJ, lam * S * rows / 1024.0))
+        continue;
+    }
     bnd.assign((size_t)V * (S + 1), 0);
     for (int v = 0; v < V; ++v)
       for (int k = 0; k <= S; ++k) bnd[(size_t)v * (S + 1) + k] = k * P[v] / S;
@@ -318,6 +377,26 @@ static int plan_parts_impl(int V, int q_len, int H, int rows_per_unit,
       const int64_t b = (Pmax * k + kCaps - 1) / kCaps;
       if (b == prev || b < 1) continue;
       prev = b;
+      if (best.S != 0) {
+        // The first part holds min(P, b) pages, the other S - 1 parts the
+        // rest, min(rest, S - 1) of them non-empty, none above
+        // ceil(rest / (S - 1)).
+        double lower = 0, cmax = 0;
+        for (int v = 0; v < V; ++v) {
+          const int64_t first = std::min(P[v], b), rest = P[v] - first;
+          const int64_t full = std::min<int64_t>(rest, S - 1);
+          lower += (double)P[v] + c0 * ((first > 0) + full) +
+                   kEmpty * ((first == 0) + (S - 1 - full));
+          cmax = std::max(cmax, first > 0 ? (double)first + c0 : kEmpty);
+          if (rest > 0)
+            cmax = std::max(cmax, (double)((rest + S - 2) / (S - 1)) + c0);
+          if (full < S - 1) cmax = std::max(cmax, kEmpty);
+        }
+        lower *= U;
+        if (std::max(lower / slots, cmax) >=
+            prune_cutoff(true, bestJ, lam * S * rows / 1024.0))
+          continue;
+      }
       bnd.assign((size_t)V * (S + 1), 0);
       for (int v = 0; v < V; ++v) {
         const int64_t first = std::min(P[v], b), rest = P[v] - first;

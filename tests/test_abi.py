@@ -206,6 +206,31 @@ def test_sched_planner_matches_reference(lib):
         assert eff == pytest.approx(eff2, rel=1e-6)
 
 
+def test_sched_planner_full_search_matches_reference(lib):
+    """The library's own search depth (up to 64 parts, 8 per request), where
+    its bounds skip most candidates, against the reference that scores every
+    candidate: a ragged batch (FP8 units), dp16 and a DCP-shaped batch."""
+    ragged = [1198, 152649, 2686, 60048, 10681, 170646, 4569, 880, 33000,
+              7, 199999, 5120, 64, 91000, 2300, 140000, 65, 15000, 700, 120000,
+              4000, 77777, 1500, 30000]
+    dcp = [(100_000 - s + 7) // 8 for _ in range(32) for s in range(8)]
+    cases = [(ragged, 96, 5, 76, 128, 32.0), ([100_000] * 16, 96, 5, 36, 256, 16.0),
+             (dcp, 96, 5, 36, 256, 16.0)]
+    for lens, H, q, slots, rpu, c0 in cases:
+        S, bnd, work, eff, ms = mla.plan_sched_ex(lens, q, H, slots, 64, 8, c0,
+                                                  1.0, rows_per_unit=rpu)
+        S2, bnd2, work2, eff2, ms2 = ref.plan_sched(lens, H, q, slots, 64, 8, c0,
+                                                    1.0, rows_per_unit=rpu)
+        assert (S, ms) == (S2, ms2), (len(lens), slots, rpu)
+        assert bnd.tolist() == bnd2 and work.tolist() == work2
+        assert eff == pytest.approx(eff2, rel=1e-6)
+        S, bnd, eff, ms = mla.plan_parts_ex(lens, q, H, slots, 64, 8, c0, 1.0,
+                                            rows_per_unit=rpu)
+        S2, bnd2, eff2, ms2 = ref.plan_parts(lens, H, q, slots, 64, 8, c0, 1.0,
+                                             rows_per_unit=rpu)
+        assert (S, ms) == (S2, ms2) and bnd.tolist() == bnd2
+
+
 def test_sched_planner_defaults_and_capacity(lib):
     lens = [3000, 90_000, 700]
     for kv, U in (("bf16", 2), ("fp8_e4m3", 4)):
