@@ -14,8 +14,11 @@ value      attention TFLOP/s over all ranks, inputs resident in HBM
            (algorithmic FLOPs 2*H*(576+512)*sum_b sum_i (L_b - q_len + 1 + i)
            per step / device time), max over ranks of the timed region
 e2e        the same metric through the public API from pinned host buffers:
-           every step copies the queries, page table and lengths to the device
-           and reads the output and LSE back (the KV cache is resident state)
+           every step plans itself on the host, copies the queries, page
+           table, lengths and plan to the device and reads the output and LSE
+           back (the KV cache is resident state); consecutive steps overlap on
+           three streams, as a serving loop runs them ("serial": the same
+           steps one at a time, i.e. one step's latency)
 roofline   the partial-decode kernel alone: algorithmic FLOPs / its mean
            CUDA-event duration inside the timed region vs measured bf16 peak
 cpu_baseline  the fp64 oracle on a bounded sample of rows, host cores
@@ -575,6 +578,137 @@ def run_projections(args):
     return 0
 
 
+def time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
+             status, dev, fl, world, dist):
+    """End-to-end throughput through the public API from pinned host buffers.
+
+    Every step plans itself on the host from the host lengths (when the run
+    uses a planner), copies its queries, page table, lengths, visibility
+    limits and plan to the device, decodes, and reads its output and LSE back;
+    the KV cache is resident state.  Consecutive steps overlap as a serving
+    loop runs them: two sets of device buffers, uploads on one stream, the
+    decode on a second, downloads on a third, ordered by events, while the
+    host plans the next step.  Every step's plan and copies lie inside the
+    timed region."""
+    import numpy as np
+    import torch
+    fixed = args.parts_cut > 0 or args.splits > 0 or bool(wl.num_splits)
+
+    def replan():
+        if fixed:
+            return None, None
+        if args.planner == "parts":
+            S2, b2, _ = mla.plan_parts(wl.B, wl.q_len, wl.H, lens, wl.num_shards,
+                                       kv_dtype=wl.kv_dtype)
+            w2 = None
+        else:
+            S2, b2, w2, _ = mla.plan_sched(wl.B, wl.q_len, wl.H, lens,
+                                           wl.num_shards, kv_dtype=wl.kv_dtype)
+        if S2 != S:
+            raise RuntimeError(f"the plan changed between steps: {S2} != {S}")
+        return b2, w2
+
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = [pin(batch.q_nope), pin(batch.q_rope), pin(batch.req_to_token),
+               pin(batch.seq_lens)]
+    if batch.kv_limit is not None:
+        host_in.append(pin(batch.kv_limit))
+    b0, w0 = replan()
+    h_sp = [torch.from_numpy(b0.copy()).pin_memory() if b0 is not None else None
+            for _ in range(2)]
+    h_wk = [torch.from_numpy(w0.copy()).pin_memory() if w0 is not None else None
+            for _ in range(2)]
+    d_in = [[torch.empty_like(h, device=dev) for h in host_in] for _ in range(2)]
+    d_sp = [torch.empty_like(h, device=dev) if h is not None else None for h in h_sp]
+    d_wk = [torch.empty_like(h, device=dev) if h is not None else None for h in h_wk]
+    O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
+                         dtype=torch.float32, device=dev)
+    LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
+                           dtype=torch.float32, device=dev)
+    d_out = [torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16,
+                         device=dev) for _ in range(2)]
+    d_lse = [torch.empty((wl.B, wl.q_len, wl.H), dtype=torch.float32, device=dev)
+             for _ in range(2)]
+    h_out = [torch.empty_like(d, device="cpu").pin_memory() for d in d_out]
+    h_lse = [torch.empty_like(d, device="cpu").pin_memory() for d in d_lse]
+    s_in, s_dec, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "dec", "out")}
+    for k in ev:  # every event recorded once before the first wait on it
+        for e in ev[k]:
+            e.record()
+    bi = sum(h.numel() * h.element_size() for h in host_in)
+    bi += sum(h.numel() * h.element_size() for h in (h_sp[0], h_wk[0]) if h is not None)
+    bo = sum(d.numel() * d.element_size() for d in (d_out[0], d_lse[0]))
+
+    def e2e_step(k):
+        i = k & 1
+        b2, w2 = replan()
+        ev["in"][i].synchronize()  # step k - 2's uploads have read the staging
+        if b2 is not None:
+            h_sp[i].numpy()[...] = b2
+        if w2 is not None:
+            h_wk[i].numpy()[...] = w2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev["dec"][i])  # step k - 2's decode is done with set i
+            for d, h in zip(d_in[i], host_in):
+                d.copy_(h, non_blocking=True)
+            if b2 is not None:
+                d_sp[i].copy_(h_sp[i], non_blocking=True)
+            if w2 is not None:
+                d_wk[i].copy_(h_wk[i], non_blocking=True)
+            ev["in"][i].record(s_in)
+        q, r, r2t, sl = d_in[i][:4]
+        kv_limit = d_in[i][4] if batch.kv_limit is not None else None
+        sp = d_sp[i] if b2 is not None else split_pages
+        wk = d_wk[i] if w2 is not None else work
+        with torch.cuda.stream(s_dec):
+            s_dec.wait_event(ev["in"][i])
+            s_dec.wait_event(ev["out"][i])  # step k - 2's output was read back
+            if args.fused:
+                mla.decode_fused(q, r, batch.kv, batch.kv_scale, r2t, sl, kv_limit,
+                                 S, wl.sm_scale, wl.num_shards, O_part, LSE_part,
+                                 counters, d_out[i], d_lse[i], status,
+                                 split_pages=sp, work=wk)
+            else:
+                mla.decode_partial(q, r, batch.kv, batch.kv_scale, r2t, sl,
+                                   kv_limit, S, wl.sm_scale, wl.num_shards, O_part,
+                                   LSE_part, status, split_pages=sp, work=wk)
+                mla.lse_combine(O_part, LSE_part, d_out[i], d_lse[i])
+            ev["dec"][i].record(s_dec)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["dec"][i])
+            h_out[i].copy_(d_out[i], non_blocking=True)
+            h_lse[i].copy_(d_lse[i], non_blocking=True)
+            ev["out"][i].record(s_out)
+
+    for k in range(3):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    n_e2e = max(10, args.steps // 2)
+    t0 = time.perf_counter()
+    for k in range(n_e2e):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e2e_s = slowest_rank(time.perf_counter() - t0, dist, dev)
+    # The same steps one at a time (each waited for before the next is
+    # planned): the latency of one step, and what the overlap hides.
+    t0 = time.perf_counter()
+    for k in range(n_e2e):
+        e2e_step(k)
+        torch.cuda.synchronize()
+    serial_s = slowest_rank(time.perf_counter() - t0, dist, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the e2e loop")
+    return {"value": job_tflops(fl, n_e2e, world, e2e_s), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n_e2e,
+            "plan": "fixed" if fixed else "per step on the host",
+            "overlap": "uploads, decode and downloads of consecutive steps on "
+                       "three streams, two buffer sets",
+            "ms_per_step": e2e_s * 1e3 / n_e2e,
+            "serial": {"value": job_tflops(fl, n_e2e, world, serial_s),
+                       "ms_per_step": serial_s * 1e3 / n_e2e}}
+
+
 def main():
     args = parse()
     if args.projections:
@@ -730,48 +864,8 @@ def main():
     # end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        hq = batch.q_nope.cpu().pin_memory()
-        hr = batch.q_rope.cpu().pin_memory()
-        ht = batch.req_to_token.cpu().pin_memory()
-        hs = batch.seq_lens.cpu().pin_memory()
-        ho = torch.empty_like(out, device="cpu").pin_memory()
-        hl = torch.empty_like(lse, device="cpu").pin_memory()
-        dq, dr = torch.empty_like(batch.q_nope), torch.empty_like(batch.q_rope)
-        dt_, ds = torch.empty_like(batch.req_to_token), torch.empty_like(batch.seq_lens)
-        bi = sum(x.numel() * x.element_size() for x in (hq, hr, ht, hs))
-        bo = sum(x.numel() * x.element_size() for x in (ho, hl))
-
-        def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dr.copy_(hr, non_blocking=True)
-            dt_.copy_(ht, non_blocking=True)
-            ds.copy_(hs, non_blocking=True)
-            if args.fused:
-                mla.decode_fused(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
-                                 batch.kv_limit, S, wl.sm_scale, wl.num_shards,
-                                 O_part, LSE_part, counters, out, lse, status,
-                                 split_pages=split_pages, work=work)
-            else:
-                mla.decode_partial(dq, dr, batch.kv, batch.kv_scale, dt_, ds,
-                                   batch.kv_limit, S, wl.sm_scale, wl.num_shards,
-                                   O_part, LSE_part, status, split_pages=split_pages,
-                                   work=work)
-                mla.lse_combine(O_part, LSE_part, out, lse)
-            ho.copy_(out, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        n_e2e = max(10, args.steps // 2)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_s = slowest_rank(time.perf_counter() - t0, dist, dev)
-        e2e = {"value": job_tflops(fl, n_e2e, world, e2e_s), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "steps": n_e2e}
+        e2e = time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
+                       status, dev, fl, world, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
