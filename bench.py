@@ -642,6 +642,11 @@ def time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
 
     def e2e_step(k):
         i = k & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev["dec"][i])  # step k - 2's decode is done with set i
+            for d, h in zip(d_in[i], host_in):
+                d.copy_(h, non_blocking=True)
+        # the host plans while the inputs upload
         b2, w2 = replan()
         ev["in"][i].synchronize()  # step k - 2's uploads have read the staging
         if b2 is not None:
@@ -649,9 +654,6 @@ def time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
         if w2 is not None:
             h_wk[i].numpy()[...] = w2
         with torch.cuda.stream(s_in):
-            s_in.wait_event(ev["dec"][i])  # step k - 2's decode is done with set i
-            for d, h in zip(d_in[i], host_in):
-                d.copy_(h, non_blocking=True)
             if b2 is not None:
                 d_sp[i].copy_(h_sp[i], non_blocking=True)
             if w2 is not None:
