@@ -435,6 +435,12 @@ def decode(batch, num_splits: Optional[int] = None, simt: bool = False,
     launch order (mla_plan_sched; the CUDA-core path takes the parts only);
     with num_splits and no split_pages the pages are dealt uniformly.
     Returns (out bf16 [B, q, H, 512], lse fp32 [B, q, H], num_splits).
+
+    Planning reads the lengths back from the device and uploads the plan
+    synchronously, so the host waits for earlier work on the stream.  A
+    serving loop keeps the lengths on the host and calls plan_sched,
+    decode_partial and lse_combine itself, with the plan uploaded from pinned
+    memory on its own stream (bench.py's end-to-end loop does that).
     """
     wl = batch.wl
     if num_splits is None and wl.num_splits:
