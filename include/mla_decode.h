@@ -127,6 +127,11 @@ int mla_plan_heuristic(int B, int q_len);
  *   J(S) = makespan(S) + lam * S * rows / 1024,   rows = V * q_len * H,
  * (the second term prices the partial outputs each extra split writes and
  * the combine re-reads).  The smallest J wins, ties go to fewer splits.
+ * All three planners skip a candidate whose lower bound max(total cost /
+ * slots, largest unit cost) + its split price cannot beat the best J so far,
+ * and stop a schedule once it reaches that J: the result is the full
+ * search's (about 0.2 ms of host time for 16 requests, 2 ms for 1024
+ * virtual requests, on 36 slots).
  *   rows_per_unit  query rows per work unit (> 0)
  *   seq_lens_host  host int32 [V] (V = num_shards * B virtual requests)
  *   slots          concurrent cluster slots (> 0)
