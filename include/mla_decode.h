@@ -33,7 +33,8 @@
  *   - Device pointers are CUDA device memory owned by the caller; host
  *     pointers are marked "host".  The library allocates nothing and never
  *     frees caller memory.  It keeps no state between calls, except the
- *     static scratch of mla_decode_scratch (zero again after every call).
+ *     static scratch of mla_decode_scratch (whose counters every call of it
+ *     clears before its decode).
  *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
  *     checked on the host before anything is launched; on error nothing is
  *     launched and mla_last_error_string() (thread-local) says why.
@@ -312,7 +313,11 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  *   LSE_part         fp32 [num_splits, num_shards, B, q_len, H]
  *   status           device int or NULL (MLA_STATUS_* bits are OR-ed in)
  * Rows of slots beyond a request's length (the tail of its last page) are
- * never used, whatever they hold.
+ * never used, whatever they hold.  A token that query i may not see adds
+ * nothing to its rows, whatever the token's row holds (NaN included): the
+ * rows of query i are bitwise those of a cache without that token.  A NaN
+ * score that a row does see makes that row NaN (O_part and LSE_part), as the
+ * definition gives.
  * Precision with FP8 KV: the contractions run on FP8 tensor cores over the
  * stored E4M3 bytes.  Each query row is represented as 2^e (hi + lo), two
  * E4M3 parts with a power-of-two row scale: exact for every element at least
@@ -343,8 +348,10 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
  *                    workspace for the parts (same sizes)
  *   counters   device int32 [B * ceil(q_len * H / 128)], 4-B aligned:
  *              all zero before the call; every call leaves them zero (also
- *              when a bounded wait timed out).  Two calls that may run at
- *              the same time must not share counters or workspace.
+ *              when a bounded wait timed out) as long as its work list
+ *              holds every unit once; after a call that set
+ *              MLA_STATUS_BAD_WORK, zero them again.  Two calls that may run
+ *              at the same time must not share counters or workspace.
  *   out        bf16 [B, q_len, H, 512] (round to nearest even), 16-B aligned
  *   lse_out    fp32 [B, q_len, H] (natural log) or NULL
  * Same errors as mla_decode_partial; MLA_ERR_INVALID_ARG if counters or out
@@ -364,12 +371,17 @@ int mla_decode(const void* q_nope_absorbed, const void* q_rope,
 /*
  * mla_decode with no workspace argument and no allocation: the arrival
  * counters and the per-part (O, LSE) results live in one static device array
- * of the library (MLA_SCRATCH_BYTES, 256-byte aligned, one per device,
- * zero-initialised when the library's device code loads), whose address is
- * looked up once per device with cudaGetSymbolAddress.  The call makes no
- * cudaMalloc or cudaFree.  The pages have no counterpart: their kernels
- * take their workspace from the serving framework; this entry point is the
- * library's own, for callers that hold no workspace.
+ * of the library (MLA_SCRATCH_BYTES, 256-byte aligned, one per device),
+ * whose address is looked up with cudaGetSymbolAddress by the first call on
+ * each device (make that first call before any stream capture; the address
+ * is kept for the life of the process, so do not call this again on a
+ * device after cudaDeviceReset).  Each call first clears the counters on
+ * its stream (cudaMemsetAsync, no allocation), so a call that left them
+ * non-zero (a work list naming no unit or one unit twice, a timed-out wait)
+ * does not affect the next.  The call makes no cudaMalloc or cudaFree.  The
+ * pages have no counterpart: their kernels take their workspace from the
+ * serving framework; this entry point is the library's own, for callers that
+ * hold no workspace.
  *   arguments     as mla_decode, without O_part, LSE_part and counters
  * Size limit: the call needs mla_scratch_bytes(B, q_len, H, num_shards,
  * num_splits) bytes; above MLA_SCRATCH_BYTES it returns MLA_ERR_SCRATCH
@@ -460,7 +472,8 @@ int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
  * num_parts partials (part j at O_part + j*rows*512, LSE_part + j*rows):
  *   M = max_j LSE_j; w_j = exp(LSE_j - M) (parts with LSE = -inf skipped);
  *   out = sum_j w_j O_j / sum_j w_j;  lse_out = M + ln sum_j w_j.
- * All parts empty: out = 0, lse_out = -inf.
+ * All parts empty: out = 0, lse_out = -inf.  A part with LSE = NaN makes the
+ * row NaN (out and lse_out).
  *   O_part   fp32 [num_parts, rows, 512], 16-B aligned
  *   LSE_part fp32 [num_parts, rows]
  *   out      bf16 [rows, 512] (round to nearest even), 16-B aligned
@@ -485,6 +498,28 @@ int mla_debug_gather(const void* kv_pages, mla_kv_dtype kv_dtype,
                      int64_t r2t_stride, const int32_t* seq_lens,
                      const int64_t* row_offset, int V, int page_size,
                      void* dense_out, mla_stream_t stream);
+
+/*
+ * Test entry point of the bounded waits (the pages define no failure
+ * handling; this is the library's own).  Every pipeline wait of the decode
+ * kernels gives up after 2 s of %globaltimer, or as soon as another warp of
+ * its CTA has given up (the CTA's abort flag), and then sets
+ * MLA_STATUS_WAIT_TIMEOUT instead of spinning on.  This launches one CTA of
+ * 64 threads whose thread 0 runs that same wait on a barrier phase that
+ *   mode 0: nothing completes: the wait gives up after its 2 s limit and
+ *           MLA_STATUS_WAIT_TIMEOUT is OR-ed into *status;
+ *   mode 1: nothing completes, but another warp raises the CTA's abort flag
+ *           after delay_us: the wait gives up then, status as in mode 0;
+ *   mode 2: another warp completes after delay_us: the wait succeeds and
+ *           *status is not touched.
+ *   delay_us    in [0, 1000000] (else MLA_ERR_INVALID_ARG)
+ *   status      device int, 4-B aligned (required)
+ *   elapsed_ns  device uint64, 8-B aligned (required): the wait's duration
+ * The kernel holds no tensor memory and starts no TMA, bulk copy or MMA, so
+ * it always ends and leaves the context usable.
+ */
+int mla_debug_wait(int mode, int delay_us, int* status, uint64_t* elapsed_ns,
+                   mla_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -5,7 +5,9 @@
 // Row `row` of `rows` over P parts (part j at O_part + j*rows*512,
 // LSE_part + j*rows): M = max_j LSE_j; w_j = exp(LSE_j - M) (parts with
 // LSE = -inf have weight 0 and are never read); out = sum_j w_j O_j / sum_j
-// w_j in bf16 (round to nearest even); lse = M + ln sum_j w_j.  One warp per
+// w_j in bf16 (round to nearest even); lse = M + ln sum_j w_j.  A part whose
+// LSE is NaN (its range held a NaN score the row sees) makes the whole row
+// NaN, out and lse, as the unsplit definition would.  One warp per
 // row: lane j reads LSE_j (all weights in one round trip, reduced with
 // shuffles), then each lane owns four float4 columns of every part
 // (coalesced 512-byte loads), two parts' loads in flight at a time, parts
@@ -43,11 +45,27 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
   constexpr uint32_t kAll = 0xffffffffu;
   // M = max_j LSE_j: lane j % 32 reads LSE_j (one round trip per 32 parts)
   float M = -INFINITY;
+  bool nan = false;
   for (int j0 = 0; j0 < P; j0 += 32)
-    if (j0 + lane < P)
-      M = fmaxf(M, load_part<kCoherent>(LSE_part + (int64_t)(j0 + lane) * rows + row));
+    if (j0 + lane < P) {
+      const float l = load_part<kCoherent>(LSE_part + (int64_t)(j0 + lane) * rows + row);
+      nan |= l != l;
+      M = fmaxf(M, l);
+    }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+  if (__any_sync(kAll, nan)) {
+    const __nv_bfloat162 qnan = __float2bfloat162_rn(__int_as_float(0x7fc00000));
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = 2 * (lane + 32 * k);
+      dst[c] = qnan;
+      dst[c + 1] = qnan;
+    }
+    if (lse_out && lane == 0) lse_out[row] = __int_as_float(0x7fc00000);
+    return;
+  }
 
   float4 acc[4];
 #pragma unroll

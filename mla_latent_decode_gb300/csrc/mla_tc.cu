@@ -97,8 +97,8 @@ struct __align__(1024) Smem {
   uint64_t pempty[kNP];     // S-CTAs: slot k consumed by the O pair
   uint64_t drain;           // O-CTAs: all earlier pair MMAs completed
   uint64_t corr_done;       // rank 2: both O-CTAs finished a rescale
-  uint64_t tail_full;       // O-CTAs: the last, partial page landed here
-  uint64_t tail_ready;      // rank 2: both halves of that page sanitised
+  uint64_t tail_full[kStagesO];   // O-CTAs: a page to sanitise landed here
+  uint64_t tail_ready[kStagesO];  // rank 2: both halves of that page sanitised
   uint64_t fin_full;        // O-CTAs: 1/l of every row arrived
   uint64_t epi_go;          // O-CTAs: the epilogue may read O (warps 4-7)
   uint64_t qready;          // rank 0: both S-CTAs' Q rows are in place
@@ -216,7 +216,9 @@ __device__ __forceinline__ void signal_abort(Smem& s, const TcParams& p,
 // CTA's row group is 2u + (rank & 1).
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
+  int m_san;  // first page of the range holding a token at or past nmin
   int64_t L, p0;
+  int64_t nmin;  // fewest tokens any query of the request sees
 };
 
 // The cluster's unit id, or -1 for a work-list entry outside [0, units).
@@ -250,11 +252,33 @@ __device__ __forceinline__ Work unit_work(const TcParams& p, int unit,
       p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
       p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
+  // Tokens in [nmin, L) are visible to some query rows of the request and
+  // masked for others; tokens at or past L to none.  The pages that hold any
+  // of them are sanitised before P V reads them (producer_o).
+  int64_t nmin = L - p.q_len + 1;
+  if (p.kv_limit) {
+    nmin = L;
+    for (int i = 0; i < p.q_len; ++i) {
+      const int64_t n = p.kv_limit[(int64_t)w.v * p.q_len + i];
+      nmin = n < nmin ? n : nmin;
+    }
+  }
+  w.nmin = nmin < 0 ? 0 : (nmin > L ? L : nmin);
+  const int64_t m_san = w.nmin / kPage - w.p0;
+  w.m_san = (int)(m_san < 0 ? 0 : (m_san > w.npages ? w.npages : m_san));
   return w;
 }
 
 __device__ __forceinline__ int tile_pages(const Work& w, int j) {
   return min(kTilePages, w.npages - j * kTilePages);
+}
+
+// Two bf16 values with every non-finite one (NaN, +-Inf) replaced by +0.
+__device__ __forceinline__ uint32_t bf16x2_finite_or_zero(uint32_t x) {
+  uint32_t keep = 0;
+  if ((x & 0x7F80u) != 0x7F80u) keep |= 0xFFFFu;
+  if ((x & 0x7F800000u) != 0x7F800000u) keep |= 0xFFFF0000u;
+  return x & keep;
 }
 
 // Base slot of page m of the unit's range, or -1 if it lies outside the pool.
@@ -323,11 +347,17 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
 // ------------------------------------------------------- O-CTA producers ---
 // Rank 2+h loads dims [256n + 128h, +128) of every page for n = 0, 1: one
 // stage of 4 boxes (box 2n + i = dims 256n + 128h + 64i), bytes of both CTAs
-// completing on rank 2's full barrier.  A request's last page may be partly
-// filled: rows past its length can hold anything (even NaN) and 0 * NaN
-// would poison O = P V, so that page lands on the CTA's own tail barrier
-// instead, its rows past the length are zeroed, and both CTAs then report to
-// rank 2 (tail_ready).
+// completing on rank 2's full barrier.  A masked token gets p = 0 exactly,
+// but 0 * NaN (or 0 * Inf) would still poison O = P V.  So the pages from
+// the one holding token nmin onwards (the draft tokens that only some query
+// rows see, and the request's partly filled last page) land on the CTA's
+// own tail barrier of their stage instead: rows at or past the length,
+// which can hold anything, are zeroed; rows in [nmin, L) keep their finite
+// values and get +0 for every non-finite one.  A query that sees such a
+// token has a NaN score for it already (the S side reads the bytes as they
+// are), which makes its whole row NaN, as the definition says; a query that
+// does not see it now adds exactly 0.  Both CTAs then report to rank 2
+// (tail_ready of the stage).
 __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane) {
@@ -344,11 +374,12 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     const int32_t b = __shfl_sync(kFull, cur, m & 31);
     const int32_t y = b < 0 ? (int32_t)p.num_slots : b;
     const int64_t t0 = (w.p0 + m) * kPage;
-    const bool partial = t0 + kPage > w.L;
+    const bool san = m >= w.m_san;
+    const uint32_t tail_full = smem_u32(&s.tail_full[stage]);
     if (lane == 0) {
       if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
-        if (partial)
-          mbar_arrive_expect_tx(smem_u32(&s.tail_full), kBoxesO * kBoxBytes);
+        if (san)
+          mbar_arrive_expect_tx(tail_full, kBoxesO * kBoxBytes);
         else if (rank == 2)
           mbar_arrive_expect_tx(smem_u32(&s.full[stage]),
                                 2 * kBoxesO * kBoxBytes);
@@ -360,8 +391,8 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
     if (ok && lane < kBoxesO) {
       const uint32_t dst = smem_u32(s.ring[stage * kBoxesO + lane]);
       const int x = 256 * (lane >> 1) + 128 * h + 64 * (lane & 1);
-      if (partial)
-        tma_load_2d(dst, map, smem_u32(&s.tail_full), x, y);
+      if (san)
+        tma_load_2d(dst, map, tail_full, x, y);
       else
         tma_load_2d_pair(dst, map, full0 + 8u * stage, x, y);
     }
@@ -370,19 +401,30 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
       stage = 0;
       phase ^= 1u;
     }
-    if (!ok || !partial) continue;
-    // The partial page is the request's last: zero its rows past the length.
-    const int keep = (int)(w.L - t0);
-    if (!mbar_wait(smem_u32(&s.tail_full), 0, &s.abort_flag)) ok = false;
+    if (!ok || !san) continue;
+    // Pages m_san, m_san + 1, ... all take this path, so this is use
+    // (m - m_san) / 4 of the stage's tail barriers.
+    const uint32_t use = (uint32_t)(m - w.m_san) / kStagesO;
+    if (!mbar_wait(tail_full, use & 1u, &s.abort_flag)) ok = false;
+    const int keep = (int)(w.L - t0 < kPage ? w.L - t0 : kPage);
+    const int64_t lo64 = w.nmin - t0;
+    const int lo = lo64 <= 0 ? 0 : (lo64 >= keep ? keep : (int)lo64);
     for (int q = 0; q < kBoxesO; ++q) {
+      // A token row is 128 contiguous bytes of the box (the swizzle only
+      // permutes its 16-byte chunks), 8 chunks.
       uint4* box = reinterpret_cast<uint4*>(s.ring[st0 * kBoxesO + q]);
+      for (int k = lo * 8 + lane; k < keep * 8; k += 32) {
+        const uint4 x = box[k];
+        box[k] = make_uint4(bf16x2_finite_or_zero(x.x), bf16x2_finite_or_zero(x.y),
+                            bf16x2_finite_or_zero(x.z), bf16x2_finite_or_zero(x.w));
+      }
       for (int k = keep * 8 + lane; k < kPage * 8; k += 32)
         box[k] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     __syncwarp();
     ok = __all_sync(kFull, ok);
-    if (ok && lane == 0) arrive_leader(smem_u32(&s.tail_ready), rank, 2);
+    if (ok && lane == 0) arrive_leader(smem_u32(&s.tail_ready[st0]), rank, 2);
   }
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
@@ -681,10 +723,11 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     if (row_ok) {
       const int64_t rows = (int64_t)p.B * p.q_len * p.H;
       const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
+      // no visible token: -inf; a NaN sum (a NaN score seen) stays NaN
       p.LSE_part[part * rows + qrow] =
-          lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+          lt == 0.f ? -INFINITY : (m_ref + log2f(lt)) * 0.69314718055994531f;
     }
-    s.fin[r] = lt > 0.f ? 1.f / lt : 0.f;
+    s.fin[r] = lt == 0.f ? 0.f : 1.f / lt;
     fence_proxy_async_smem();
     named_bar_sync(2, 128);
     if (warp == 4 && lane == 0 && !s.abort_flag)
@@ -709,7 +752,6 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
                                       const Work& w, uint32_t tmem,
                                       uint32_t rank) {
   uint32_t stage = 0, phase = 0, ev = 0;
-  const bool has_tail = (w.p0 + w.npages) * kPage > w.L;
   bool ok = true;
   const uint32_t drain3 = mapa(smem_u32(&s.drain), 3);
   // Each P message lands by a bulk copy whose bytes complete on pfull[k];
@@ -747,9 +789,11 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       }
       ++ev;
     }
-    const bool tail = has_tail && m == w.npages - 1;
-    if (tail ? !mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)
-             : !mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+    // a page from m_san on arrives sanitised by both producers (tail_ready)
+    const bool san = m >= w.m_san;
+    if (san ? !mbar_wait(smem_u32(&s.tail_ready[stage]),
+                         ((uint32_t)(m - w.m_san) / kStagesO) & 1u, &s.abort_flag)
+            : !mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
       ok = false;
       break;
     }
@@ -946,8 +990,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&s.drain), 2);      // pair commit + rank 2's arrive
     mbar_init(smem_u32(&s.corr_done), 8);  // 4 correction warps x 2 O-CTAs
-    mbar_init(smem_u32(&s.tail_full), 1);
-    mbar_init(smem_u32(&s.tail_ready), 2);
+    for (int i = 0; i < kStagesO; ++i) {
+      mbar_init(smem_u32(&s.tail_full[i]), 1);
+      mbar_init(smem_u32(&s.tail_ready[i]), 2);
+    }
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.epi_go), 4);
     mbar_init(smem_u32(&s.qready), 16);

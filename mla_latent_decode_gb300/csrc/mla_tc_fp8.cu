@@ -294,8 +294,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
 // Per-pair work description, identical on both CTAs of the pair.
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
+  int m_san;  // first page of the range holding a token at or past nmin
   int64_t L, p0;
-  bool tail;  // the split's last page is the request's partial last page
+  int64_t nmin;  // fewest tokens any query of the request sees
 };
 
 // The pair's unit id (split, virtual request v, row group g) = (split * V +
@@ -329,8 +330,31 @@ __device__ __forceinline__ Work pair_work(const TcParams& p, int pair) {
       p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
       p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
-  w.tail = w.npages > 0 && p1 == P && (L % kPage) != 0;
+  // Tokens in [nmin, L) are visible to some query rows of the request and
+  // masked for others; tokens at or past L to none.  The pages that hold any
+  // of them are sanitised before P V reads them (tail_warp).
+  int64_t nmin = L - p.q_len + 1;
+  if (p.kv_limit) {
+    nmin = L;
+    for (int i = 0; i < p.q_len; ++i) {
+      const int64_t n = p.kv_limit[(int64_t)w.v * p.q_len + i];
+      nmin = n < nmin ? n : nmin;
+    }
+  }
+  w.nmin = nmin < 0 ? 0 : (nmin > L ? L : nmin);
+  const int64_t m_san = w.nmin / kPage - w.p0;
+  w.m_san = (int)(m_san < 0 ? 0 : (m_san > w.npages ? w.npages : m_san));
   return w;
+}
+
+// Four E4M3 bytes with every NaN code (S.1111.111; E4M3 has no infinity)
+// replaced by 0.
+__device__ __forceinline__ uint32_t e4m3x4_nan_to_zero(uint32_t x) {
+  uint32_t keep = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (((x >> (8 * k)) & 0x7Fu) != 0x7Fu) keep |= 0xFFu << (8 * k);
+  return x & keep;
 }
 
 __device__ __forceinline__ int tile_pages(const Work& w, int j) {
@@ -452,7 +476,11 @@ __device__ __forceinline__ void producer_o(Smem& s, const CUtensorMap* map,
 // length (their slots are undefined; 0 keeps every product finite) and of
 // pages the tile lacks; track the running max |scale| over the split and its
 // exponent g (max |scale| 2^g in [0.5, 1)); publish the tile's scale * 2^g
-// as f16 pairs (the factor the packers apply to p) and g.
+// as f16 pairs (the factor the packers apply to p) and g.  A non-finite scale
+// of a token the request holds stays in tscale, so the scores of the rows
+// that see the token are NaN (as the definition gives); it counts as 0 for g
+// and for the factor, so the rows that do not see it (p = 0) add exactly 0
+// and keep their units.
 __device__ __forceinline__ void scale_warp(Smem& s, const TcParams& p,
                                            const Work& w, uint32_t rank,
                                            int lane) {
@@ -475,9 +503,11 @@ __device__ __forceinline__ void scale_warp(Smem& s, const TcParams& p,
     for (int i = 0; i < 4; ++i) {  // token pair q = lane + 32 i
       const int t = 2 * (lane + 32 * i);
       const float2 x = *reinterpret_cast<const float2*>(&s.tscale[ts][t]);
-      v[2 * i] = t < valid ? x.x : 0.f;
-      v[2 * i + 1] = t + 1 < valid ? x.y : 0.f;
-      *reinterpret_cast<float2*>(&s.tscale[ts][t]) = make_float2(v[2 * i], v[2 * i + 1]);
+      const float x0 = t < valid ? x.x : 0.f, x1 = t + 1 < valid ? x.y : 0.f;
+      *reinterpret_cast<float2*>(&s.tscale[ts][t]) = make_float2(x0, x1);
+      // finite part only: NaN and +-Inf compare false
+      v[2 * i] = fabsf(x0) <= 3.402823466e38f ? x0 : 0.f;
+      v[2 * i + 1] = fabsf(x1) <= 3.402823466e38f ? x1 : 0.f;
       mx = max3(mx, fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
     }
 #pragma unroll
@@ -875,10 +905,11 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 #pragma unroll
         for (int k = 0; k < kPartials; ++k) lt += s.xch[k][row];
         if (row < w.nrows)
+          // no visible token: -inf; a NaN sum (a NaN score seen) stays NaN
           p.LSE_part[prt * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + row] =
-              lt > 0.f ? (m + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+              lt == 0.f ? -INFINITY : (m + log2f(lt)) * 0.69314718055994531f;
         // O (units 2^(m_ref - g)) / l (units 2^m_ref) = O 2^-g / l
-        s.fin[row] = lt > 0.f ? exp2i(-g_cur) / lt : 0.f;
+        s.fin[row] = lt == 0.f ? 0.f : exp2i(-g_cur) / lt;
       };
       finish(rA, mA);
       finish(rB, mB);
@@ -898,34 +929,53 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   if (!__all_sync(kFull, ok) && lane == 0) signal_abort(s, p, rank);
 }
 
-// ------------------------------------------------- O-CTA: tail page zeros -
-// The request's partial last page: rows at or past the length hold
-// undefined bytes (NaN in E4M3 would survive 0 * NaN in P V'), so warp 2
-// zeroes them in the ring stage before the MMA reads it.  The MMA thread,
-// which waits on the ring in order, hands the landed page over (tail_go).
+// ------------------------------------------ O-CTA: sanitise masked rows ---
+// A masked token gets p = 0 exactly, but 0 * NaN would still poison
+// O = P' V.  So for every page from the one holding token nmin onwards (the
+// draft tokens only some query rows see, and the request's partly filled
+// last page), warp 2 cleans the landed ring stage before the MMA reads it:
+// rows at or past the length, which can hold anything, are zeroed; rows in
+// [nmin, L) keep their bytes with every NaN code set to 0.  A query that
+// sees such a token already has a NaN score for it (the S side reads the
+// bytes as they are), which makes its whole row NaN, as the definition
+// says; a query that does not see it now adds exactly 0.  The MMA thread,
+// which waits on the ring in order, hands each landed page over (tail_go)
+// and waits for it back (tail_ready), one page at a time.
 __device__ __forceinline__ void tail_warp(Smem& s, const TcParams& p,
                                           const Work& w, uint32_t rank,
                                           int lane) {
-  if (!w.tail) return;
-  const int m = w.npages - 1;
-  const int stage = m % kStages;
-  if (!mbar_wait(smem_u32(&s.tail_go), 0, &s.abort_flag)) {
-    if (lane == 0) signal_abort(s, p, rank);
-    return;
+  for (int m = w.m_san; m < w.npages; ++m) {
+    const uint32_t use = (uint32_t)(m - w.m_san);
+    if (!mbar_wait(smem_u32(&s.tail_go), use & 1u, &s.abort_flag)) {
+      if (lane == 0) signal_abort(s, p, rank);
+      return;
+    }
+    const int stage = m % kStages;
+    const int64_t t0 = (w.p0 + m) * kPage;
+    const int keep = (int)(w.L - t0 < kPage ? w.L - t0 : kPage);
+    const int64_t lo64 = w.nmin - t0;
+    const int lo = lo64 <= 0 ? 0 : (lo64 >= keep ? keep : (int)lo64);
+    const int nr = kPage - lo;
+    // 4 boxes x nr rows x 8 chunks of 16 bytes; a row's 128 bytes are
+    // contiguous (the swizzle permutes chunks within the row).
+    for (int idx = lane; idx < 4 * nr * 8; idx += 32) {
+      const int bx = idx / (nr * 8), rem = idx % (nr * 8);
+      const int row = lo + rem / 8, ch = rem % 8;
+      uint4* c = reinterpret_cast<uint4*>(s.ring[stage] + bx * kBoxBytes +
+                                          (row >> 3) * 1024 + (row & 7) * 128 +
+                                          ch * 16);
+      if (row >= keep) {
+        *c = make_uint4(0, 0, 0, 0);
+      } else {
+        const uint4 x = *c;
+        *c = make_uint4(e4m3x4_nan_to_zero(x.x), e4m3x4_nan_to_zero(x.y),
+                        e4m3x4_nan_to_zero(x.z), e4m3x4_nan_to_zero(x.w));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
   }
-  const int valid = (int)(w.L - (w.p0 + m) * kPage);  // 1..63
-  const int nz = kPage - valid;
-  // 4 boxes x nz rows x 8 chunks of 16 bytes; a row's 128 bytes are
-  // contiguous (the swizzle permutes chunks within the row).
-  for (int idx = lane; idx < 4 * nz * 8; idx += 32) {
-    const int bx = idx / (nz * 8), rem = idx % (nz * 8);
-    const int row = valid + rem / 8, ch = rem % 8;
-    *reinterpret_cast<uint4*>(s.ring[stage] + bx * kBoxBytes + (row >> 3) * 1024 +
-                              (row & 7) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&s.tail_ready));
 }
 
 // ------------------------------------------------------- O-CTA: packers ---
@@ -1010,9 +1060,10 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       ok = false;
       break;
     }
-    if (w.tail && m == w.npages - 1) {
+    if (m >= w.m_san) {  // the tail warp sanitises the page first
       mbar_arrive(smem_u32(&s.tail_go));
-      if (!mbar_wait(smem_u32(&s.tail_ready), 0, &s.abort_flag)) {
+      if (!mbar_wait(smem_u32(&s.tail_ready), (uint32_t)(m - w.m_san) & 1u,
+                     &s.abort_flag)) {
         ok = false;
         break;
       }
