@@ -24,7 +24,7 @@ ROW_DIM, NOPE_DIM, ROPE_DIM, VALUE_DIM, PAGE_SIZE = 576, 512, 64, 512, 64
 KV_BF16, KV_FP8_E4M3 = 0, 1
 _KV_DTYPE = {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3}
 ROWS_PER_UNIT = 256  # query rows per work unit of the BF16 tensor-core kernel
-STATUS_WAIT_TIMEOUT, STATUS_BAD_LENGTH, STATUS_BAD_SLOT = 1, 2, 4
+STATUS_WAIT_TIMEOUT, STATUS_BAD_LENGTH, STATUS_BAD_SLOT, STATUS_BAD_WORK = 1, 2, 4, 8
 
 _lib = None
 _lock = threading.Lock()
@@ -85,6 +85,7 @@ def library() -> ctypes.CDLL:
             "mla_project_out": (i32, [p, p, p, i32, i32, p, p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
+            "mla_debug_wait": (i32, [i32, i32, p, p, p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -102,6 +103,12 @@ def _check(rc: int) -> int:
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _on(t: torch.Tensor):
+    """Make the tensor's device current for a call: the library launches
+    on (and looks up per-device state for) the current device."""
+    return torch.cuda.device(t.device)
 
 
 def _stream(stream: Optional[torch.cuda.Stream]):
@@ -283,14 +290,15 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
             req_to_token.stride(0), _ptr(seq_lens), _ptr(kv_limit), B, q_len,
             H, num_shards, PAGE_SIZE, float(sm_scale), num_splits,
             _ptr(split_pages))
-    tail = (_ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream))
-    if simt:
-        if work is not None:
-            raise ValueError("the CUDA-core path takes no work list")
-        _check(library().mla_decode_partial_simt(*args, *tail))
-    else:
-        _check(library().mla_decode_partial(
-            *args, _ptr(work), 0 if work is None else work.numel(), *tail))
+    with _on(q_nope):
+        tail = (_ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream))
+        if simt:
+            if work is not None:
+                raise ValueError("the CUDA-core path takes no work list")
+            _check(library().mla_decode_partial_simt(*args, *tail))
+        else:
+            _check(library().mla_decode_partial(
+                *args, _ptr(work), 0 if work is None else work.numel(), *tail))
     return O_part, LSE_part
 
 
@@ -324,13 +332,15 @@ def decode_fused(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         out = torch.empty((B, q_len, H, VALUE_DIM), dtype=torch.bfloat16, device=dev)
     if lse_out is None:
         lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
-    _check(library().mla_decode(
-        _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
-        kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
-        _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
-        num_splits, _ptr(split_pages), _ptr(work),
-        0 if work is None else work.numel(), _ptr(O_part), _ptr(LSE_part),
-        _ptr(counters), _ptr(out), _ptr(lse_out), _ptr(status), _stream(stream)))
+    with _on(q_nope):
+        _check(library().mla_decode(
+            _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
+            kv.shape[0], _ptr(req_to_token), req_to_token.stride(0),
+            _ptr(seq_lens), _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE,
+            float(sm_scale), num_splits, _ptr(split_pages), _ptr(work),
+            0 if work is None else work.numel(), _ptr(O_part), _ptr(LSE_part),
+            _ptr(counters), _ptr(out), _ptr(lse_out), _ptr(status),
+            _stream(stream)))
     return out, lse_out
 
 
@@ -352,13 +362,14 @@ def decode_scratch(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
         out = torch.empty((B, q_len, H, VALUE_DIM), dtype=torch.bfloat16, device=dev)
     if lse_out is None:
         lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
-    _check(library().mla_decode_scratch(
-        _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
-        kv.shape[0], _ptr(req_to_token), req_to_token.stride(0), _ptr(seq_lens),
-        _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE, float(sm_scale),
-        num_splits, _ptr(split_pages), _ptr(work),
-        0 if work is None else work.numel(), _ptr(out), _ptr(lse_out),
-        _ptr(status), _stream(stream)))
+    with _on(q_nope):  # the scratch array used is the current device's
+        _check(library().mla_decode_scratch(
+            _ptr(q_nope), _ptr(q_rope), _ptr(kv), _ptr(kv_scale), _kv_dtype(kv),
+            kv.shape[0], _ptr(req_to_token), req_to_token.stride(0),
+            _ptr(seq_lens), _ptr(kv_limit), B, q_len, H, num_shards, PAGE_SIZE,
+            float(sm_scale), num_splits, _ptr(split_pages), _ptr(work),
+            0 if work is None else work.numel(), _ptr(out), _ptr(lse_out),
+            _ptr(status), _stream(stream)))
     return out, lse_out
 
 
@@ -423,6 +434,16 @@ def debug_gather(kv, req_to_token, seq_lens, row_offset, total_rows: int,
         req_to_token.stride(0), _ptr(seq_lens), _ptr(row_offset),
         req_to_token.shape[0], PAGE_SIZE, _ptr(out), _stream(stream)))
     return out[:total_rows]
+
+
+def debug_wait(mode: int, delay_us: int, status, elapsed_ns, stream=None):
+    """Run the kernels' bounded wait on a barrier phase that nothing
+    completes (mode 0), that another warp aborts (1) or completes (2) after
+    delay_us; see mla_debug_wait.  `status` int32 [1], `elapsed_ns` int64 [1]
+    (device)."""
+    with _on(status):
+        _check(library().mla_debug_wait(mode, delay_us, _ptr(status),
+                                        _ptr(elapsed_ns), _stream(stream)))
 
 
 def decode(batch, num_splits: Optional[int] = None, simt: bool = False,

@@ -6,10 +6,11 @@
 // mla_decode_scratch takes them from one static __device__ array (256-byte
 // aligned, MLA_SCRATCH_BYTES), whose device address is looked up once per
 // device with cudaGetSymbolAddress; no cudaMalloc or cudaFree is ever made.
-// The counters start zero (static device memory is zero-initialised when the
-// module loads) and every call leaves them zero.  The array is one per
-// device and process: calls that may overlap on a device race on it (see
-// include/mla_decode.h).
+// Every call clears the counters on its stream before the decode
+// (cudaMemsetAsync on the array's address, no allocation): a call that left
+// them non-zero (a work list naming no unit, or one unit twice) cannot
+// offset a later call's counts.  The array is one per device and process:
+// calls that may overlap on a device race on it (see include/mla_decode.h).
 #include <mutex>
 
 #include "mla_internal.h"
@@ -23,7 +24,11 @@ constexpr int kMaxDevices = 64;
 
 int64_t round256(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
-// Device address of g_scratch on the current device (looked up once).
+// Device address of g_scratch on the current device, looked up on the first
+// call made with that device current and kept for the life of the process
+// (a cudaDeviceReset reloads the device code, after which the kept address
+// is stale: such a process must not call mla_decode_scratch on that device
+// again).
 int scratch_base(void** base) {
   static std::mutex mu;
   static void* cache[kMaxDevices] = {};
@@ -107,7 +112,11 @@ int mla_decode_scratch(const void* q_nope_absorbed, const void* q_rope,
   const int64_t parts = (int64_t)num_shards * num_splits;
   uint8_t* p = static_cast<uint8_t*>(base);
   int32_t* counters = reinterpret_cast<int32_t*>(p);
-  p += round256((int64_t)B * ((q_len * H + 127) / 128) * 4);
+  const int64_t counter_bytes = (int64_t)B * ((q_len * H + 127) / 128) * 4;
+  cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)counter_bytes,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch counters)");
+  p += round256(counter_bytes);
   float* LSE_part = reinterpret_cast<float*>(p);
   p += round256(parts * rows * 4);
   float* O_part = reinterpret_cast<float*>(p);

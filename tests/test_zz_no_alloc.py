@@ -1,8 +1,8 @@
 """mla_decode_scratch: the fused decode with its workspace in the library's
 static device scratch (no allocation, no workspace argument).
 
-Collected last (file name) and independent of the other tests' state: the
-scratch counters are zero at load and after every call, whatever ran before.
+Collected last (file name) and independent of the other tests' state: every
+call clears the scratch counters before its decode, whatever ran before.
 CPU tests cover the size rule and the size limit (checked before any other
 argument, so nothing is launched); GPU tests compare with mla_decode on
 caller workspace bit for bit and check that repeated calls allocate no
@@ -107,3 +107,30 @@ def test_scratch_decode_allocates_nothing_and_repeats(lib):
     ref_o, ref_l = mla.decode_fused(*args, split_pages=sp)
     torch.cuda.synchronize()
     assert torch.equal(ref_o, out0) and torch.equal(ref_l, lse0)
+
+
+@pytest.mark.gpu
+def test_scratch_decode_recovers_after_bad_work_list(lib):
+    """A work list with an entry that names no unit sets MLA_STATUS_BAD_WORK
+    and leaves that unit's arrival count short in the static scratch; the
+    next call must not inherit it (each call clears the counters first)."""
+    wl = synth.Workload("nab", 3, 5, 96, [1000, 257, 70])
+    batch = synth.make_batch(wl, seed=52, device="cuda")
+    S = 3  # three arrivals per (request, row unit): a missing one leaves 2
+    args = (batch.q_nope, batch.q_rope, batch.kv, batch.kv_scale,
+            batch.req_to_token, batch.seq_lens, batch.kv_limit, S, wl.sm_scale)
+    units = S * wl.B * (-(-wl.q_len * wl.H // 256))
+    good = torch.arange(units, dtype=torch.int32, device="cuda")
+    bad = good.clone()
+    bad[0] = 1 << 30  # names no unit: that cluster does nothing
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.decode_scratch(*args, work=bad, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 8  # MLA_STATUS_BAD_WORK
+    for _ in range(2):
+        st.zero_()
+        o1, l1 = mla.decode_scratch(*args, work=good, status=st)
+        o2, l2 = mla.decode_fused(*args, work=good)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
