@@ -30,6 +30,14 @@
 //     the per-token factors and the 8-bit conversions stay off the softmax.
 //   Each product thus takes two 8-bit MMAs, as long as one 16-bit MMA, and
 //   the tensor cores read the E4M3 bytes with no conversion pass.
+//   * A query element far above the rest of its row (beyond 32x the row's
+//     mean |q|: an outlier channel) would set the row scale and push the
+//     small elements under the split's floor.  Such channels (up to 4 per
+//     128-row group, shared by the group's rows) are left out of Qhi/Qlo;
+//     an idle warp copies their E4M3 key bytes out of each ring stage before
+//     the stage is released, and the softmax adds q_c * k8_t,c to the raw
+//     score in fp32 (exact: 8 x 4 significant bits).  The split exponent
+//     then comes from the remaining elements.
 //   Rank 0 (S-CTA) holds Qhi/Qlo (TMEM columns [0, 256) for the 512 c_kv
 //   dims, shared memory for the 64 RoPE dims), split from query rows that
 //   TMA brings into the still idle ring, and one 256-column S tile; rank 1
@@ -41,6 +49,7 @@
 //   2^(m_ref - g), l in units of 2^m_ref.  Every wait is bounded
 //   (ptx_sm103.cuh).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "mla_combine.cuh"
 #include "mla_tma.cuh"
@@ -71,6 +80,11 @@ constexpr uint32_t kSCol0 = 256;    // S buffer columns
 constexpr float kTau = 8.f;         // lazy-rescale threshold (log2 units)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kPartials = 8;         // 32-token groups of an S tile
+// Query exceptions: elements above kExcRatio x their row's mean |q| leave the
+// two-part E4M3 split (whose exponent they would otherwise set) for an exact
+// fp32 path; a 128-row group takes up to kExc such channels.
+constexpr int kExc = 4;
+constexpr float kExcRatio = 32.f;
 // Register split of the S-CTA (setmaxnreg): 640 threads launch with 96
 // registers each (61,440 of 65,536); the producer/MMA/scale warpgroup (warps
 // 0-3) gives registers away so the four softmax warpgroups can hold their
@@ -101,8 +115,14 @@ struct __align__(1024) Smem {
   uint8_t pslot[kNP][kPSlotStride];
   uint32_t tsg[4][kTilePages * kPage / 2];  // S-CTA: f16 pairs scale * 2^g
   int tg[4];                // S-CTA: scale exponent g of tile j % 4
-  float fin[kRows];
+  union {
+    float fin[kRows];              // 1 / l per row (after the tile loop)
+    uint16_t xe[kRows][kExc];      // S-CTA: bf16 q of the exception channels
+  };
   float xch[kPartials][kRows];  // S-CTA: row values per 32-token group
+  uint8_t xk[2][kExc][kTilePages * kPage];  // S-CTA: E4M3 K bytes of the
+                                            // exception channels, tile j % 2
+  int xtab[kExc];           // S-CTA: the group's exception channels (-1: none)
   uint64_t full[kStages];   // TMA -> MMA (bytes)
   uint64_t empty[kStages];  // MMA -> producer
   uint64_t scfull[4];       // S-CTA: scale bulk copies landed
@@ -113,6 +133,8 @@ struct __align__(1024) Smem {
   uint64_t packed[kNP];     // O-CTA: P' of slot k split into Phi | Plo
   uint64_t pempty[kNP];
   uint64_t drain, corr_done, fin_full, qready, tail_go, tail_ready;
+  uint64_t xkfull[2];       // S-CTA: exception K bytes of tile j % 2 copied
+  uint64_t xkempty[2];      // S-CTA: the softmax warps done with them
   uint64_t qbar;            // S-CTA: the query boxes landed
   uint32_t tmem_base;
   int abort_flag;
@@ -210,6 +232,44 @@ __device__ __forceinline__ float absmax_bf16x8(uint4 x) {
   return m;
 }
 
+// Sum of |x| of the 8 bf16 values of a 16-byte chunk.
+__device__ __forceinline__ float abssum_bf16x8(uint4 x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    m += fabsf(__uint_as_float(w[k] << 16)) + fabsf(__uint_as_float(w[k] & 0xFFFF0000u));
+  return m;
+}
+
+// bf16 element e (0..7) of a 16-byte chunk, as raw bits.
+__device__ __forceinline__ uint32_t bf16_bits_of(uint4 x, int e) {
+  const uint32_t w = (e >> 1) == 0 ? x.x : (e >> 1) == 1 ? x.y : (e >> 1) == 2 ? x.z : x.w;
+  return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// The chunk with element e (0..7) set to zero when dim0 + e is one of the
+// group's exception channels.
+__device__ __forceinline__ uint4 drop_channels(uint4 x, int dim0, const int (&tab)[kExc],
+                                               int ntab) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  for (int k = 0; k < ntab; ++k) {
+    const int e = tab[k] - dim0;
+    if (e >= 0 && e < 8) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Two E4M3 bytes (lower byte first) -> two floats (exact).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t b2, float& lo, float& hi) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h)
+      : "r"(b2));
+  lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+}
+
 // Q split: values a (element 2c) and b (element 2c + 1), already multiplied
 // by the row's 2^-e, become hi = e4m3 pair and lo = e4m3 pair of the
 // remainders (lower byte = element 2c).  The remainder a - hi(a) is exact in
@@ -294,9 +354,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
 // Per-pair work description, identical on both CTAs of the pair.
 struct Work {
   int v, b, shard, split, r_base, nrows, npages;
-  int m_san;  // first page of the range holding a token at or past nmin
   int64_t L, p0;
-  int64_t nmin;  // fewest tokens any query of the request sees
 };
 
 // The pair's unit id (split, virtual request v, row group g) = (split * V +
@@ -330,21 +388,26 @@ __device__ __forceinline__ Work pair_work(const TcParams& p, int pair) {
       p.split_pages ? p.split_pages + (int64_t)w.v * (p.num_splits + 1) : nullptr,
       p.num_splits, w.split, P, w.p0, p1);
   w.npages = (int)(p1 - w.p0);
-  // Tokens in [nmin, L) are visible to some query rows of the request and
-  // masked for others; tokens at or past L to none.  The pages that hold any
-  // of them are sanitised before P V reads them (tail_warp).
-  int64_t nmin = L - p.q_len + 1;
+  return w;
+}
+
+// Tokens in [nmin, L) are visible to some query rows of the request and
+// masked for others; tokens at or past L to none.  The pages of the pair's
+// range from m_san on hold such tokens and are sanitised before P V reads
+// them (tail_warp).  Computed only by the O-CTA roles that need it.
+__device__ __forceinline__ void masked_range(const TcParams& p, const Work& w,
+                                             int64_t& nmin_out, int& m_san_out) {
+  int64_t nmin = w.L - p.q_len + 1;
   if (p.kv_limit) {
-    nmin = L;
+    nmin = w.L;
     for (int i = 0; i < p.q_len; ++i) {
       const int64_t n = p.kv_limit[(int64_t)w.v * p.q_len + i];
       nmin = n < nmin ? n : nmin;
     }
   }
-  w.nmin = nmin < 0 ? 0 : (nmin > L ? L : nmin);
-  const int64_t m_san = w.nmin / kPage - w.p0;
-  w.m_san = (int)(m_san < 0 ? 0 : (m_san > w.npages ? w.npages : m_san));
-  return w;
+  nmin_out = nmin < 0 ? 0 : (nmin > w.L ? w.L : nmin);
+  const int64_t m_san = nmin_out / kPage - w.p0;
+  m_san_out = (int)(m_san < 0 ? 0 : (m_san > w.npages ? w.npages : m_san));
 }
 
 // Four E4M3 bytes with every NaN code (S.1111.111; E4M3 has no infinity)
@@ -388,6 +451,12 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   // The ring holds the query rows until every softmax warp has moved them.
   if (lane == 0 && !mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) ok = false;
   ok = __shfl_sync(kFull, ok, 0);
+  // A stage is released by the MMA's commit and by the extractor, which has
+  // work only when the group has exception channels; without them this warp
+  // makes that second arrival itself as soon as it takes the stage (it then
+  // counts towards the stage's next release), so the release waits for the
+  // MMA alone.
+  const bool self_release = s.xtab[0] < 0;
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles && ok; ++j) {
     const int m0 = j * kTilePages;
@@ -422,10 +491,12 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
       const bool rope = c == kBlocksPerTile - 1;
       const uint32_t box = rope ? kRopeBoxBytes : kBoxBytes;
       if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag))
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+          if (self_release) mbar_arrive(smem_u32(&s.empty[stage]));
           mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * box);
-        else
+        } else {
           ok = false;
+        }
       }
       ok = __shfl_sync(kFull, ok, 0);
       if (ok && lane < np)
@@ -522,6 +593,67 @@ __device__ __forceinline__ void scale_warp(Smem& s, const TcParams& p,
     fence_proxy_async_smem();  // tscale is the next bulk copy's target
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.tsready[ts]));
+  }
+  if (!ok && lane == 0) signal_abort(s, p, rank);
+}
+
+// S-CTA warp 3: the group's exception channels (xtab, final once every
+// softmax warp has passed qready).  For every ring stage of every tile it
+// copies those channels' E4M3 key bytes of the stage's 128-dim block (or the
+// RoPE block) for the tile's tokens into xk[j % 2][k][token] and then
+// releases the stage with the MMA (empty counts both).  Without exception
+// channels it has nothing to do (the producer makes its arrivals).
+__device__ __forceinline__ void extractor(Smem& s, const TcParams& p,
+                                          const Work& w, uint32_t rank,
+                                          int lane) {
+  bool ok = true;
+  if (!mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) ok = false;
+  int tab[kExc], ntab = 0;
+#pragma unroll
+  for (int k = 0; k < kExc; ++k) {
+    tab[k] = s.xtab[k];
+    ntab += tab[k] >= 0 ? 1 : 0;
+  }
+  if (ok && ntab == 0) return;
+  uint32_t stage = 0, phase = 0;
+  const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
+  for (int j = 0; j < ntiles && ok; ++j) {
+    const int np = tile_pages(w, j);
+    const int xb = j & 1;
+    if (!mbar_wait(smem_u32(&s.xkempty[xb]), ((j >> 1) & 1) ^ 1u, &s.abort_flag)) {
+      ok = false;
+      break;
+    }
+    for (int c = 0; c < kBlocksPerTile && ok; ++c) {
+      if (!mbar_wait(smem_u32(&s.full[stage]), phase, &s.abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int k = 0; k < ntab; ++k) {
+        const int d = tab[k];
+        if ((d < MLA_NOPE_DIM ? d >> 7 : kBlocksPerTile - 1) != c) continue;
+        for (int t = lane; t < np * kPage; t += 32) {
+          const int pg = t >> 6, tr = t & 63;
+          uint32_t off;
+          if (c < kBlocksPerTile - 1) {  // 8-KB box per page, 128-B swizzle
+            const int dd = d & 127;
+            off = pg * kBoxBytes + box_chunk_offset(tr, dd >> 4) + (dd & 15);
+          } else {  // 4-KB RoPE box per page, 64-B swizzle
+            const int dd = d - MLA_NOPE_DIM;
+            off = pg * kRopeBoxBytes + (tr >> 3) * 512 + (tr & 7) * 64 +
+                  ((((dd >> 4) ^ (tr >> 1)) & 3) << 4) + (dd & 15);
+          }
+          s.xk[xb][k][t] = s.ring[stage][off];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.empty[stage]));
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok && lane == 0) mbar_arrive(smem_u32(&s.xkfull[xb]));
   }
   if (!ok && lane == 0) signal_abort(s, p, rank);
 }
@@ -647,21 +779,80 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
                          : zero4;
   };
 
-  // Row scale 2^e from the warpgroups' partial |q| maxima.
-  float amax = 0.f;
-  if (g < 2) {
+  // This warpgroup's dims of row r: chunks 32g .. 32g + 31 of the c_kv dims
+  // (g < 2) or the 8 chunks of RoPE dims (g == 2); 16-byte chunk k, dims
+  // dim0(k) .. dim0(k) + 7.
+  const int nchunks = g < 2 ? 32 : (g == 2 ? 8 : 0);
+  auto my_chunk = [&](int k) -> uint4 {
+    return g < 2 ? qchunk(32 * g + k) : qrope_chunk(k);
+  };
+  auto dim0 = [&](int k) -> int {
+    return g < 2 ? 8 * (32 * g + k) : MLA_NOPE_DIM + 8 * k;
+  };
+  // Row statistics from the warpgroups' parts: largest |q| and sum of |q|.
+  float amax = 0.f, asum = 0.f;
+  {
+    float m4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-    for (int k = 0; k < 32; ++k)
-      amax = fmaxf(amax, absmax_bf16x8(qchunk(32 * g + k)));
-  } else if (g == 2) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, absmax_bf16x8(qrope_chunk(k)));
+    for (int k = 0; k < nchunks; ++k) {
+      const uint4 x = my_chunk(k);
+      m4[k & 3] = fmaxf(m4[k & 3], absmax_bf16x8(x));
+      s4[k & 3] += abssum_bf16x8(x);
+    }
+    amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    asum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
   }
   s.xch[g][r] = amax;
+  s.xch[4 + g][r] = asum;
   named_bar_sync(1, 512);
   auto qmax = [&](int row) {
     return fmaxf(max3(s.xch[0][row], s.xch[1][row], s.xch[2][row]), s.xch[3][row]);
   };
+  // Exception candidates: elements above kExcRatio x the row's mean |q|
+  // claim a slot of the group's channel table (first come; a channel already
+  // there is shared; with the table full the element stays in the split).
+  {
+    const float tau = kExcRatio / MLA_ROW_DIM *
+                      ((s.xch[4][r] + s.xch[5][r]) + (s.xch[6][r] + s.xch[7][r]));
+    if (qmax(r) > tau) {
+      for (int k = 0; k < nchunks; ++k) {
+        const uint4 x = my_chunk(k);
+        if (absmax_bf16x8(x) <= tau) continue;
+        for (int e = 0; e < 8; ++e) {
+          if (fabsf(__uint_as_float(bf16_bits_of(x, e) << 16)) <= tau) continue;
+          const int d = dim0(k) + e;
+          for (int t = 0; t < kExc; ++t) {
+            const int old = atomicCAS(&s.xtab[t], -1, d);
+            if (old == -1 || old == d) break;
+          }
+        }
+      }
+    }
+  }
+  named_bar_sync(1, 512);
+  int tab[kExc], ntab = 0;
+#pragma unroll
+  for (int k = 0; k < kExc; ++k) {
+    tab[k] = s.xtab[k];
+    ntab += tab[k] >= 0 ? 1 : 0;
+  }
+  if (ntab > 0) {
+    // The split's row scale from the elements outside the table; the owner
+    // of each table channel keeps the row's value there for the exact path.
+    float m = 0.f;
+    for (int k = 0; k < nchunks; ++k)
+      m = fmaxf(m, absmax_bf16x8(drop_channels(my_chunk(k), dim0(k), tab, ntab)));
+    for (int t = 0; t < ntab; ++t) {
+      const int d = tab[t];
+      const int owner = d < MLA_NOPE_DIM ? d >> 8 : 2;
+      if (owner == g) {
+        const uint4 x = d < MLA_NOPE_DIM ? qchunk(d >> 3) : qrope_chunk((d - MLA_NOPE_DIM) >> 3);
+        s.xe[r][t] = (uint16_t)bf16_bits_of(x, d & 7);
+      }
+    }
+    s.xch[g][r] = m;  // every row max was read before the barrier above
+    named_bar_sync(1, 512);
+  }
   const float inv = exp2i(-row_exponent(qmax(r)));
   // score factor sm_scale * log2(e) * 2^e of rows A and B
   const float crowA = p.scale_log2 * exp2i(row_exponent(qmax(rA)));
@@ -680,7 +871,9 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         uint2 h, l;
-        split_q8(qchunk(32 * g + 8 * c + k), inv, h, l);
+        uint4 x = qchunk(32 * g + 8 * c + k);
+        if (ntab > 0) x = drop_channels(x, 8 * (32 * g + 8 * c + k), tab, ntab);
+        split_q8(x, inv, h, l);
         vh[2 * k] = h.x;
         vh[2 * k + 1] = h.y;
         vl[2 * k] = l.x;
@@ -694,8 +887,13 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk cc = elements 16cc..16cc+15
       uint2 h0, l0, h1, l1;
-      split_q8(qrope_chunk(2 * cc), inv, h0, l0);
-      split_q8(qrope_chunk(2 * cc + 1), inv, h1, l1);
+      uint4 x0 = qrope_chunk(2 * cc), x1 = qrope_chunk(2 * cc + 1);
+      if (ntab > 0) {
+        x0 = drop_channels(x0, MLA_NOPE_DIM + 16 * cc, tab, ntab);
+        x1 = drop_channels(x1, MLA_NOPE_DIM + 16 * cc + 8, tab, ntab);
+      }
+      split_q8(x0, inv, h0, l0);
+      split_q8(x1, inv, h1, l1);
       const uint32_t off = (r >> 3) * 512 + (r & 7) * 64 +
                            (((cc ^ (r >> 1)) & 3) << 4);
       *reinterpret_cast<uint4*>(s.qrope[0] + off) = make_uint4(h0.x, h0.y, h1.x, h1.y);
@@ -738,6 +936,42 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.sempty));
+
+    // Exception channels: raw += q_c 2^-e k8_t,c for rows A and B, exact in
+    // fp32 (a bf16 value times an E4M3 byte), from the bytes warp 3 copied.
+    if (s.xtab[0] >= 0) {  // the group has exception channels (uniform)
+      const int xb = j & 1;
+      if (ok && !mbar_wait(smem_u32(&s.xkfull[xb]), (j >> 1) & 1, &s.abort_flag))
+        ok = false;
+      if (ok && has) {
+        // 2^-e of each row: crow / scale_log2 is a power of two
+        const float invA = 1.f / (crowA / p.scale_log2);
+        const float invB = 1.f / (crowB / p.scale_log2);
+        for (int k = 0; k < kExc && s.xtab[k] >= 0; ++k) {
+          const float xa = __uint_as_float((uint32_t)s.xe[rA][k] << 16) * invA;
+          const float xb2 = __uint_as_float((uint32_t)s.xe[rB][k] << 16) * invB;
+          const uint32_t* kb =
+              reinterpret_cast<const uint32_t*>(&s.xk[xb][k][kPage * g + 32 * hp]);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {  // tokens 4q .. 4q + 3
+            const uint32_t w4 = kb[q];
+            float k0, k1, k2, k3;
+            e4m3x2_to_f32(w4 & 0xFFFFu, k0, k1);
+            e4m3x2_to_f32(w4 >> 16, k2, k3);
+            a[4 * q] = __float_as_uint(fmaf(xa, k0, __uint_as_float(a[4 * q])));
+            a[4 * q + 1] = __float_as_uint(fmaf(xa, k1, __uint_as_float(a[4 * q + 1])));
+            a[4 * q + 2] = __float_as_uint(fmaf(xa, k2, __uint_as_float(a[4 * q + 2])));
+            a[4 * q + 3] = __float_as_uint(fmaf(xa, k3, __uint_as_float(a[4 * q + 3])));
+            b[4 * q] = __float_as_uint(fmaf(xb2, k0, __uint_as_float(b[4 * q])));
+            b[4 * q + 1] = __float_as_uint(fmaf(xb2, k1, __uint_as_float(b[4 * q + 1])));
+            b[4 * q + 2] = __float_as_uint(fmaf(xb2, k2, __uint_as_float(b[4 * q + 2])));
+            b[4 * q + 3] = __float_as_uint(fmaf(xb2, k3, __uint_as_float(b[4 * q + 3])));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.xkempty[xb]));
+    }
 
     // Token scales: raw -> raw * scale_t for both rows (one broadcast load
     // of four scales serves eight scores).
@@ -944,8 +1178,11 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
 __device__ __forceinline__ void tail_warp(Smem& s, const TcParams& p,
                                           const Work& w, uint32_t rank,
                                           int lane) {
-  for (int m = w.m_san; m < w.npages; ++m) {
-    const uint32_t use = (uint32_t)(m - w.m_san);
+  int64_t nmin;
+  int m_san;
+  masked_range(p, w, nmin, m_san);
+  for (int m = m_san; m < w.npages; ++m) {
+    const uint32_t use = (uint32_t)(m - m_san);
     if (!mbar_wait(smem_u32(&s.tail_go), use & 1u, &s.abort_flag)) {
       if (lane == 0) signal_abort(s, p, rank);
       return;
@@ -953,7 +1190,7 @@ __device__ __forceinline__ void tail_warp(Smem& s, const TcParams& p,
     const int stage = m % kStages;
     const int64_t t0 = (w.p0 + m) * kPage;
     const int keep = (int)(w.L - t0 < kPage ? w.L - t0 : kPage);
-    const int64_t lo64 = w.nmin - t0;
+    const int64_t lo64 = nmin - t0;
     const int lo = lo64 <= 0 ? 0 : (lo64 >= keep ? keep : (int)lo64);
     const int nr = kPage - lo;
     // 4 boxes x nr rows x 8 chunks of 16 bytes; a row's 128 bytes are
@@ -1028,6 +1265,9 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
                                       uint32_t rank) {
   uint32_t stage = 0, phase = 0, ev = 0;
   bool ok = true;
+  int64_t nmin;
+  int m_san;
+  masked_range(p, w, nmin, m_san);
   // Each P message lands by a bulk copy whose bytes complete on pfull[k];
   // this CTA arms the barrier (one arrival + the byte count) itself, so the
   // sender needs no cluster-scope arrive: the first use of each slot is armed
@@ -1060,9 +1300,9 @@ __device__ __forceinline__ void mma_o(Smem& s, const TcParams& p,
       ok = false;
       break;
     }
-    if (m >= w.m_san) {  // the tail warp sanitises the page first
+    if (m >= m_san) {  // the tail warp sanitises the page first
       mbar_arrive(smem_u32(&s.tail_go));
-      if (!mbar_wait(smem_u32(&s.tail_ready), (uint32_t)(m - w.m_san) & 1u,
+      if (!mbar_wait(smem_u32(&s.tail_ready), (uint32_t)(m - m_san) & 1u,
                      &s.abort_flag)) {
         ok = false;
         break;
@@ -1204,7 +1444,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s.ctl_last = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
-      mbar_init(smem_u32(&s.empty[i]), 1);
+      // S-CTA: the MMA's commit and the extractor (warp 3) release a stage
+      mbar_init(smem_u32(&s.empty[i]), rank == 0 ? 2 : 1);
+    }
+    for (int i = 0; i < kExc; ++i) s.xtab[i] = -1;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.xkfull[i]), 1);
+      mbar_init(smem_u32(&s.xkempty[i]), 16);  // the 16 softmax warps
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s.scfull[i]), 1);
@@ -1307,6 +1553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
       } else if (warp == 2) {
         scale_warp(s, p, w, rank, lane);
+      } else {
+        extractor(s, p, w, rank, lane);
       }
       teardown();
       return;
