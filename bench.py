@@ -304,7 +304,11 @@ def run_reference(args):
 
 def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
     """Median device time (ms) of one partial-decode + combine pair at S
-    splits, CUDA events on the launching stream."""
+    splits, CUDA events on the launching stream.  The steps are enqueued back
+    to back (no host synchronisation between them, so the host's launch work
+    overlaps the previous step instead of sitting between the events); with
+    KV smaller than twice the L2 a 256-MB buffer is written between steps,
+    outside the events, so every step reads its inputs from DRAM."""
     import torch
     dev = batch.q_nope.device
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -323,18 +327,22 @@ def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
                            split_pages=split_pages, work=work)
         mla.lse_combine(O_part, LSE_part, out, lse)
 
+    kv_bytes = batch.kv.numel() * batch.kv.element_size()
+    flush_buf = (torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+                 if kv_bytes < 256 * 2**20 else None)
     for _ in range(warmup):
         run()
     torch.cuda.synchronize()
-    ts = []
-    for _ in range(iters):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for k, (a, b) in enumerate(evs):
+        if flush_buf is not None:
+            flush_buf.fill_(k & 0xFF)
         a.record(stream)
         run()
         b.record(stream)
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) for a, b in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     return statistics.median(ts)
@@ -382,8 +390,9 @@ def run_c0_scan(args):
 def run_sweep(args):
     """Wave-quantisation sweep: for every (B, context) point, the pair timed
     with the pages' split rule and with the planner's split (and any extra
-    split counts asked for), one JSON line per point.  Inputs larger than L2
-    (>= 115 MB of KV at B = 1, 100k) so no flush is needed."""
+    split counts asked for), one JSON line per point (time_pair: device time
+    per step, the L2 flushed between steps when the KV is smaller than twice
+    the L2)."""
     import torch
 
     import mla_latent_decode_gb300 as mla
