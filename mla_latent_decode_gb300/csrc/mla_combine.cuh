@@ -11,7 +11,7 @@
 // row: lane j reads LSE_j (all weights in one round trip, reduced with
 // shuffles), then each lane owns four float4 columns of every part
 // (coalesced 512-byte loads), two parts' loads in flight at a time, parts
-// accumulated in order.
+// accumulated in order; for few rows several warps share a row (below).
 // kCoherent: the parts were written by other CTAs of the running kernel, so
 // they are read through L2 only (no read-only or L1 copy that could be
 // stale); otherwise the read-only path.
@@ -35,13 +35,21 @@ __device__ __forceinline__ float4 load_part4(const float4* p) {
   return kCoherent ? __ldcg(p) : __ldg(p);
 }
 
-template <bool kCoherent>
+// kWs warps share a row: warp `slice` of them owns value columns
+// [slice * 512 / kWs, +512 / kWs), each lane kF4 = 4 / kWs float4 columns of
+// every part, with kPar = 8 / kF4 parts' loads in flight at a time (eight
+// float4 loads per lane whatever kWs).  Every warp of the row computes the
+// weights itself; slice 0 writes lse_out.
+template <bool kCoherent, int kWs = 1>
 __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
                                             const float* __restrict__ LSE_part,
                                             int P, int64_t rows, int64_t row,
                                             __nv_bfloat16* __restrict__ out,
                                             float* __restrict__ lse_out,
-                                            int lane) {
+                                            int lane, int slice = 0) {
+  static_assert(kWs == 1 || kWs == 2 || kWs == 4, "warps per row");
+  constexpr int kF4 = 4 / kWs;   // float4 columns per lane and part
+  constexpr int kPar = 8 / kF4;  // parts in flight
   constexpr uint32_t kAll = 0xffffffffu;
   // M = max_j LSE_j: lane j % 32 reads LSE_j (one round trip per 32 parts)
   float M = -INFINITY;
@@ -54,22 +62,24 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
     }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+  // float4 column of this lane's k-th slot
+  auto col = [&](int k) { return slice * (128 / kWs) + lane + 32 * k; };
+  __nv_bfloat162* dst =
+      reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
   if (__any_sync(kAll, nan)) {
     const __nv_bfloat162 qnan = __float2bfloat162_rn(__int_as_float(0x7fc00000));
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int c = 2 * (lane + 32 * k);
-      dst[c] = qnan;
-      dst[c + 1] = qnan;
+    for (int k = 0; k < kF4; ++k) {
+      dst[2 * col(k)] = qnan;
+      dst[2 * col(k) + 1] = qnan;
     }
-    if (lse_out && lane == 0) lse_out[row] = __int_as_float(0x7fc00000);
+    if (lse_out && slice == 0 && lane == 0) lse_out[row] = __int_as_float(0x7fc00000);
     return;
   }
 
-  float4 acc[4];
+  float4 acc[kF4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < kF4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float W = 0.f;  // lane-partial sum of the weights, reduced below
   if (M != -INFINITY) {
     for (int j0 = 0; j0 < P; j0 += 32) {
@@ -80,36 +90,30 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
         wl = lj == -INFINITY ? 0.f : expf(lj - M);
       }
       W += wl;
-      // parts in order, two at a time so both parts' loads are in flight;
-      // an empty part (weight 0) is never read
-      for (int t = 0; t < n; t += 2) {
-        const float w0 = __shfl_sync(kAll, wl, t);
-        const float w1 = t + 1 < n ? __shfl_sync(kAll, wl, t + 1) : 0.f;
-        const float4* s0 = reinterpret_cast<const float4*>(
-            O_part + ((int64_t)(j0 + t) * rows + row) * MLA_VALUE_DIM);
-        const float4* s1 = reinterpret_cast<const float4*>(
-            O_part + ((int64_t)(j0 + t + 1) * rows + row) * MLA_VALUE_DIM);
-        float4 x0[4], x1[4];
+      // parts in order, kPar at a time so their loads are in flight
+      // together; an empty part (weight 0) is never read
+      for (int t = 0; t < n; t += kPar) {
+        float w[kPar];
+        float4 x[kPar][kF4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          x0[k] = w0 != 0.f ? load_part4<kCoherent>(s0 + lane + 32 * k)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-          x1[k] = w1 != 0.f ? load_part4<kCoherent>(s1 + lane + 32 * k)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < kPar; ++q) {
+          w[q] = t + q < n ? __shfl_sync(kAll, wl, t + q) : 0.f;
+          const float4* src = reinterpret_cast<const float4*>(
+              O_part + ((int64_t)(j0 + t + q) * rows + row) * MLA_VALUE_DIM);
+#pragma unroll
+          for (int k = 0; k < kF4; ++k)
+            x[q][k] = w[q] != 0.f ? load_part4<kCoherent>(src + col(k))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (w0 != 0.f) {
-            acc[k].x = fmaf(w0, x0[k].x, acc[k].x);
-            acc[k].y = fmaf(w0, x0[k].y, acc[k].y);
-            acc[k].z = fmaf(w0, x0[k].z, acc[k].z);
-            acc[k].w = fmaf(w0, x0[k].w, acc[k].w);
-          }
-          if (w1 != 0.f) {
-            acc[k].x = fmaf(w1, x1[k].x, acc[k].x);
-            acc[k].y = fmaf(w1, x1[k].y, acc[k].y);
-            acc[k].z = fmaf(w1, x1[k].z, acc[k].z);
-            acc[k].w = fmaf(w1, x1[k].w, acc[k].w);
+        for (int q = 0; q < kPar; ++q) {
+          if (w[q] == 0.f) continue;
+#pragma unroll
+          for (int k = 0; k < kF4; ++k) {
+            acc[k].x = fmaf(w[q], x[q][k].x, acc[k].x);
+            acc[k].y = fmaf(w[q], x[q][k].y, acc[k].y);
+            acc[k].z = fmaf(w[q], x[q][k].z, acc[k].z);
+            acc[k].w = fmaf(w[q], x[q][k].w, acc[k].w);
           }
         }
       }
@@ -118,15 +122,14 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kAll, W, o);
   const float inv = W > 0.f ? 1.f / W : 0.f;
-  __nv_bfloat162* dst =
-      reinterpret_cast<__nv_bfloat162*>(out + row * MLA_VALUE_DIM);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int c = 2 * (lane + 32 * k);  // bf16x2 index of column 4*(lane+32k)
+  for (int k = 0; k < kF4; ++k) {
+    const int c = 2 * col(k);  // bf16x2 index of float4 column col(k)
     dst[c] = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
     dst[c + 1] = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
   }
-  if (lse_out && lane == 0) lse_out[row] = W > 0.f ? M + logf(W) : -INFINITY;
+  if (lse_out && slice == 0 && lane == 0)
+    lse_out[row] = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
 }  // namespace mla

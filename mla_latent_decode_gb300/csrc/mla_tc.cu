@@ -972,6 +972,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const Work w = unit_work(p, cluster_unit(p), rank);
 
+  // The stream's next kernel (the LSE combine) may be scheduled from now
+  // on; it waits for this grid's completion before it reads a part.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     s.ctl_slot = 0;
