@@ -1437,9 +1437,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const Work w = pair_work(p, unit);
 
-  // The stream's next kernel (the LSE combine) may be scheduled from now
-  // on; it waits for this grid's completion before it reads a part.
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     s.ctl_slot = 0;
