@@ -319,9 +319,13 @@ int mla_check_page_table(const int32_t* req_to_token_host, int64_t stride,
  * score that a row does see makes that row NaN (O_part and LSE_part), as the
  * definition gives.
  * Precision with FP8 KV: the contractions run on FP8 tensor cores over the
- * stored E4M3 bytes.  Each query row is represented as 2^e (hi + lo), two
+ * stored E4M3 bytes.  Query elements above 32x their row's mean |q|
+ * (outlier channels, up to 4 per group of 128 rows, shared by the group)
+ * leave the 8-bit representation and are multiplied with the key bytes in
+ * fp32, exactly.  The rest of each row is represented as 2^e (hi + lo), two
  * E4M3 parts with a power-of-two row scale: exact for every element at least
- * 2^-9 of the row's largest |q|, off by at most 2^-17 of it otherwise.  The
+ * 2^-9 of the row's largest remaining |q|, off by at most 2^-17 of it
+ * otherwise (a fifth outlier channel in one group stays in this split).  The
  * probabilities (times the token's scale) are represented as E4M3 + E5M2
  * parts, 2^-7 relative error at most.  kv_scale must be finite; its
  * magnitude may lie anywhere in [2^-100, 2^100].
