@@ -525,6 +525,23 @@ int mla_debug_gather(const void* kv_pages, mla_kv_dtype kv_dtype,
 int mla_debug_wait(int mode, int delay_us, int* status, uint64_t* elapsed_ns,
                    mla_stream_t stream);
 
+/*
+ * Test entry point of the FP8 cache write's division (mla_kv_write): the
+ * write forms each code's quotient x / scale from one correctly rounded
+ * reciprocal of the row's scale and one Markstein correction instead of an
+ * IEEE division per element.  This runs that routine against the IEEE
+ * division for every positive finite bf16 row maximum amax (scale =
+ * fl32(amax / 448); scales outside [2^-90, 2^120], where the write divides
+ * directly, are skipped) and every bf16 element x with |x| <= amax, and adds to
+ * the two device counters (uint64, zeroed by the caller) the cases where
+ * quotients of magnitude 2^-11 or more differ in any bit, and where the
+ * E4M3 codes differ.  Both stay 0 for a correct build.  No counterpart on
+ * the pages (a property of the quantiser the reading of the pages fixes).
+ * Errors: NULL counter -> MLA_ERR_INVALID_ARG; misaligned -> MLA_ERR_MISALIGNED.
+ */
+int mla_debug_quotients(uint64_t* bit_mismatches, uint64_t* code_mismatches,
+                        mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

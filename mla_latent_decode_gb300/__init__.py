@@ -86,6 +86,7 @@ def library() -> ctypes.CDLL:
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
             "mla_debug_wait": (i32, [i32, i32, p, p, p]),
+            "mla_debug_quotients": (i32, [p, p, p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -444,6 +445,16 @@ def debug_wait(mode: int, delay_us: int, status, elapsed_ns, stream=None):
     with _on(status):
         _check(library().mla_debug_wait(mode, delay_us, _ptr(status),
                                         _ptr(elapsed_ns), _stream(stream)))
+
+
+def debug_quotients(counters, stream=None):
+    """Exhaustive check of the FP8 cache write's division routine against the
+    IEEE division (see mla_debug_quotients); `counters` int64 [2] on the
+    device, zeroed: bit mismatches, code mismatches are added."""
+    with _on(counters):
+        _check(library().mla_debug_quotients(
+            ctypes.c_void_p(counters.data_ptr()),
+            ctypes.c_void_p(counters.data_ptr() + 8), _stream(stream)))
 
 
 def decode(batch, num_splits: Optional[int] = None, simt: bool = False,

@@ -38,11 +38,18 @@ def _rows(n, seed):
     # 448 makes the scale exactly 1 (midpoints of the value set are exact)
     x[6, 0] = 448.0
     x[6, 1:9] = [1.0625, 1.1875, -2.125, 0.0029296875, 300.0, -13.0, 0.75, 15.5]
+    # a row maximum small enough (scale under 2^-90) for the direct division
+    x[7] *= 1e-30
+    # E4M3 midpoints and the 2^-10 boundary at a power-of-two scale 2^-60
+    x[8, :] = 0.0
+    x[8, 0] = 448.0 * 2.0 ** -60
+    x[8, 1:8] = np.array([1.0625, -2.125, 2.0 ** -10, -(2.0 ** -10), 3 * 2.0 ** -11,
+                          208.0, 0.0029296875]) * 2.0 ** -60
     t = torch.from_numpy(x).to(torch.bfloat16)
     return t, t.to(torch.float32).numpy()  # the bf16 values, widened exactly
 
 
-@pytest.mark.parametrize("n", [7, 300])
+@pytest.mark.parametrize("n", [9, 300])
 def test_fp8_write_matches_oracle_bytes(n):
     rows, exact = _rows(n, seed=n)
     num_slots = 4096
@@ -61,6 +68,18 @@ def test_fp8_write_matches_oracle_bytes(n):
     mask = np.ones(num_slots, bool)
     mask[slots.numpy()] = False
     assert (kv.cpu().numpy()[mask] == 0x7F).all()
+
+
+def test_write_quotients_equal_ieee_division_exhaustively():
+    """The write divides by a row's scale through one correctly rounded
+    reciprocal and one Markstein correction: over every positive finite
+    bf16 row maximum and every bf16 element it meets, its quotients equal
+    the IEEE binary32 division bit for bit wherever they can set a code
+    (|q| >= 2^-11), and every E4M3 code is the same."""
+    counters = torch.zeros(2, dtype=torch.int64, device="cuda")
+    mla.debug_quotients(counters)
+    torch.cuda.synchronize()
+    assert counters.tolist() == [0, 0]
 
 
 def test_bf16_write_is_a_copy_and_bad_slot_is_reported():
