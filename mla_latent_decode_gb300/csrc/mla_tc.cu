@@ -102,7 +102,8 @@ struct __align__(1024) Smem {
   uint64_t fin_full;        // O-CTAs: 1/l of every row arrived
   uint64_t epi_go;          // O-CTAs: the epilogue may read O (warps 4-7)
   uint64_t qready;          // rank 0: both S-CTAs' Q rows are in place
-  uint64_t qbar;            // S-CTAs: a pass of query boxes landed
+  uint64_t qbar;            // S-CTAs: the query boxes landed
+  uint64_t qmoved;          // S-CTAs: Q_nope dims 256.. left ring stages 4..7
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -281,14 +282,52 @@ __device__ __forceinline__ uint32_t bf16x2_finite_or_zero(uint32_t x) {
   return x & keep;
 }
 
-// Base slot of page m of the unit's range, or -1 if it lies outside the pool.
-__device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
-                                             int m) {
+// The page-table entry of page m of the unit's range as stored (0 past the
+// range), and its check: the base slot, or -1 if it lies outside the pool.
+// Split so that a load can be put in flight before its value is needed.
+__device__ __forceinline__ int32_t page_entry(const TcParams& p, const Work& w,
+                                              int m) {
   if (m >= w.npages) return 0;
-  const int32_t base = p.r2t[(int64_t)w.v * p.r2t_stride + (w.p0 + m) * kPage];
+  return p.r2t[(int64_t)w.v * p.r2t_stride + (w.p0 + m) * kPage];
+}
+__device__ __forceinline__ int32_t checked_base(const TcParams& p, int32_t base) {
   if (base < 0 || (base & (kPage - 1)) || (int64_t)base + kPage > p.num_slots)
     return -1;
   return base;
+}
+__device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
+                                             int m) {
+  return checked_base(p, page_entry(p, w, m));
+}
+
+// S-CTA, thread 0, at kernel entry: initialise the query barriers and put the
+// query rows of this CTA's row group in flight (boxes of 64 values x
+// q_box_rows rows): Q_nope dims 0..255 into the four P slots, dims 256..511
+// into ring stages 4..7, Q_rope into its operand buffer, all on qbar.
+constexpr int kQRingStage0 = 4;
+static_assert(kQRingStage0 + 4 <= kStages, "query boxes in the ring");
+__device__ __forceinline__ void issue_query(Smem& s, const CUtensorMap* qn_map,
+                                            const CUtensorMap* qr_map,
+                                            const TcParams& p, int unit,
+                                            uint32_t rank) {
+  const int u = unit % p.U;
+  const int v = (unit / p.U) % p.V;
+  const int b = v % p.B;
+  const int qy = b * p.q_len * p.H + (2 * u + (int)(rank & 1)) * kRows;
+  const uint32_t qbar = smem_u32(&s.qbar);
+  mbar_init(qbar, 1);
+  mbar_init(smem_u32(&s.qmoved), 4);  // the 4 warps of softmax warpgroup 0
+  fence_mbar_init();
+  prefetch_tmap(qn_map);
+  prefetch_tmap(qr_map);
+  const uint32_t box = (uint32_t)p.q_box_rows * 128u;
+  mbar_arrive_expect_tx(qbar, 9 * box);
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t dst = k < 4 ? smem_u32(s.pslot[k])
+                               : smem_u32(s.ring[(kQRingStage0 + k - 4) * kBoxesPerStage]);
+    tma_load_3d(dst, qn_map, qbar, 64 * k, qy, 0);
+  }
+  tma_load_3d(smem_u32(s.qrope), qr_map, qbar, 0, qy, 0);
 }
 
 // ------------------------------------------------------- S-CTA producers ---
@@ -302,10 +341,14 @@ __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
 // the S columns they feed, which the softmax masks.
 __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
-                                           uint32_t rank, int lane) {
+                                           uint32_t rank, int lane,
+                                           int32_t cur, int32_t nxt) {
+  // cur, nxt: the raw page-table entries of pages lane and 32 + lane
+  cur = checked_base(p, cur);
+  nxt = checked_base(p, nxt);
   uint32_t stage = 0, phase = 0;
-  int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
+  bool q_out = false;  // the query boxes have left ring stages 4..7
   const uint32_t full0 = mapa(smem_u32(&s.full[0]), 0);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
   for (int j = 0; j < ntiles && ok; ++j) {
@@ -324,7 +367,13 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
     if (lane < mine && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
     for (int c = 0; c < kBf16BoxesPerPage && ok; ++c) {
       if (lane == 0) {
-        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+        // Stages 4..7 hold the query's c_kv dims 256..511 until the softmax
+        // has moved them into tensor memory.
+        if (!q_out && stage == kQRingStage0) {
+          if (!mbar_wait(smem_u32(&s.qmoved), 0, &s.abort_flag)) ok = false;
+          q_out = true;
+        }
+        if (ok && mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
           if (rank == 0)
             mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * kBoxBytes);
         } else {
@@ -510,57 +559,42 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   const int64_t qrow = (int64_t)w.b * p.q_len * p.H + rr;
 
   // Q rows by TMA (boxes of 64 values x 128 rows, 128-byte swizzle, rows
-  // from this CTA's first): the rope part straight into its MMA operand
-  // buffer; the nope part in two passes of four boxes through the P slots,
-  // idle until the first S tile, from which warpgroup 0 moves row r to TMEM
-  // lane r (columns [0, 256), column c holding elements 2c, 2c+1).
+  // from this CTA's first), issued at kernel entry (issue_query): the rope
+  // part straight into its MMA operand buffer; the nope part's dims 0..255
+  // in the P slots, idle until the first S tile, and dims 256..511 in ring
+  // stages 4..7, which the producer fills only once they are moved out
+  // (qmoved).  Warpgroup 0 moves row r to TMEM lane r (columns [0, 256),
+  // column c holding elements 2c, 2c+1).
   {
-    const int qy = w.b * p.q_len * p.H + w.r_base;
-    const uint32_t box = (uint32_t)p.q_box_rows * 128u;
-    const uint32_t qbar = smem_u32(&s.qbar);
-    if (warp == 4 && lane == 0) {
-      mbar_arrive_expect_tx(qbar, 5 * box);
-      for (int k = 0; k < 4; ++k)
-        tma_load_3d(smem_u32(s.pslot[k]), qn_map, qbar, 64 * k, qy, 0);
-      tma_load_3d(smem_u32(s.qrope), qr_map, qbar, 0, qy, 0);
-    }
-    bool qok = mbar_wait(qbar, 0, &s.abort_flag);
+    const bool qok = mbar_wait(smem_u32(&s.qbar), 0, &s.abort_flag);
     if (g == 0) {
-      for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) {
-          named_bar_sync(2, 128);  // every row of the first pass read
-          if (warp == 4 && lane == 0) {
-            mbar_arrive_expect_tx(qbar, 4 * box);
-            for (int k = 0; k < 4; ++k)
-              tma_load_3d(smem_u32(s.pslot[k]), qn_map, qbar, 64 * (4 + k), qy,
-                          0);
-          }
-          qok = qok && mbar_wait(qbar, 1, &s.abort_flag);
-        }
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        const uint8_t* src = k < 4 ? s.pslot[k] : s.ring[(kQRingStage0 + k - 4) * kBoxesPerStage];
+        uint32_t v[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t v[32];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 x =
-                row_ok && qok ? *reinterpret_cast<const uint4*>(
-                                    s.pslot[k] + box_chunk_offset(r, e))
-                              : make_uint4(0, 0, 0, 0);
-            v[4 * e] = x.x;
-            v[4 * e + 1] = x.y;
-            v[4 * e + 2] = x.z;
-            v[4 * e + 3] = x.w;
-          }
-          tmem_st32(tmem + lane_base + 32u * (4 * pass + k), v);
+        for (int e = 0; e < 8; ++e) {
+          const uint4 x = row_ok && qok ? *reinterpret_cast<const uint4*>(
+                                              src + box_chunk_offset(r, e))
+                                        : make_uint4(0, 0, 0, 0);
+          v[4 * e] = x.x;
+          v[4 * e + 1] = x.y;
+          v[4 * e + 2] = x.z;
+          v[4 * e + 3] = x.w;
         }
+        tmem_st32(tmem + lane_base + 32u * k, v);
       }
       tmem_wait_st();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.qmoved));
     }
     if (!__all_sync(kFull, qok) && lane == 0) signal_abort(s, p, rank);
   }
+  // Q is complete in this CTA (TMEM stores waited for, the rope box landed
+  // on qbar): the signal only reports finished work, so it is relaxed.
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) arrive_leader(smem_u32(&s.qready), rank, 0);
+  if (lane == 0) signal_leader(smem_u32(&s.qready), rank, 0);
 
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
@@ -965,12 +999,23 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
-  if (cluster_unit(p) < 0) {  // every CTA of the cluster read the same entry
+  const int unit = cluster_unit(p);
+  if (unit < 0) {  // every CTA of the cluster read the same entry
     if (rank == 0 && threadIdx.x == 0 && p.status)
       atomicOr(p.status, MLA_STATUS_BAD_WORK);
     return;
   }
-  const Work w = unit_work(p, cluster_unit(p), rank);
+  // The query rows need only the unit id: the S-CTAs put them in flight
+  // before anything else, so their load overlaps the rest of the set-up.
+  if (rank < 2 && threadIdx.x == 0) issue_query(s, &qn_map, &qr_map, p, unit, rank);
+  const Work w = unit_work(p, unit, rank);
+  // The S producer's first page-table entries, also in flight during the
+  // set-up (checked only when the producer starts).
+  int32_t pb_cur = 0, pb_nxt = 0;
+  if (rank < 2 && warp == 0 && w.npages > 0) {
+    pb_cur = page_entry(p, w, lane);
+    pb_nxt = page_entry(p, w, 32 + lane);
+  }
 
   // The stream's next kernel (the LSE combine) may be scheduled from now
   // on; it waits for this grid's completion before it reads a part.
@@ -1000,7 +1045,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.epi_go), 4);
     mbar_init(smem_u32(&s.qready), 16);
-    mbar_init(smem_u32(&s.qbar), 1);
     if (rank >= 2 && w.npages > 0) {
       mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
       // rank 2 also receives rank 1's 16 flag bytes per message
@@ -1010,10 +1054,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
-    if (rank < 2) {
-      prefetch_tmap(&qn_map);
-      prefetch_tmap(&qr_map);
-    }
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -1078,7 +1118,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
       if (warp == 0) {
-        producer_s(s, &kv_map, p, w, rank, lane);
+        producer_s(s, &kv_map, p, w, rank, lane, pb_cur, pb_nxt);
       } else if (warp == 1 && rank == 0) {
         if (lane == 0) mma_s(s, p, w, tmem, rank);
         __syncwarp();
@@ -1107,7 +1147,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= 8) {
       store_o_upper(s, p, w, tmem, warp, lane);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (rank < 2 && threadIdx.x == 0) {
+    // No tokens for this split: the query boxes issued at entry land before
+    // the CTA leaves.
+    mbar_wait(smem_u32(&s.qbar), 0, &s.abort_flag);
+  }
+  if (w.npages == 0 && warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0 (O-CTAs), LSE = -inf (S-CTAs).
     const int r = (warp & 3) * 32 + lane;
     if (r < w.nrows) {
