@@ -715,6 +715,29 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
   }
 }
 
+// S-CTA, thread 0, at kernel entry (the boxes need only the unit id, so
+// their load overlaps the rest of the set-up): initialise qbar and load the
+// pair's query rows, boxes of 64 values x q_box_rows rows with the 128-byte
+// swizzle, the c_kv dims into the still idle ring and the RoPE dims into P
+// slot 0.
+__device__ __forceinline__ void issue_query(Smem& s, const CUtensorMap* qn_map,
+                                            const CUtensorMap* qr_map,
+                                            const TcParams& p, int unit) {
+  const int g = unit % p.G;
+  const int v = (unit / p.G) % p.V;
+  const int qy = (v % p.B) * p.q_len * p.H + g * kRows;
+  const uint32_t qbar = smem_u32(&s.qbar);
+  mbar_init(qbar, 1);
+  fence_mbar_init();
+  prefetch_tmap(qn_map);
+  prefetch_tmap(qr_map);
+  const uint32_t box = (uint32_t)p.q_box_rows * 128u;
+  mbar_arrive_expect_tx(qbar, 9 * box);
+  for (int k = 0; k < 8; ++k)
+    tma_load_3d(smem_u32(s.ring[0]) + 16384u * k, qn_map, qbar, 64 * k, qy, 0);
+  tma_load_3d(smem_u32(s.pslot[0]), qr_map, qbar, 0, qy, 0);
+}
+
 // ------------------------------------------------------ S-CTA: softmax ----
 // Warps 4..19: four warpgroups; warpgroup g (warps 4g + 4 .. 4g + 7) owns
 // page g of each S tile, warp quad (warp % 4) owns TMEM lanes (query rows)
@@ -756,15 +779,8 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   const int rA = quad * 32 + (lane & 15), rB = rA + 16;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
 
+  // The query boxes were put in flight at kernel entry (issue_query).
   const uint32_t qbar = smem_u32(&s.qbar);
-  if (warp == 4 && lane == 0) {
-    const uint32_t box = (uint32_t)p.q_box_rows * 128u;
-    const int qy = w.b * p.q_len * p.H + w.r_base;
-    mbar_arrive_expect_tx(qbar, 9 * box);
-    for (int k = 0; k < 8; ++k)
-      tma_load_3d(smem_u32(s.ring[0]) + 16384u * k, qn_map, qbar, 64 * k, qy, 0);
-    tma_load_3d(smem_u32(s.pslot[0]), qr_map, qbar, 0, qy, 0);
-  }
   const bool qok = mbar_wait(qbar, 0, &s.abort_flag);
   // 16-byte chunk k of this row's c_kv dims (k < 64) or RoPE dims (k < 8).
   auto qchunk = [&](int k) -> uint4 {
@@ -1435,6 +1451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       atomicOr(p.status, MLA_STATUS_BAD_WORK);
     return;
   }
+  if (rank == 0 && threadIdx.x == 0) issue_query(s, &qn_map, &qr_map, p, unit);
   const Work w = pair_work(p, unit);
 
   if (threadIdx.x == 0) {
@@ -1468,7 +1485,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.corr_done), 4);
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.qready), 16);
-    mbar_init(smem_u32(&s.qbar), 1);
     mbar_init(smem_u32(&s.tail_go), 1);
     mbar_init(smem_u32(&s.tail_ready), 1);
     if (rank == 1 && w.npages > 0) {
@@ -1479,10 +1495,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&kv_map);
     prefetch_tmap(&rope_map);
-    if (rank == 0) {
-      prefetch_tmap(&qn_map);
-      prefetch_tmap(&qr_map);
-    }
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -1577,7 +1589,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= 8 && warp < 12) {
       packer(s, p, w, rank, warp, lane);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (rank == 0 && threadIdx.x == 0) {
+    // No tokens for this split: the query boxes issued at entry land before
+    // the CTA leaves.
+    mbar_wait(smem_u32(&s.qbar), 0, &s.abort_flag);
+  }
+  if (w.npages == 0 && warp >= 4 && warp < 8) {
     // No tokens for this split: O = 0, LSE = -inf.
     const int r = (warp & 3) * 32 + lane;
     if (r < w.nrows) {
