@@ -447,7 +447,11 @@ int mla_kv_write(const void* rows, int64_t n, const int32_t* slots,
  *     o_latent bf16 [M, H, 512] (the decode's out); w_vc bf16 [H, 512, 128]
  *     (reading: v_head_dim 128, the pages give w_vc's name only); o_v bf16
  *     [M, H, 128]
- * All arrays device, contiguous, 16-B aligned; 1 <= H <= 65535, M >= 1.
+ * All arrays device, contiguous, 16-B aligned; H >= 1, M >= 1, and
+ * ceil(M / 128) * H * 4 < 2^31 (else MLA_ERR_INVALID_ARG).  Launched with
+ * programmatic dependent launch: the kernel starts while the stream's
+ * previous kernels finish, prefetches its weights into L2, and waits for
+ * them before it reads any input or writes any output.
  * A bounded wait that gives up sets MLA_STATUS_WAIT_TIMEOUT in status.
  */
 int mla_absorb_q(const void* q_nope, const void* w_kc, void* q_absorbed, int M,

@@ -72,3 +72,28 @@ def test_projection_argument_errors():
     w = torch.zeros((96, 128, 512), dtype=torch.bfloat16, device="cuda")
     y = torch.zeros((1, 1, 96, 512), dtype=torch.bfloat16, device="cuda")
     assert lib.mla_absorb_q(mla._ptr(x), mla._ptr(w), mla._ptr(y), 0, 96, None, None) == -1
+
+
+def test_chained_launches_read_what_the_previous_launch_wrote():
+    """Both projections let the stream's next kernel start early and prefetch
+    its weights before waiting: a launch whose activations and weights are
+    the output of the launch just before it (no synchronisation between
+    them) must read the written values."""
+    H = 96
+    g = torch.Generator(device="cuda").manual_seed(7)
+    o = torch.randn((512, 1, H, 512), generator=g, device="cuda").to(torch.bfloat16)
+    w_vc = (torch.randn((H, 512, 128), generator=g, device="cuda") / 22.6).to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = torch.full((512, 1, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    z = torch.empty((80, 1, H, 512), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        mla.project_out(o, w_vc, y, status=st)
+        mla.absorb_q(y[:80], y.view(H, 128, 512), z, status=st)
+        y.fill_(float("nan"))
+        mla.project_out(o, w_vc, y, status=st)
+        mla.absorb_q(y[:80], y.view(H, 128, 512), z, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check(y.view(512, H, 128), o.view(512, H, 512), w_vc)
+    _check(z.view(80, H, 512), y[:80].view(80, H, 128), y.view(H, 128, 512))
