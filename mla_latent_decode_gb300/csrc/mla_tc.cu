@@ -300,34 +300,42 @@ __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
   return checked_base(p, page_entry(p, w, m));
 }
 
-// S-CTA, thread 0, at kernel entry: initialise the query barriers and put the
+// S-CTA, warp 0, at kernel entry: initialise the query barriers and put the
 // query rows of this CTA's row group in flight (boxes of 64 values x
 // q_box_rows rows): Q_nope dims 0..255 into the four P slots, dims 256..511
-// into ring stages 4..7, Q_rope into its operand buffer, all on qbar.
+// into ring stages 4..7, Q_rope into its operand buffer, all on qbar.  Lane
+// k issues box k: a thread's TMA loads are processed one after another
+// (~0.25 us each whatever their size), loads of different threads side by
+// side.
 constexpr int kQRingStage0 = 4;
 static_assert(kQRingStage0 + 4 <= kStages, "query boxes in the ring");
 __device__ __forceinline__ void issue_query(Smem& s, const CUtensorMap* qn_map,
                                             const CUtensorMap* qr_map,
                                             const TcParams& p, int unit,
-                                            uint32_t rank) {
+                                            uint32_t rank, int lane) {
   const int u = unit % p.U;
   const int v = (unit / p.U) % p.V;
   const int b = v % p.B;
   const int qy = b * p.q_len * p.H + (2 * u + (int)(rank & 1)) * kRows;
   const uint32_t qbar = smem_u32(&s.qbar);
-  mbar_init(qbar, 1);
-  mbar_init(smem_u32(&s.qmoved), 4);  // the 4 warps of softmax warpgroup 0
-  fence_mbar_init();
-  prefetch_tmap(qn_map);
-  prefetch_tmap(qr_map);
-  const uint32_t box = (uint32_t)p.q_box_rows * 128u;
-  mbar_arrive_expect_tx(qbar, 9 * box);
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t dst = k < 4 ? smem_u32(s.pslot[k])
-                               : smem_u32(s.ring[(kQRingStage0 + k - 4) * kBoxesPerStage]);
-    tma_load_3d(dst, qn_map, qbar, 64 * k, qy, 0);
+  if (lane == 0) {
+    mbar_init(qbar, 1);
+    mbar_init(smem_u32(&s.qmoved), 4);  // the 4 warps of softmax warpgroup 0
+    fence_mbar_init();
+    prefetch_tmap(qn_map);
+    prefetch_tmap(qr_map);
+    const uint32_t box = (uint32_t)p.q_box_rows * 128u;
+    mbar_arrive_expect_tx(qbar, 9 * box);
   }
-  tma_load_3d(smem_u32(s.qrope), qr_map, qbar, 0, qy, 0);
+  __syncwarp();
+  if (lane < 8) {
+    const uint32_t dst =
+        lane < 4 ? smem_u32(s.pslot[lane])
+                 : smem_u32(s.ring[(kQRingStage0 + lane - 4) * kBoxesPerStage]);
+    tma_load_3d(dst, qn_map, qbar, 64 * lane, qy, 0);
+  } else if (lane == 8) {
+    tma_load_3d(smem_u32(s.qrope), qr_map, qbar, 0, qy, 0);
+  }
 }
 
 // ------------------------------------------------------- S-CTA producers ---
@@ -338,7 +346,11 @@ __device__ __forceinline__ void issue_query(Smem& s, const CUtensorMap* qn_map,
 // MMA released it (empty, multicast to both).  Page bases are read 32 pages
 // ahead (one per lane) so a TMA issue never waits on a dependent global
 // load.  Pages of a short last tile that are not loaded leave stale bytes in
-// the S columns they feed, which the softmax masks.
+// the S columns they feed, which the softmax masks.  A thread's TMA loads
+// are processed one after another (~0.25 us each), so the first tile's
+// chunks 0..7, which fill the empty ring, are issued by 16 lanes at once
+// (chunks 4..7 once the query has left their stages); later chunks, paced
+// by the MMA, by lanes 0 and 1 (more lanes in flight there measured slower).
 __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
                                            const TcParams& p, const Work& w,
                                            uint32_t rank, int lane,
@@ -346,11 +358,39 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   // cur, nxt: the raw page-table entries of pages lane and 32 + lane
   cur = checked_base(p, cur);
   nxt = checked_base(p, nxt);
-  uint32_t stage = 0, phase = 0;
+  static_assert(kStages < kBf16BoxesPerPage && kQRingStage0 == kStages / 2,
+                "the ring's first pass lies in tile 0");
   bool ok = true;
-  bool q_out = false;  // the query boxes have left ring stages 4..7
   const uint32_t full0 = mapa(smem_u32(&s.full[0]), 0);
   const int ntiles = (w.npages + kTilePages - 1) / kTilePages;
+  {
+    // Tile 0, chunks 0..7: lanes 2i, 2i + 1 issue chunk i of both pages.
+    const int np = tile_pages(w, 0);
+    const int mine = min(2, max(0, np - 2 * (int)rank));
+    const int32_t bq = __shfl_sync(kFull, cur, 2 * (int)rank + (lane & 1));
+    const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
+    if (lane < mine && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
+    const int i = lane >> 1;
+    for (int half = 0; half < 2; ++half) {
+      if (half == 1) {
+        // Stages 4..7 hold the query's c_kv dims 256..511 until the softmax
+        // has moved them into tensor memory.
+        if (lane == 0 && !mbar_wait(smem_u32(&s.qmoved), 0, &s.abort_flag))
+          ok = false;
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;
+      }
+      const int c = half * kQRingStage0 + i;  // chunk = ring stage
+      if (i < kQRingStage0) {
+        if (rank == 0 && (lane & 1) == 0)
+          mbar_arrive_expect_tx(smem_u32(&s.full[c]), np * kBoxBytes);
+        if ((lane & 1) < mine)
+          tma_load_2d_pair(smem_u32(s.ring[c * kBoxesPerStage + (lane & 1)]),
+                           map, full0 + 8u * c, c * 64, yq);
+      }
+    }
+  }
+  uint32_t stage = 0, phase = 1;  // the ring's second pass
   for (int j = 0; j < ntiles && ok; ++j) {
     const int m0 = j * kTilePages;
     if (m0 % 32 == 0 && m0 > 0) {
@@ -364,16 +404,11 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
     const int32_t bq =
         __shfl_sync(kFull, cur, (m0 + 2 * (int)rank + (lane & 1)) & 31);
     const int32_t yq = bq < 0 ? (int32_t)p.num_slots : bq;
-    if (lane < mine && bq < 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_SLOT);
-    for (int c = 0; c < kBf16BoxesPerPage && ok; ++c) {
+    if (j > 0 && lane < mine && bq < 0 && p.status)
+      atomicOr(p.status, MLA_STATUS_BAD_SLOT);
+    for (int c = j == 0 ? kStages : 0; c < kBf16BoxesPerPage && ok; ++c) {
       if (lane == 0) {
-        // Stages 4..7 hold the query's c_kv dims 256..511 until the softmax
-        // has moved them into tensor memory.
-        if (!q_out && stage == kQRingStage0) {
-          if (!mbar_wait(smem_u32(&s.qmoved), 0, &s.abort_flag)) ok = false;
-          q_out = true;
-        }
-        if (ok && mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
+        if (mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, &s.abort_flag)) {
           if (rank == 0)
             mbar_arrive_expect_tx(smem_u32(&s.full[stage]), np * kBoxBytes);
         } else {
@@ -1007,7 +1042,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
   }
   // The query rows need only the unit id: the S-CTAs put them in flight
   // before anything else, so their load overlaps the rest of the set-up.
-  if (rank < 2 && threadIdx.x == 0) issue_query(s, &qn_map, &qr_map, p, unit, rank);
+  if (rank < 2 && warp == 0) issue_query(s, &qn_map, &qr_map, p, unit, rank, lane);
   const Work w = unit_work(p, unit, rank);
   // The S producer's first page-table entries, also in flight during the
   // set-up (checked only when the producer starts).
