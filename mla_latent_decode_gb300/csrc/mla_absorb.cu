@@ -48,29 +48,6 @@ constexpr int kBoxW = 64 * 128;   // 64 K rows x 64 N bf16 = 8 KB
 constexpr int kBoxOut = 32 * 128; // 32 rows x 64 N bf16 = 4 KB
 constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
-// TMA store of the 3-D box at (x, y, z) from this CTA's shared memory
-// (elements outside the tensor are not written), tracked by the thread's
-// bulk async-group.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
-                                             int32_t x, int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, "
-      "%2, %3}], [%4];" ::"l"(tmap),
-      "r"(x), "r"(y), "r"(z), "r"(src)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// The thread's committed stores have read their shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// The thread's committed stores have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 template <int K, int N, int NC, int STAGES>
 struct HeadGemm {
   static constexpr int kStageBytes = kBoxA + (NC / 64) * kBoxW;

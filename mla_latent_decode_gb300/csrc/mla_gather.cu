@@ -71,6 +71,23 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
   return MLA_OK;
 }
 
+int make_o_part_map(CUtensorMap* map, float* O_part, int64_t total_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)MLA_VALUE_DIM, (cuuint64_t)total_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)MLA_VALUE_DIM * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, O_part, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled (O_part) failed (%d)",
+                (int)r);
+  return MLA_OK;
+}
+
 int make_query_maps(CUtensorMap* nope, CUtensorMap* rope, const DecodeArgs& a,
                     int* box_rows) {
   const uint64_t rows = (uint64_t)a.B * a.q_len * a.H;

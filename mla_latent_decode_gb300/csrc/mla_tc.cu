@@ -39,6 +39,8 @@
 //   cluster finishes early.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "mla_combine.cuh"
 #include "mla_tma.cuh"
 #include "ptx_sm103.cuh"
@@ -131,6 +133,7 @@ struct TcParams {
   float* LSE_part;
   int* status;
   int q_box_rows;          // rows of a query TMA box: min(128, B * q_len * H)
+  int o_tma;               // O_part rows leave by TMA store (o_map is valid)
   __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
   float* lse_out;
   int* counters;
@@ -924,6 +927,7 @@ __device__ __forceinline__ void relay_o(Smem& s, const TcParams& p,
 // of row 4i + l / 8: every store instruction writes four full 128-byte
 // lines of O_part.
 __device__ __forceinline__ void store_o_rows(Smem& s, const TcParams& p,
+                                             const CUtensorMap* o_map,
                                              const Work& w, uint32_t tmem,
                                              int warp, int lane, int half) {
   const int quad = warp & 3;
@@ -931,10 +935,46 @@ __device__ __forceinline__ void store_o_rows(Smem& s, const TcParams& p,
   const float inv = s.fin[quad * 32 + lane];
   const int64_t rows = (int64_t)p.B * p.q_len * p.H;
   const int64_t part = (int64_t)w.split * (p.V / p.B) + w.shard;
-  float* const dst0 = p.O_part + (part * rows + (int64_t)w.b * p.q_len * p.H +
-                                  w.r_base + quad * 32) * MLA_VALUE_DIM;
+  const int64_t row0 =
+      part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + quad * 32;
+  float* const dst0 = p.O_part + row0 * MLA_VALUE_DIM;
   const int nvalid = w.nrows - quad * 32;  // rows of this warp in range
-  uint8_t* const buf = s.ring[warp - 4];
+  if (p.o_tma && nvalid >= 32) {
+    // Whole 32-row blocks leave by TMA store, 32 values (128 bytes) per
+    // box: four boxes of this warp's 16 KB of the idle ring in turn, box i
+    // stored by lane i (a thread's TMA operations are processed one after
+    // another), which waits for the box's previous store to have read it
+    // before the warp refills it.
+    uint8_t* const bufs = s.ring[2 * (warp - 4)];
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      const int c0 = 256 * half + 32 * k;
+      const int bi = k & 3;
+      uint8_t* const box = bufs + bi * 4096;
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + c0, v);
+      if (k >= 4 && lane == bi) bulk_wait_read_all();
+      __syncwarp();
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<float4*>(box + box_chunk_offset(lane, e)) =
+            make_float4(__uint_as_float(v[4 * e]) * inv,
+                        __uint_as_float(v[4 * e + 1]) * inv,
+                        __uint_as_float(v[4 * e + 2]) * inv,
+                        __uint_as_float(v[4 * e + 3]) * inv);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == bi) {
+        tma_store_2d(o_map, smem_u32(box), c0, (int32_t)row0);
+        bulk_commit_group();
+      }
+    }
+    if (lane < 4) bulk_wait_read_all();
+    __syncwarp();
+    return;
+  }
+  uint8_t* const buf = s.ring[2 * (warp - 4)];  // this warp's 16 KB as above
 #pragma unroll 1
   for (int k = 0; k < 8; ++k) {
     const int c0 = 256 * half + 32 * k;
@@ -965,11 +1005,12 @@ __device__ __forceinline__ void store_o_rows(Smem& s, const TcParams& p,
 // Warps 8..11 of each O-CTA: the second half of the value columns, once
 // warps 4..7 have seen the last drain and 1/l.
 __device__ __forceinline__ void store_o_upper(Smem& s, const TcParams& p,
+                                              const CUtensorMap* o_map,
                                               const Work& w, uint32_t tmem,
                                               int warp, int lane) {
   if (!mbar_wait(smem_u32(&s.epi_go), 0, &s.abort_flag)) return;
   tc_fence_after();
-  store_o_rows(s, p, w, tmem, warp, lane, 1);
+  store_o_rows(s, p, o_map, w, tmem, warp, lane, 1);
 }
 
 // ---------------------------------------- O-CTA: correction + epilogue ----
@@ -979,6 +1020,7 @@ __device__ __forceinline__ void store_o_upper(Smem& s, const TcParams& p,
 // or, the last one, for the epilogue: O_part = O / l over the first half of
 // the value columns (warps 8..11 take the second, after epi_go).
 __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
+                                                  const CUtensorMap* o_map,
                                                   const Work& w, uint32_t tmem,
                                                   uint32_t rank, int warp,
                                                   int lane) {
@@ -1020,7 +1062,7 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
   tc_fence_after();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&s.epi_go));
-  store_o_rows(s, p, w, tmem, warp, lane, 0);
+  store_o_rows(s, p, o_map, w, tmem, warp, lane, 0);
 }
 
 // ------------------------------------------------------------- kernel ----
@@ -1028,6 +1070,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                           const __grid_constant__ CUtensorMap qn_map,
                           const __grid_constant__ CUtensorMap qr_map,
+                          const __grid_constant__ CUtensorMap o_map,
                           const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -1089,6 +1132,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
     prefetch_tmap(&kv_map);
+    if (rank >= 2 && p.o_tma) prefetch_tmap(&o_map);
   }
   if (rank == 0 && threadIdx.x == 32 && p.seq_lens[w.v] > p.r2t_stride &&
       p.status)
@@ -1178,9 +1222,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4 && warp < 8) {
-      correct_and_store(s, p, w, tmem, rank, warp, lane);
+      correct_and_store(s, p, &o_map, w, tmem, rank, warp, lane);
     } else if (warp >= 8) {
-      store_o_upper(s, p, w, tmem, warp, lane);
+      store_o_upper(s, p, &o_map, w, tmem, warp, lane);
     }
   } else if (rank < 2 && threadIdx.x == 0) {
     // No tokens for this split: the query boxes issued at entry land before
@@ -1242,12 +1286,22 @@ int launch_tc(const DecodeArgs& a) {
   if (rc != MLA_OK) return rc;
   rc = make_query_maps(&qn_map, &qr_map, a, &p.q_box_rows);
   if (rc != MLA_OK) return rc;
+  // The partial outputs leave by TMA store when their rows fit the tensor
+  // map's 32-bit coordinates; the fused combine, which reads other
+  // clusters' parts in the same launch, keeps the plain stores its fences
+  // order.
+  CUtensorMap o_map;
+  std::memset(&o_map, 0, sizeof(o_map));
+  const int64_t o_rows =
+      (int64_t)p.num_splits * a.num_shards * a.B * a.q_len * a.H;
+  p.o_tma = !p.counters && o_rows < 0x7fffffff &&
+            make_o_part_map(&o_map, p.O_part, o_rows) == MLA_OK;
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc)");
   mla_partial_tc_kernel<<<(unsigned)(units * kCtas), kThreads, kSmemBytes,
-                          a.stream>>>(map, qn_map, qr_map, p);
+                          a.stream>>>(map, qn_map, qr_map, o_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_partial_tc_kernel");
   return MLA_OK;

@@ -45,6 +45,11 @@ int make_tensor_map_bf16_3d(CUtensorMap* map, const void* base,
 int make_query_maps(CUtensorMap* nope, CUtensorMap* rope, const DecodeArgs& a,
                     int* box_rows);
 
+// Tensor map of the partial outputs, fp32 [total_rows, 512], in boxes of 32
+// rows x 32 values (128 bytes) with the 128-byte swizzle: the O-CTAs' TMA
+// stores.
+int make_o_part_map(CUtensorMap* map, float* O_part, int64_t total_rows);
+
 // Tensor map of an E4M3 pool in boxes of 64 rows x 64 bytes with the 64-byte
 // swizzle (4 KB): the RoPE key columns 512..575 of one page, the K-major
 // operand layout the FP8 decode kernel's tensor cores read for those dims.

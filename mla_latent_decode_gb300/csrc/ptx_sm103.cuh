@@ -189,6 +189,36 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x,
       : "memory");
 }
 
+// TMA stores from this CTA's shared memory (elements outside the tensor are
+// not written), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src,
+                                             int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, "
+      "%2}], [%3];" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
+                                             int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, "
+      "%2, %3}], [%4];" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The thread's committed stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The thread's committed stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Programmatic dependent launch: let the next kernel of the stream (launched
 // with programmatic stream serialization) start its prologue now; and wait
 // until every grid this one depends on has completed with its memory
