@@ -103,9 +103,9 @@ struct __align__(1024) Smem {
   uint64_t tail_ready[kStagesO];  // rank 2: both halves of that page sanitised
   uint64_t fin_full;        // O-CTAs: 1/l of every row arrived
   uint64_t epi_go;          // O-CTAs: the epilogue may read O (warps 4-7)
-  uint64_t qready;          // rank 0: both S-CTAs' Q rows are in place
+  uint64_t qready;          // rank 0: both S-CTAs' query boxes landed
   uint64_t qbar;            // S-CTAs: the query boxes landed
-  uint64_t qmoved;          // S-CTAs: Q_nope dims 256.. left ring stages 4..7
+  uint64_t qmoved;          // S-CTAs: Q_nope is in TMEM (its boxes are free)
   uint32_t tmem_base;
   int abort_flag;
   int ctl_slot;
@@ -323,7 +323,7 @@ __device__ __forceinline__ void issue_query(Smem& s, const CUtensorMap* qn_map,
   const uint32_t qbar = smem_u32(&s.qbar);
   if (lane == 0) {
     mbar_init(qbar, 1);
-    mbar_init(smem_u32(&s.qmoved), 4);  // the 4 warps of softmax warpgroup 0
+    mbar_init(smem_u32(&s.qmoved), 1);  // the pair commit after the copies
     fence_mbar_init();
     prefetch_tmap(qn_map);
     prefetch_tmap(qr_map);
@@ -528,6 +528,21 @@ __device__ __forceinline__ void mma_s(Smem& s, const TcParams& p,
     return;
   }
   tc_fence_after();
+  // Q_nope into TMEM columns [0, 256) of both S-CTAs (row r in lane r,
+  // column c holding elements 2c, 2c+1): box k (dims 64k..) in 4 copies of
+  // 16 dims; the commit frees the boxes' buffers (qmoved) once the copies
+  // have read them, and the MMAs below, issued after the copies by this
+  // thread, see the copied values.
+#pragma unroll 1
+  for (int k = 0; k < 8; ++k) {
+    const uint8_t* src =
+        k < 4 ? s.pslot[k] : s.ring[(kQRingStage0 + k - 4) * kBoxesPerStage];
+    const uint64_t q = sdesc_sw128(smem_u32(src), 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      tmem_cp_128x256b_pair(tmem + 32u * k + 8u * kk, q + 2 * kk);
+  }
+  mma_commit_pair(smem_u32(&s.qmoved), kMaskS);
   const uint32_t d = tmem + kSCol0;
   const uint64_t qr = sdesc_sw128(smem_u32(s.qrope), 16, 1024);
   uint32_t stage = 0, phase = 0;
@@ -600,39 +615,19 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   // from this CTA's first), issued at kernel entry (issue_query): the rope
   // part straight into its MMA operand buffer; the nope part's dims 0..255
   // in the P slots, idle until the first S tile, and dims 256..511 in ring
-  // stages 4..7, which the producer fills only once they are moved out
-  // (qmoved).  Warpgroup 0 moves row r to TMEM lane r (columns [0, 256),
-  // column c holding elements 2c, 2c+1).
-  {
-    const bool qok = mbar_wait(smem_u32(&s.qbar), 0, &s.abort_flag);
-    if (g == 0) {
-#pragma unroll 1
-      for (int k = 0; k < 8; ++k) {
-        const uint8_t* src = k < 4 ? s.pslot[k] : s.ring[(kQRingStage0 + k - 4) * kBoxesPerStage];
-        uint32_t v[32];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint4 x = row_ok && qok ? *reinterpret_cast<const uint4*>(
-                                              src + box_chunk_offset(r, e))
-                                        : make_uint4(0, 0, 0, 0);
-          v[4 * e] = x.x;
-          v[4 * e + 1] = x.y;
-          v[4 * e + 2] = x.z;
-          v[4 * e + 3] = x.w;
-        }
-        tmem_st32(tmem + lane_base + 32u * k, v);
-      }
-      tmem_wait_st();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.qmoved));
+  // stages 4..7, which the producer fills only once they are copied out
+  // (qmoved).  Once both S-CTAs' boxes landed, the MMA thread copies Q_nope
+  // into TMEM (mma_s).  The landing is finished work seen on qbar, so the
+  // signal is relaxed.
+  if (warp == 4) {
+    if (lane == 0) {
+      if (mbar_wait(smem_u32(&s.qbar), 0, &s.abort_flag))
+        signal_leader(smem_u32(&s.qready), rank, 0);
+      else
+        signal_abort(s, p, rank);
     }
-    if (!__all_sync(kFull, qok) && lane == 0) signal_abort(s, p, rank);
+    __syncwarp();
   }
-  // Q is complete in this CTA (TMEM stores waited for, the rope box landed
-  // on qbar): the signal only reports finished work, so it is relaxed.
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) signal_leader(smem_u32(&s.qready), rank, 0);
 
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
@@ -1122,7 +1117,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&s.fin_full), 1);
     mbar_init(smem_u32(&s.epi_go), 4);
-    mbar_init(smem_u32(&s.qready), 16);
+    mbar_init(smem_u32(&s.qready), 2);  // one thread per S-CTA
     if (rank >= 2 && w.npages > 0) {
       mbar_arrive_expect_tx(smem_u32(&s.fin_full), kRows * 4);
       // rank 2 also receives rank 1's 16 flag bytes per message

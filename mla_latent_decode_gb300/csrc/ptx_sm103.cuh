@@ -428,6 +428,17 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar,
       "h"(cta_mask)
       : "memory");
 }
+// Copy a 128-row x 256-bit matrix from shared memory (matrix descriptor
+// `desc`, the layout an MMA operand descriptor describes) into TMEM lanes
+// 0..127, columns [taddr.col, +8), in both CTAs of the pair, each from its own
+// shared memory at the same address.  Ordered before the issuing thread's
+// later tcgen05.mma; a later tcgen05.commit covers it.
+__device__ __forceinline__ void tmem_cp_128x256b_pair(uint32_t taddr,
+                                                      uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr),
+               "l"(desc)
+               : "memory");
+}
 // 2-D tiled TMA load into this CTA's shared memory whose bytes complete on a
 // barrier of either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
