@@ -17,8 +17,8 @@
 //     ranks 0,1, the "S pair": rank r owns row group 2u + r: Q_nope (bf16
 //       pairs) in TMEM columns [0, 256), Q_rope in shared memory, both
 //       brought by TMA (Q_nope through the P slots, idle until the first S
-//       tile), one S buffer of 256 columns (an S tile = 4 pages = 256
-//       tokens).  Rank r loads pages 2r, 2r+1 of every tile in 16-KB stages
+//       tile, and ring stages 4..7, then copied into TMEM by tcgen05.cp),
+//       one S buffer of 256 columns (an S tile = 4 pages = 256 tokens).  Rank r loads pages 2r, 2r+1 of every tile in 16-KB stages
 //       (one 64-dim chunk of its two pages, 128-byte swizzled TMA boxes);
 //       each stage feeds 4 pair MMAs of M=256, N=256, K=16 issued by rank
 //       0.  Two softmax
