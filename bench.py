@@ -134,17 +134,20 @@ def measured_peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash(fp8=False):
-    """Hash of the sources the BF16 (or FP8) tensor-core kernel compiles from."""
+def kernel_source_hash(fp8=False, kernel=None):
+    """Hash of the sources the BF16 (or FP8) tensor-core decode kernel
+    compiles from, or with kernel="projection" the per-head projection
+    kernel's."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_decode_gb300", "csrc")
-    for f in ("mla_tc_fp8.cu" if fp8 else "mla_tc.cu", "ptx_sm103.cuh",
-              "mla_tma.cuh", "mla_internal.h"):
+    main = ("mla_absorb.cu" if kernel == "projection"
+            else "mla_tc_fp8.cu" if fp8 else "mla_tc.cu")
+    for f in (main, "ptx_sm103.cuh", "mla_tma.cuh", "mla_internal.h"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_name, units, fp8=False):
+def profiled_traffic(config_name, units, fp8=False, kernel=None):
     """DRAM bytes per launch from a committed ncu summary, only if it was
     taken on the current source of the kernel the workload runs; scaled by
     units if captured smaller."""
@@ -153,7 +156,7 @@ def profiled_traffic(config_name, units, fp8=False):
     except Exception:
         return None
     e = d.get("workloads", {}).get(config_name)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash(fp8):
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(fp8, kernel):
         return None
     return e["dram_bytes_per_launch"] * units / e.get("units", units)
 
@@ -575,6 +578,9 @@ def run_projections(args):
     total_bytes = sum(v[2] for v in res.values())
     gbs = total_bytes / (total_us * 1e-6) / 1e9
     peak = float(peaks["hbm_gbs"])
+    # DRAM bytes of one projection pair (both launches), when profiled on
+    # the current kernel source
+    traffic = profiled_traffic(f"projections_{args.config}", 1, kernel="projection")
     print(json.dumps({
         "metric": "MLA per-head projections us/layer (mla_absorb_q + mla_project_out)",
         "value": total_us, "unit": "us", "n_gpus": 1, "steps": args.steps,
@@ -587,7 +593,7 @@ def run_projections(args):
                          "per projection, more than L2); launches replayed from a CUDA graph"},
         "ops": {k: {"us": v[0], "gbs": v[1], "bytes": v[2]} for k, v in res.items()},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": None,
+                     "frac": gbs / peak, "traffic": traffic,
                      "kernel": "mla_head_gemm_kernel",
                      "peak_kind": f"{kind} copy bandwidth"},
         "clocks": clk, "gpu_launches": 2 * R * args.steps}))
