@@ -73,6 +73,10 @@ def parse(argv=None):
     ap.add_argument("--projections", action="store_true",
                     help="time mla_absorb_q and mla_project_out at --config's "
                          "rows (B * q_len) and heads instead of the decode step")
+    ap.add_argument("--parts", choices=("f32", "bf16"), default="bf16",
+                    help="partial outputs between the two launches: bf16 "
+                         "(mla_decode_partial_bf16_parts; BF16 KV only, FP8 KV "
+                         "keeps fp32) or fp32")
     ap.add_argument("--fused", action="store_true",
                     help="time mla_decode (partial + combine in one launch) "
                          "instead of mla_decode_partial + mla_lse_combine")
@@ -305,6 +309,17 @@ def run_reference(args):
     return 0
 
 
+PARTS = {"dtype": "bf16"}  # the --parts choice, read by every step builder
+
+
+def part_dtype(wl):
+    """Element type of the partial outputs for workload wl: bf16 when asked
+    for and the KV is BF16 (the bf16-parts entry serves BF16 KV only)."""
+    import torch
+    return (torch.bfloat16 if PARTS["dtype"] == "bf16" and wl.kv_dtype == "bf16"
+            else torch.float32)
+
+
 def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
     """Median device time (ms) of one partial-decode + combine pair at S
     splits, CUDA events on the launching stream.  The steps are enqueued back
@@ -316,7 +331,7 @@ def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):
     dev = batch.q_nope.device
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
-                         dtype=torch.float32, device=dev)
+                         dtype=part_dtype(wl), device=dev)
     LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
                            dtype=torch.float32, device=dev)
     out = torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16, device=dev)
@@ -644,7 +659,7 @@ def time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
     d_sp = [torch.empty_like(h, device=dev) if h is not None else None for h in h_sp]
     d_wk = [torch.empty_like(h, device=dev) if h is not None else None for h in h_wk]
     O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
-                         dtype=torch.float32, device=dev)
+                         dtype=part_dtype(wl), device=dev)
     LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
                            dtype=torch.float32, device=dev)
     d_out = [torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16,
@@ -735,6 +750,7 @@ def time_e2e(mla, args, wl, batch, lens, S, split_pages, work, counters,
 
 def main():
     args = parse()
+    PARTS["dtype"] = args.parts
     if args.projections:
         return run_projections(args)
     if args.kv_write_rows > 0:
@@ -799,8 +815,10 @@ def main():
     S_pages = mla.plan_heuristic(wl.B, wl.q_len)
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the fused launch keeps fp32 parts (its merge reads them in the launch)
     O_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H, 512),
-                         dtype=torch.float32, device=dev)
+                         dtype=torch.float32 if args.fused else part_dtype(wl),
+                         device=dev)
     LSE_part = torch.empty((S, wl.num_shards, wl.B, wl.q_len, wl.H),
                            dtype=torch.float32, device=dev)
     out = torch.empty((wl.B, wl.q_len, wl.H, 512), dtype=torch.bfloat16, device=dev)
@@ -918,7 +936,10 @@ def main():
                 "parallelism": f"dp{world} (independent requests per rank)",
                 "step": ("mla_decode: partial decode and LSE combine fused in one launch"
                          if args.fused else
-                         "mla_decode_partial + mla_lse_combine (two launches)"),
+                         "mla_decode_partial + mla_lse_combine (two launches)"
+                         if part_dtype(wl) == torch.float32 else
+                         "mla_decode_partial_bf16_parts + mla_lse_combine_bf16_parts "
+                         "(two launches, bf16 partial outputs)"),
             },
             "us_per_layer": ms_per_step * 1e3,
             "partial_us": part_mean * 1e3,

@@ -342,6 +342,24 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
                        int* status, mla_stream_t stream);
 
 /*
+ * mla_decode_partial with bf16 partial outputs: the same computation and
+ * arguments, but O_part is bf16 [num_splits, num_shards, B, q_len, H, 512],
+ * 16-B aligned, each normalised value rounded to nearest even from fp32
+ * (the survey's A7 step allows a bf16 O_part; LSE_part stays fp32).  Half
+ * the bytes of the epilogue's stores and of the combine's reads; each part
+ * gains at most 2^-9 relative rounding before the merge.  BF16 KV only (FP8
+ * KV: MLA_ERR_UNSUPPORTED).  Merge with mla_lse_combine_bf16_parts.
+ */
+int mla_decode_partial_bf16_parts(
+    const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,
+    const float* kv_scale, mla_kv_dtype kv_dtype, int64_t num_slots,
+    const int32_t* req_to_token, int64_t r2t_stride, const int32_t* seq_lens,
+    const int32_t* kv_limit, int B, int q_len, int H, int num_shards,
+    int page_size, float sm_scale, int num_splits, const int32_t* split_pages,
+    const int32_t* work, int num_work, void* O_part, float* LSE_part,
+    int* status, mla_stream_t stream);
+
+/*
  * Whole decode in one launch ([K3-MLA]: the partial (O, LSE) per split and
  * shard, then dcp_lse_combine): mla_decode_partial followed by the
  * mla_lse_combine over its num_splits * num_shards parts, fused.  Each
@@ -492,6 +510,15 @@ int mla_decode_partial_simt(const void* q_nope_absorbed, const void* q_rope,
 int mla_lse_combine(const float* O_part, const float* LSE_part, int num_parts,
                     int64_t rows, void* out, float* lse_out,
                     mla_stream_t stream);
+
+/*
+ * The same merge over bf16 parts (O_part bf16 [num_parts, rows, 512], 16-B
+ * aligned, as mla_decode_partial_bf16_parts writes them), each value widened
+ * exactly to fp32 before the weighted sum.
+ */
+int mla_lse_combine_bf16_parts(const void* O_part, const float* LSE_part,
+                               int num_parts, int64_t rows, void* out,
+                               float* lse_out, mla_stream_t stream);
 
 /*
  * Page-table gather through the decode kernel's own TMA path (for the

@@ -70,6 +70,9 @@ def library() -> ctypes.CDLL:
             "mla_decode_partial": (i32, [p, p, p, p, i32, i64, p, i64, p, p, i32,
                                          i32, i32, i32, i32, f32, i32, p, p, i32,
                                          p, p, p, p]),
+            "mla_decode_partial_bf16_parts": (i32, [p, p, p, p, i32, i64, p, i64, p,
+                                                    p, i32, i32, i32, i32, i32, f32,
+                                                    i32, p, p, i32, p, p, p, p]),
             "mla_decode_partial_simt": (i32, [p, p, p, p, i32, i64, p, i64, p, p,
                                               i32, i32, i32, i32, i32, f32, i32, p,
                                               p, p, p, p]),
@@ -84,6 +87,7 @@ def library() -> ctypes.CDLL:
             "mla_absorb_q": (i32, [p, p, p, i32, i32, p, p]),
             "mla_project_out": (i32, [p, p, p, i32, i32, p, p]),
             "mla_lse_combine": (i32, [p, p, i32, i64, p, p, p]),
+            "mla_lse_combine_bf16_parts": (i32, [p, p, i32, i64, p, p, p]),
             "mla_debug_gather": (i32, [p, i32, i64, p, i64, p, p, i32, i32, p, p]),
             "mla_debug_wait": (i32, [i32, i32, p, p, p]),
             "mla_debug_quotients": (i32, [p, p, p]),
@@ -269,20 +273,23 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
                    kv_limit, num_splits: int, sm_scale: float,
                    num_shards: int = 1, O_part=None, LSE_part=None,
                    status=None, simt: bool = False, stream=None,
-                   split_pages=None, work=None):
+                   split_pages=None, work=None, part_dtype=None):
     """Partial (O, LSE) per split and shard; see mla_decode_partial.
     `split_pages`: device int32 [num_shards*B, num_splits+1] or None;
     `work`: device int32 unit ids in launch order (plan_sched) or None
-    (tensor-core path only).
+    (tensor-core path only).  A bf16 O_part (given, or part_dtype=
+    torch.bfloat16) calls mla_decode_partial_bf16_parts.
 
-    Returns (O_part fp32 [S, shards, B, q, H, 512], LSE_part fp32 [S, shards,
-    B, q, H]); outputs are allocated with torch unless given.
+    Returns (O_part [S, shards, B, q, H, 512], fp32 unless bf16 was asked
+    for, LSE_part fp32 [S, shards, B, q, H]); outputs are allocated with
+    torch unless given.
     """
     B, q_len, H, _ = q_nope.shape
     dev = q_nope.device
     if O_part is None:
         O_part = torch.empty((num_splits, num_shards, B, q_len, H, VALUE_DIM),
-                             dtype=torch.float32, device=dev)
+                             dtype=part_dtype or torch.float32, device=dev)
+    bf16_parts = O_part.dtype == torch.bfloat16
     if LSE_part is None:
         LSE_part = torch.empty((num_splits, num_shards, B, q_len, H),
                                dtype=torch.float32, device=dev)
@@ -294,12 +301,14 @@ def decode_partial(q_nope, q_rope, kv, kv_scale, req_to_token, seq_lens,
     with _on(q_nope):
         tail = (_ptr(O_part), _ptr(LSE_part), _ptr(status), _stream(stream))
         if simt:
-            if work is not None:
-                raise ValueError("the CUDA-core path takes no work list")
+            if work is not None or bf16_parts:
+                raise ValueError("the CUDA-core path takes no work list and "
+                                 "writes fp32 parts")
             _check(library().mla_decode_partial_simt(*args, *tail))
         else:
-            _check(library().mla_decode_partial(
-                *args, _ptr(work), 0 if work is None else work.numel(), *tail))
+            fn = (library().mla_decode_partial_bf16_parts if bf16_parts
+                  else library().mla_decode_partial)
+            _check(fn(*args, _ptr(work), 0 if work is None else work.numel(), *tail))
     return O_part, LSE_part
 
 
@@ -421,8 +430,10 @@ def lse_combine(O_part, LSE_part, out=None, lse_out=None, stream=None):
                           device=O_part.device)
     if lse_out is None:
         lse_out = torch.empty(row_shape, dtype=torch.float32, device=O_part.device)
-    _check(library().mla_lse_combine(_ptr(O_part), _ptr(LSE_part), parts, rows,
-                                     _ptr(out), _ptr(lse_out), _stream(stream)))
+    fn = (library().mla_lse_combine_bf16_parts if O_part.dtype == torch.bfloat16
+          else library().mla_lse_combine)
+    _check(fn(_ptr(O_part), _ptr(LSE_part), parts, rows, _ptr(out), _ptr(lse_out),
+              _stream(stream)))
     return out, lse_out
 
 

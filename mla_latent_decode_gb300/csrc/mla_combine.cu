@@ -13,13 +13,15 @@
 
 namespace {
 
+using namespace mla;
+
 constexpr int kWarpsPerBlock = 8;
 
 // kWs warps per row (column slices of 512 / kWs values): with few rows the
 // merge is latency-bound, and more warps keep more loads in flight.
-template <int kWs>
+template <int kWs, typename PartT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    mla_lse_combine_kernel(const float* __restrict__ O_part,
+    mla_lse_combine_kernel(const PartT* __restrict__ O_part,
                            const float* __restrict__ LSE_part, int P,
                            int64_t rows, __nv_bfloat16* __restrict__ out,
                            float* __restrict__ lse_out) {
@@ -31,8 +33,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
   const int64_t row = gw / kWs;
   if (row >= rows) return;
-  mla::combine_row<false, kWs>(O_part, LSE_part, P, rows, row, out, lse_out,
-                               lane, (int)(gw % kWs));
+  mla::combine_row<false, kWs, PartT>(O_part, LSE_part, P, rows, row, out,
+                                      lse_out, lane, (int)(gw % kWs));
 }
 
 // Warps per row for a merge of `rows` rows: as many (up to four) as keep the
@@ -42,13 +44,9 @@ int warps_per_row(int64_t rows) {
   return rows * 4 <= 8192 ? 4 : (rows * 2 <= 8192 ? 2 : 1);
 }
 
-}  // namespace
-
-using namespace mla;
-
-extern "C" int mla_lse_combine(const float* O_part, const float* LSE_part,
-                               int num_parts, int64_t rows, void* out,
-                               float* lse_out, mla_stream_t stream) {
+template <typename PartT>
+int launch_combine(const PartT* O_part, const float* LSE_part, int num_parts,
+                   int64_t rows, void* out, float* lse_out, mla_stream_t stream) {
   if (!O_part || !LSE_part || !out)
     return fail(MLA_ERR_INVALID_ARG, "O_part, LSE_part and out are required");
   if (num_parts < 1 || rows < 1)
@@ -76,13 +74,31 @@ extern "C" int mla_lse_combine(const float* O_part, const float* LSE_part,
   cfg.numAttrs = 1;
   __nv_bfloat16* const o = static_cast<__nv_bfloat16*>(out);
   cudaError_t e =
-      ws == 4 ? cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<4>, O_part,
+      ws == 4 ? cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<4, PartT>, O_part,
                                    LSE_part, num_parts, rows, o, lse_out)
-      : ws == 2 ? cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<2>, O_part,
+      : ws == 2 ? cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<2, PartT>, O_part,
                                      LSE_part, num_parts, rows, o, lse_out)
-                : cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<1>, O_part,
+                : cudaLaunchKernelEx(&cfg, mla_lse_combine_kernel<1, PartT>, O_part,
                                      LSE_part, num_parts, rows, o, lse_out);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch mla_lse_combine_kernel");
   return MLA_OK;
+}
+
+}  // namespace
+
+using namespace mla;
+
+extern "C" int mla_lse_combine(const float* O_part, const float* LSE_part,
+                               int num_parts, int64_t rows, void* out,
+                               float* lse_out, mla_stream_t stream) {
+  return launch_combine(O_part, LSE_part, num_parts, rows, out, lse_out, stream);
+}
+
+extern "C" int mla_lse_combine_bf16_parts(const void* O_part,
+                                          const float* LSE_part, int num_parts,
+                                          int64_t rows, void* out,
+                                          float* lse_out, mla_stream_t stream) {
+  return launch_combine(static_cast<const __nv_bfloat16*>(O_part), LSE_part,
+                        num_parts, rows, out, lse_out, stream);
 }

@@ -35,13 +35,28 @@ __device__ __forceinline__ float4 load_part4(const float4* p) {
   return kCoherent ? __ldcg(p) : __ldg(p);
 }
 
+// Four consecutive values of a part row as fp32: one 16-byte load of fp32
+// parts or one 8-byte load of bf16 parts (widened exactly).  `c4` counts
+// groups of four values from `row`.
+template <bool kCoherent>
+__device__ __forceinline__ float4 load_four(const float* row, int c4) {
+  return load_part4<kCoherent>(reinterpret_cast<const float4*>(row) + c4);
+}
+template <bool kCoherent>
+__device__ __forceinline__ float4 load_four(const __nv_bfloat16* row, int c4) {
+  const uint2* q = reinterpret_cast<const uint2*>(row) + c4;
+  const uint2 u = kCoherent ? __ldcg(q) : __ldg(q);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
 // kWs warps share a row: warp `slice` of them owns value columns
 // [slice * 512 / kWs, +512 / kWs), each lane kF4 = 4 / kWs float4 columns of
 // every part, with kPar = 8 / kF4 parts' loads in flight at a time (eight
 // float4 loads per lane whatever kWs).  Every warp of the row computes the
 // weights itself; slice 0 writes lse_out.
-template <bool kCoherent, int kWs = 1>
-__device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
+template <bool kCoherent, int kWs = 1, typename PartT = float>
+__device__ __forceinline__ void combine_row(const PartT* __restrict__ O_part,
                                             const float* __restrict__ LSE_part,
                                             int P, int64_t rows, int64_t row,
                                             __nv_bfloat16* __restrict__ out,
@@ -98,11 +113,11 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ O_part,
 #pragma unroll
         for (int q = 0; q < kPar; ++q) {
           w[q] = t + q < n ? __shfl_sync(kAll, wl, t + q) : 0.f;
-          const float4* src = reinterpret_cast<const float4*>(
-              O_part + ((int64_t)(j0 + t + q) * rows + row) * MLA_VALUE_DIM);
+          const PartT* src =
+              O_part + ((int64_t)(j0 + t + q) * rows + row) * MLA_VALUE_DIM;
 #pragma unroll
           for (int k = 0; k < kF4; ++k)
-            x[q][k] = w[q] != 0.f ? load_part4<kCoherent>(src + col(k))
+            x[q][k] = w[q] != 0.f ? load_four<kCoherent>(src, col(k))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll

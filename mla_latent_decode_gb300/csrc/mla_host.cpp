@@ -596,6 +596,32 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
   return launch_tc(a);
 }
 
+int mla_decode_partial_bf16_parts(
+    const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,
+    const float* kv_scale, mla_kv_dtype kv_dtype, int64_t num_slots,
+    const int32_t* req_to_token, int64_t r2t_stride, const int32_t* seq_lens,
+    const int32_t* kv_limit, int B, int q_len, int H, int num_shards,
+    int page_size, float sm_scale, int num_splits, const int32_t* split_pages,
+    const int32_t* work, int num_work, void* O_part, float* LSE_part,
+    int* status, mla_stream_t stream) {
+  DecodeArgs a{q_nope_absorbed, q_rope,    kv_pages, kv_scale,  kv_dtype,
+               num_slots,       req_to_token, r2t_stride, seq_lens, kv_limit,
+               B,               q_len,     H,        num_shards, page_size,
+               sm_scale,        num_splits, split_pages,
+               static_cast<float*>(O_part), LSE_part, status,
+               (cudaStream_t)stream};
+  a.work = work;
+  a.num_work = num_work;
+  a.o_bf16 = 1;
+  int rc = check_decode_args(a);
+  if (rc != MLA_OK) return rc;
+  rc = check_work(a);
+  if (rc != MLA_OK) return rc;
+  if (kv_dtype != MLA_KV_BF16)
+    return fail(MLA_ERR_UNSUPPORTED, "bf16 partial outputs: BF16 KV only");
+  return launch_tc(a);
+}
+
 int mla_decode(const void* q_nope_absorbed, const void* q_rope,
                const void* kv_pages, const float* kv_scale,
                mla_kv_dtype kv_dtype, int64_t num_slots,

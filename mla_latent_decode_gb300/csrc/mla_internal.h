@@ -59,6 +59,8 @@ struct DecodeArgs {
   // increasing ids; num_work = V * num_splits * U (checked by check_work).
   const int32_t* work = nullptr;
   int num_work = 0;
+  // O_part holds bf16 values (same element layout) instead of fp32.
+  int o_bf16 = 0;
 };
 
 // Pages [p0, p1) of split s of a request with P pages.  With a split table

@@ -134,6 +134,7 @@ struct TcParams {
   int* status;
   int q_box_rows;          // rows of a query TMA box: min(128, B * q_len * H)
   int o_tma;               // O_part rows leave by TMA store (o_map is valid)
+  int o_bf16;              // O_part holds bf16 values (else fp32)
   __nv_bfloat16* out;      // fused combine (NULL counters: partials only)
   float* lse_out;
   int* counters;
@@ -934,6 +935,53 @@ __device__ __forceinline__ void store_o_rows(Smem& s, const TcParams& p,
       part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + quad * 32;
   float* const dst0 = p.O_part + row0 * MLA_VALUE_DIM;
   const int nvalid = w.nrows - quad * 32;  // rows of this warp in range
+  if (p.o_bf16) {
+    // bf16 partial outputs: 64 values (128 bytes) per row of a box, four
+    // boxes per warp and half, box k stored by lane k; a partial 32-row
+    // block is written by its lanes directly (64 bytes per row and step).
+    __nv_bfloat16* const dst_b =
+        reinterpret_cast<__nv_bfloat16*>(p.O_part) + row0 * MLA_VALUE_DIM;
+    uint8_t* const bufs = s.ring[2 * (warp - 4)];
+    const bool by_tma = p.o_tma && nvalid >= 32;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      const int c0 = 256 * half + 64 * k;
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem + lane_base + c0, va);
+      tmem_ld32(tmem + lane_base + c0 + 32, vb);
+      tmem_wait_ld();
+      uint4 q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t* v = e < 4 ? va + 8 * e : vb + 8 * (e - 4);
+        q[e] = make_uint4(pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                          pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                          pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                          pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+      }
+      if (by_tma) {
+        uint8_t* const box = bufs + k * 4096;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(box + box_chunk_offset(lane, e)) = q[e];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == k) {
+          tma_store_3d(o_map, smem_u32(box), c0, (int32_t)row0, 0);
+          bulk_commit_group();
+        }
+      } else if (lane < nvalid) {
+        uint4* d = reinterpret_cast<uint4*>(dst_b + (int64_t)lane * MLA_VALUE_DIM + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[e] = q[e];
+      }
+    }
+    if (by_tma) {
+      if (lane < 4) bulk_wait_read_all();
+      __syncwarp();
+    }
+    return;
+  }
   if (p.o_tma && nvalid >= 32) {
     // Whole 32-row blocks leave by TMA store, 32 values (128 bytes) per
     // box: four boxes of this warp's 16 KB of the idle ring in turn, box i
@@ -1236,6 +1284,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
           part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r;
       if (rank < 2) {
         p.LSE_part[orow] = -INFINITY;
+      } else if (p.o_bf16) {
+        uint4* d = reinterpret_cast<uint4*>(
+            reinterpret_cast<__nv_bfloat16*>(p.O_part) + orow * MLA_VALUE_DIM);
+        for (int e = 0; e < MLA_VALUE_DIM / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
       } else {
         float4* d4 = reinterpret_cast<float4*>(p.O_part + orow * MLA_VALUE_DIM);
         for (int e = 0; e < MLA_VALUE_DIM / 4; ++e)
@@ -1289,8 +1341,19 @@ int launch_tc(const DecodeArgs& a) {
   std::memset(&o_map, 0, sizeof(o_map));
   const int64_t o_rows =
       (int64_t)p.num_splits * a.num_shards * a.B * a.q_len * a.H;
-  p.o_tma = !p.counters && o_rows < 0x7fffffff &&
-            make_o_part_map(&o_map, p.O_part, o_rows) == MLA_OK;
+  p.o_bf16 = a.o_bf16;
+  if (p.o_bf16) {
+    const uint64_t dims[3] = {(uint64_t)MLA_VALUE_DIM, (uint64_t)o_rows, 1};
+    const uint64_t strides[2] = {(uint64_t)MLA_VALUE_DIM * 2,
+                                 (uint64_t)o_rows * MLA_VALUE_DIM * 2};
+    const uint32_t box[3] = {64, 32, 1};
+    p.o_tma = !p.counters && o_rows < 0x7fffffff &&
+              make_tensor_map_bf16_3d(&o_map, p.O_part, dims, strides, box) ==
+                  MLA_OK;
+  } else {
+    p.o_tma = !p.counters && o_rows < 0x7fffffff &&
+              make_o_part_map(&o_map, p.O_part, o_rows) == MLA_OK;
+  }
   cudaError_t e = cudaFuncSetAttribute(
       mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       kSmemBytes);
