@@ -115,3 +115,27 @@ def test_bf16_parts_reject_fp8_kv():
     batch = synth.make_batch(wl, seed=54, device="cuda")
     with pytest.raises(mla.MlaError):
         mla.decode_partial(*_args(batch, 2), part_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("P,rows", [(7, 1000), (40, 300), (3, 20000)])
+def test_bf16_combine_matches_oracle_and_widened_fp32_merge(P, rows):
+    """The bf16 merge over more than 32 parts (two rounds of LSE loads) and
+    over many rows (one warp per row), with empty parts and all-empty rows:
+    bitwise the fp32 merge of the widened parts, and within one bf16
+    rounding of the fp64 merge of those parts."""
+    import oracle
+    g = torch.Generator(device="cuda").manual_seed(P + rows)
+    O = torch.randn((P, rows, 512), generator=g, device="cuda").to(torch.bfloat16)
+    L = torch.randn((P, rows), generator=g, device="cuda") * 3
+    L[P // 2, :100] = -float("inf")   # empty parts
+    L[:, 100:110] = -float("inf")     # all parts empty
+    out, lse = mla.lse_combine(O, L)
+    out_w, lse_w = mla.lse_combine(O.float(), L)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_w) and torch.equal(lse, lse_w)
+    O_ref, l_ref = oracle.lse_combine(f64(O), f64(L))
+    got = f64(out)
+    assert np.array_equal(got[100:110], np.zeros((10, 512)))
+    assert np.isneginf(f64(lse)[100:110]).all()
+    np.testing.assert_allclose(got, O_ref, rtol=2 ** -8, atol=1e-6)
+    np.testing.assert_allclose(f64(lse), l_ref, rtol=0, atol=1e-5)
