@@ -75,8 +75,7 @@ def parse(argv=None):
                          "rows (B * q_len) and heads instead of the decode step")
     ap.add_argument("--parts", choices=("f32", "bf16"), default="bf16",
                     help="partial outputs between the two launches: bf16 "
-                         "(mla_decode_partial_bf16_parts; BF16 KV only, FP8 KV "
-                         "keeps fp32) or fp32")
+                         "(mla_decode_partial_bf16_parts) or fp32")
     ap.add_argument("--fused", action="store_true",
                     help="time mla_decode (partial + combine in one launch) "
                          "instead of mla_decode_partial + mla_lse_combine")
@@ -313,11 +312,9 @@ PARTS = {"dtype": "bf16"}  # the --parts choice, read by every step builder
 
 
 def part_dtype(wl):
-    """Element type of the partial outputs for workload wl: bf16 when asked
-    for and the KV is BF16 (the bf16-parts entry serves BF16 KV only)."""
+    """Element type of the partial outputs (the --parts choice)."""
     import torch
-    return (torch.bfloat16 if PARTS["dtype"] == "bf16" and wl.kv_dtype == "bf16"
-            else torch.float32)
+    return torch.bfloat16 if PARTS["dtype"] == "bf16" else torch.float32
 
 
 def time_pair(mla, batch, wl, S, iters, warmup=3, split_pages=None, work=None):

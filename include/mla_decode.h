@@ -347,8 +347,8 @@ int mla_decode_partial(const void* q_nope_absorbed, const void* q_rope,
  * 16-B aligned, each normalised value rounded to nearest even from fp32
  * (the survey's A7 step allows a bf16 O_part; LSE_part stays fp32).  Half
  * the bytes of the epilogue's stores and of the combine's reads; each part
- * gains at most 2^-9 relative rounding before the merge.  BF16 KV only (FP8
- * KV: MLA_ERR_UNSUPPORTED).  Merge with mla_lse_combine_bf16_parts.
+ * gains at most 2^-9 relative rounding before the merge.  BF16 and FP8 KV
+ * (tensor-core kernels).  Merge with mla_lse_combine_bf16_parts.
  */
 int mla_decode_partial_bf16_parts(
     const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,

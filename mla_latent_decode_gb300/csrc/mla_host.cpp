@@ -617,8 +617,6 @@ int mla_decode_partial_bf16_parts(
   if (rc != MLA_OK) return rc;
   rc = check_work(a);
   if (rc != MLA_OK) return rc;
-  if (kv_dtype != MLA_KV_BF16)
-    return fail(MLA_ERR_UNSUPPORTED, "bf16 partial outputs: BF16 KV only");
   return launch_tc(a);
 }
 

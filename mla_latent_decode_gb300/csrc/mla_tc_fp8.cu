@@ -162,7 +162,8 @@ struct TcParams {
   int units;                   // V * num_splits * G
   int B, q_len, H, V, num_splits, G;
   float scale_log2;        // sm_scale * log2(e)
-  float* O_part;
+  float* O_part;           // fp32, or bf16 when o_bf16
+  int o_bf16;
   float* LSE_part;
   int* status;
   int q_box_rows;          // rows of a query TMA box: min(128, B * q_len * H)
@@ -1407,6 +1408,44 @@ __device__ __forceinline__ void correct_and_store(Smem& s, const TcParams& p,
                                   w.r_base + quad * 32) * MLA_VALUE_DIM;
   const int nvalid = w.nrows - quad * 32;  // rows of this warp in range
   uint8_t* const buf = s.ring[0] + 4096 * quad;
+  if (p.o_bf16) {
+    // bf16 partial outputs: 64 values (128 bytes) per staged row, the same
+    // staging and full-line stores.
+    __nv_bfloat16* const dst_b =
+        reinterpret_cast<__nv_bfloat16*>(p.O_part) +
+        (part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + quad * 32) *
+            MLA_VALUE_DIM;
+#pragma unroll 1
+    for (int c0 = 0; c0 < MLA_VALUE_DIM; c0 += 64) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem + lane_base + c0, va);
+      tmem_ld32(tmem + lane_base + c0 + 32, vb);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t* v = e < 4 ? va + 8 * e : vb + 8 * (e - 4);
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * j]) * inv,
+                                                   __uint_as_float(v[2 * j + 1]) * inv);
+          q[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(buf + box_chunk_offset(lane, e)) =
+            make_uint4(q[0], q[1], q[2], q[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3), e = lane & 7;
+        const uint4 f = *reinterpret_cast<const uint4*>(buf + box_chunk_offset(rr, e));
+        if (rr < nvalid)
+          *reinterpret_cast<uint4*>(dst_b + (int64_t)rr * MLA_VALUE_DIM + c0 + 8 * e) = f;
+      }
+      __syncwarp();  // every lane read the box before it is refilled
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c0 = 0; c0 < MLA_VALUE_DIM; c0 += 32) {
     uint32_t v[32];
@@ -1604,6 +1643,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           part * rows + (int64_t)w.b * p.q_len * p.H + w.r_base + r;
       if (rank == 0) {
         p.LSE_part[orow] = -INFINITY;
+      } else if (p.o_bf16) {
+        uint4* d = reinterpret_cast<uint4*>(
+            reinterpret_cast<__nv_bfloat16*>(p.O_part) + orow * MLA_VALUE_DIM);
+        for (int e = 0; e < MLA_VALUE_DIM / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
       } else {
         float4* d4 = reinterpret_cast<float4*>(p.O_part + orow * MLA_VALUE_DIM);
         for (int e = 0; e < MLA_VALUE_DIM / 4; ++e)
@@ -1636,6 +1679,7 @@ int launch_tc_fp8(const DecodeArgs& a) {
   p.G = (a.q_len * a.H + kRows - 1) / kRows;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
   p.O_part = a.O_part;
+  p.o_bf16 = a.o_bf16;
   p.LSE_part = a.LSE_part;
   p.status = a.status;
   p.out = static_cast<__nv_bfloat16*>(a.out);

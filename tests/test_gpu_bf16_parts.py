@@ -1,5 +1,5 @@
 """GPU checks of the bf16 partial outputs (mla_decode_partial_bf16_parts and
-mla_lse_combine_bf16_parts).
+mla_lse_combine_bf16_parts), BF16 and FP8 KV.
 
 Each part is the fp32 path's normalised O rounded once to bf16, so:
 - every part matches the oracle's part under the BF16 tolerances;
@@ -110,11 +110,38 @@ def test_bf16_parts_empty_splits_are_zero():
     assert torch.equal(O_part, O_f.to(torch.bfloat16))
 
 
-def test_bf16_parts_reject_fp8_kv():
-    wl = synth.Workload("f", 1, 5, 96, [300], kv_dtype="fp8_e4m3")
+FP8_CASES = [
+    ("fp8_small", synth.Workload("f8", 3, 5, 96, [1000, 257, 5], kv_dtype="fp8_e4m3")),
+    ("fp8_rows_700_q7", synth.Workload("f87", 2, 7, 100, [900, 450], kv_dtype="fp8_e4m3")),
+    ("fp8_sharded", synth.Workload("f8d", 3, 5, 96, [517, 64, 9], num_shards=8,
+                                   kv_dtype="fp8_e4m3")),
+]
+
+
+@pytest.mark.parametrize("name,wl", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+def test_bf16_parts_fp8_kv(name, wl):
+    """The FP8 kernel's bf16 parts: the fp32 parts rounded once, the LSE
+    parts bit for bit, and the merge within the FP8 tolerances."""
     batch = synth.make_batch(wl, seed=54, device="cuda")
-    with pytest.raises(mla.MlaError):
-        mla.decode_partial(*_args(batch, 2), part_dtype=torch.bfloat16)
+    S, sp, wk = _plan(batch)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Ob, Lb = mla.decode_partial(*_args(batch, S), num_shards=wl.num_shards,
+                                status=st, split_pages=sp, work=wk,
+                                part_dtype=torch.bfloat16)
+    Of, Lf = mla.decode_partial(*_args(batch, S), num_shards=wl.num_shards,
+                                status=st, split_pages=sp, work=wk)
+    out_b, lse_b = mla.lse_combine(Ob, Lb)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(Ob, Of.to(torch.bfloat16)), name
+    assert torch.equal(Lb, Lf), name
+    if wl.num_shards == 1:
+        O_ref, l_ref = oracle_rows(batch, synth.host_bits(batch), None)
+    else:
+        host, Bq = compact_unsharded(batch, list(range(wl.B)))
+        O_ref, l_ref = oracle_rows_host(host, Bq, wl, True, None)
+    check_close(f64(out_b).reshape(-1, 512), f64(lse_b).reshape(-1), O_ref, l_ref,
+                "fp8_e4m3", name)
 
 
 @pytest.mark.parametrize("P,rows", [(7, 1000), (40, 300), (3, 20000)])
