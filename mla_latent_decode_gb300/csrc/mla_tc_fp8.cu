@@ -796,15 +796,16 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
                          : zero4;
   };
 
-  // This warpgroup's dims of row r: chunks 32g .. 32g + 31 of the c_kv dims
-  // (g < 2) or the 8 chunks of RoPE dims (g == 2); 16-byte chunk k, dims
-  // dim0(k) .. dim0(k) + 7.
-  const int nchunks = g < 2 ? 32 : (g == 2 ? 8 : 0);
+  // This warpgroup's dims of row r, a quarter of the 576: c_kv chunks
+  // 16g .. 16g + 15 (dims 128g .. 128g + 127) and RoPE chunks 2g, 2g + 1
+  // (dims 512 + 16g ..); its 16-byte chunk k (0..17) holds dims dim0(k) ..
+  // dim0(k) + 7.
+  constexpr int nchunks = 18;
   auto my_chunk = [&](int k) -> uint4 {
-    return g < 2 ? qchunk(32 * g + k) : qrope_chunk(k);
+    return k < 16 ? qchunk(16 * g + k) : qrope_chunk(2 * g + k - 16);
   };
   auto dim0 = [&](int k) -> int {
-    return g < 2 ? 8 * (32 * g + k) : MLA_NOPE_DIM + 8 * k;
+    return k < 16 ? 8 * (16 * g + k) : MLA_NOPE_DIM + 8 * (2 * g + k - 16);
   };
   // Row statistics from the warpgroups' parts: largest |q| and sum of |q|.
   float amax = 0.f, asum = 0.f;
@@ -861,7 +862,7 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
       m = fmaxf(m, absmax_bf16x8(drop_channels(my_chunk(k), dim0(k), tab, ntab)));
     for (int t = 0; t < ntab; ++t) {
       const int d = tab[t];
-      const int owner = d < MLA_NOPE_DIM ? d >> 8 : 2;
+      const int owner = d < MLA_NOPE_DIM ? d >> 7 : (d - MLA_NOPE_DIM) >> 4;
       if (owner == g) {
         const uint4 x = d < MLA_NOPE_DIM ? qchunk(d >> 3) : qrope_chunk((d - MLA_NOPE_DIM) >> 3);
         s.xe[r][t] = (uint16_t)bf16_bits_of(x, d & 7);
@@ -878,46 +879,44 @@ __device__ __forceinline__ void softmax(Smem& s, const TcParams& p,
   const int64_t nA = visible_count(p, w, rA), nB = visible_count(p, w, rB);
 
   // Qhi / Qlo: c_kv dims -> TMEM columns [0, 128) and [128, 256) (column c
-  // holds elements 4c..4c+3; warpgroup g < 2 writes dims 256g .. 256g + 255,
+  // holds elements 4c..4c+3; warpgroup g writes dims 128g .. 128g + 127,
   // 64 dims = 16 columns per step), RoPE dims -> shared memory, K-major rows
-  // of 64 bytes with the 64-byte swizzle.
-  if (g < 2) {
+  // of 64 bytes with the 64-byte swizzle (warpgroup g: elements 16g ..
+  // 16g + 15).  The four warpgroups share the work evenly.
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t vh[16], vl[16];
+  for (int c = 0; c < 2; ++c) {
+    uint32_t vh[16], vl[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint2 h, l;
-        uint4 x = qchunk(32 * g + 8 * c + k);
-        if (ntab > 0) x = drop_channels(x, 8 * (32 * g + 8 * c + k), tab, ntab);
-        split_q8(x, inv, h, l);
-        vh[2 * k] = h.x;
-        vh[2 * k + 1] = h.y;
-        vl[2 * k] = l.x;
-        vl[2 * k + 1] = l.y;
-      }
-      tmem_st16(tmem + lane_base + 64u * g + 16u * c, vh);
-      tmem_st16(tmem + lane_base + kQLoCol + 64u * g + 16u * c, vl);
+    for (int k = 0; k < 8; ++k) {
+      uint2 h, l;
+      uint4 x = qchunk(16 * g + 8 * c + k);
+      if (ntab > 0) x = drop_channels(x, 8 * (16 * g + 8 * c + k), tab, ntab);
+      split_q8(x, inv, h, l);
+      vh[2 * k] = h.x;
+      vh[2 * k + 1] = h.y;
+      vl[2 * k] = l.x;
+      vl[2 * k + 1] = l.y;
     }
-    tmem_wait_st();
-  } else if (g == 2) {
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk cc = elements 16cc..16cc+15
-      uint2 h0, l0, h1, l1;
-      uint4 x0 = qrope_chunk(2 * cc), x1 = qrope_chunk(2 * cc + 1);
-      if (ntab > 0) {
-        x0 = drop_channels(x0, MLA_NOPE_DIM + 16 * cc, tab, ntab);
-        x1 = drop_channels(x1, MLA_NOPE_DIM + 16 * cc + 8, tab, ntab);
-      }
-      split_q8(x0, inv, h0, l0);
-      split_q8(x1, inv, h1, l1);
-      const uint32_t off = (r >> 3) * 512 + (r & 7) * 64 +
-                           (((cc ^ (r >> 1)) & 3) << 4);
-      *reinterpret_cast<uint4*>(s.qrope[0] + off) = make_uint4(h0.x, h0.y, h1.x, h1.y);
-      *reinterpret_cast<uint4*>(s.qrope[1] + off) = make_uint4(l0.x, l0.y, l1.x, l1.y);
-    }
-    fence_proxy_async_smem();
+    tmem_st16(tmem + lane_base + 32u * g + 16u * c, vh);
+    tmem_st16(tmem + lane_base + kQLoCol + 32u * g + 16u * c, vl);
   }
+  {
+    const int cc = g;  // 16-byte chunk cc = elements 16cc..16cc+15
+    uint2 h0, l0, h1, l1;
+    uint4 x0 = qrope_chunk(2 * cc), x1 = qrope_chunk(2 * cc + 1);
+    if (ntab > 0) {
+      x0 = drop_channels(x0, MLA_NOPE_DIM + 16 * cc, tab, ntab);
+      x1 = drop_channels(x1, MLA_NOPE_DIM + 16 * cc + 8, tab, ntab);
+    }
+    split_q8(x0, inv, h0, l0);
+    split_q8(x1, inv, h1, l1);
+    const uint32_t off = (r >> 3) * 512 + (r & 7) * 64 +
+                         (((cc ^ (r >> 1)) & 3) << 4);
+    *reinterpret_cast<uint4*>(s.qrope[0] + off) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+    *reinterpret_cast<uint4*>(s.qrope[1] + off) = make_uint4(l0.x, l0.y, l1.x, l1.y);
+  }
+  tmem_wait_st();
+  fence_proxy_async_smem();
   if (!__all_sync(kFull, qok) && lane == 0) signal_abort(s, p, rank);
   tc_fence_before();
   __syncwarp();
