@@ -823,7 +823,7 @@ def main():
     stream = torch.cuda.current_stream()
     counters = mla.fused_counters(wl.B, wl.q_len, wl.H, dev)
 
-    def step(ev=None):
+    def step(ev=None, mid=True):
         if args.fused:
             if ev is not None:
                 ev[0].record(stream)
@@ -842,7 +842,7 @@ def main():
                            batch.req_to_token, batch.seq_lens, batch.kv_limit, S,
                            wl.sm_scale, wl.num_shards, O_part, LSE_part, status,
                            split_pages=split_pages, work=work)
-        if ev is not None:
+        if ev is not None and mid:
             ev[1].record(stream)
         mla.lse_combine(O_part, LSE_part, out, lse)
         if ev is not None:
@@ -870,23 +870,35 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.1)  # let the sampler take its first reading
+    # The steps as a caller runs them: an event between the two launches
+    # would stop the combine's programmatic overlap with the partial decode's
+    # tail (~4 us per step), so these steps carry events around the step only.
     t_start.record(stream)
     for k in range(args.steps):
         if flush:
             flush_buf.fill_(k & 0xFF)
-        step(evs[k])
+        step(evs[k], mid=False)
     t_end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    if flush:  # time the steps only, not the flushes between them
+        total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
+    # The same K steps again with an event between the launches: the partial
+    # decode's own duration (the roofline's) and the combine's.
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(args.steps)]
+    for k in range(args.steps):
+        if flush:
+            flush_buf.fill_(k & 0xFF)
+        step(evk[k])
     torch.cuda.synchronize()
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    part_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    part_ms = [e[0].elapsed_time(e[1]) for e in evk]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in evk]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in timed region")
-    if flush:  # time the steps only, not the flushes between them
-        total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
     total_ms = slowest_rank(total_ms, dist, dev)
     fl = wl.flops()
     ms_per_step = total_ms / args.steps
@@ -931,6 +943,9 @@ def main():
                 "l2": (f"KV {kv_bytes / 1e6:.1f} MB < 2 x L2: 256-MB L2 flush between timed steps, value from per-step event spans"
                        if flush else f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB KV), no flush"),
                 "parallelism": f"dp{world} (independent requests per rank)",
+                "timing": ("value from K steps with events around each step only; "
+                           "partial_us, combine_us and the roofline from a second "
+                           "pass of K steps with an event between the two launches"),
                 "step": ("mla_decode: partial decode and LSE combine fused in one launch"
                          if args.fused else
                          "mla_decode_partial + mla_lse_combine (two launches)"
