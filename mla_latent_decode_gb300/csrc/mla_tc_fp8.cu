@@ -435,6 +435,19 @@ __device__ __forceinline__ int32_t page_base(const TcParams& p, const Work& w,
   return base;
 }
 
+// Start the 2-D box at (x, y) of a tensor on its way into L2, and a plain
+// range of `bytes` (a multiple of 16, 16-byte aligned): no shared memory is
+// written and nothing waits for them.
+__device__ __forceinline__ void prefetch_box_l2(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_bytes_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes)
+               : "memory");
+}
+
 // ------------------------------------------------------------ producers ---
 // S-CTA: per S tile (up to 4 pages) the pages' 64 scales each into
 // tscale[j % 4] by bulk copy (zeros, written here, for a page outside the
@@ -449,6 +462,19 @@ __device__ __forceinline__ void producer_s(Smem& s, const CUtensorMap* map,
   uint32_t stage = 0, phase = 0;
   int32_t cur = page_base(p, w, lane), nxt = page_base(p, w, 32 + lane);
   bool ok = true;
+  // While the softmax warps prepare the query, the first tile's K boxes and
+  // scales are pulled into L2 (lane l: page l), so their loads after qready
+  // find them there.
+  if (lane < min(kTilePages, w.npages) && cur >= 0) {
+#pragma unroll 1
+    for (int c = 0; c < kBlocksPerTile; ++c) {
+      if (c == kBlocksPerTile - 1)
+        prefetch_box_l2(map_rope, MLA_NOPE_DIM, cur);
+      else
+        prefetch_box_l2(map, 128 * c, cur);
+    }
+    prefetch_bytes_l2(p.kv_scale + cur, kPage * 4);
+  }
   // The ring holds the query rows until every softmax warp has moved them.
   if (lane == 0 && !mbar_wait(smem_u32(&s.qready), 0, &s.abort_flag)) ok = false;
   ok = __shfl_sync(kFull, ok, 0);
